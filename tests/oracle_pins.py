@@ -1,0 +1,372 @@
+"""Pins that tie the oracle to facts outside itself.
+
+Each pin takes a loaded oracle library (ctypes) and raises AssertionError if
+the oracle disagrees with what the pages or the mathematics fix.  They are
+kept as plain functions so that ``test_oracle_pins.py`` can run them against
+the real oracle and ``test_oracle_mutants.py`` can run them against builds
+of the oracle with a deliberately planted mistake (every mutant must fail at
+least one pin).
+
+What each pin checks against:
+  * format pins        -- values fixed by IEEE 754 binary16 and by the
+                          bfloat16 definition; numpy/torch conversions.
+  * brute-force pins   -- numpy's int64 matmul of the logical matrices on
+                          16x8x16 and 16x16x16 tiles (the m16n8k16 and WMMA
+                          16x16x16 shapes), all four storage orders.
+  * closed forms       -- identity, all-ones (= K), rank one.
+  * layout pin         -- the 2x3 example of the pages (tests/golden).
+  * epilogue pins      -- alpha/beta on integer data against numpy; beta == 0
+                          never reads C.
+"""
+from __future__ import annotations
+
+import json
+import math
+import os
+
+import numpy as np
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+F16_ONE, BF16_ONE = 0x3C00, 0x3F80
+
+
+def _f16_bits(x) -> np.ndarray:
+    """numpy's own binary16 conversion (independent of the oracle's encoder)."""
+    with np.errstate(over="ignore"):
+        return np.asarray(x, dtype=np.float64).astype(np.float16).view(np.uint16)
+
+
+def _bf16_bits(x) -> np.ndarray:
+    """torch's float32 -> bfloat16 conversion (exact for the small integers
+    and short fractions the pins use)."""
+    import torch
+    t = torch.from_numpy(np.asarray(x, dtype=np.float32).copy()).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def _store(logical: np.ndarray, layout: str, ld: int | None = None, pad_bits: int = 0x7E00):
+    """Lay a logical matrix out in row- or column-major storage with leading
+    dimension ld, padding with a NaN bit pattern.  Uses numpy's own C/F
+    ordering, not the oracle's offset formulas."""
+    rows, cols = logical.shape
+    if layout == "row":
+        ld = ld or cols
+        buf = np.full((rows, ld), pad_bits, dtype=logical.dtype)
+        buf[:, :cols] = logical
+    else:
+        ld = ld or rows
+        buf = np.full((cols, ld), pad_bits, dtype=logical.dtype)
+        buf[:, :rows] = logical.T
+    return np.ascontiguousarray(buf), ld
+
+
+def _int_matrix(rng, rows, cols, lo=-2, hi=2):
+    return rng.integers(lo, hi + 1, size=(rows, cols))
+
+
+# --------------------------------------------------------------------------
+# format pins
+# --------------------------------------------------------------------------
+
+def pin_f16_known_values(lib):
+    d = lambda h: lib.oracle_f16_decode(h)
+    assert d(0x3C00) == 1.0
+    assert d(0x7BFF) == 65504.0
+    assert d(0x0001) == 2.0 ** -24
+    assert d(0x0400) == 2.0 ** -14
+    assert d(0x03FF) == 1023 * 2.0 ** -24
+    assert d(0xC000) == -2.0
+    assert d(0x3555) == (1 + 0x155 / 1024) * 2 ** -2
+    z = d(0x8000)
+    assert z == 0.0 and math.copysign(1.0, z) < 0
+    assert d(0x7C00) == math.inf and d(0xFC00) == -math.inf
+    assert math.isnan(d(0x7E00))
+
+
+def pin_bf16_known_values(lib):
+    d = lambda h: lib.oracle_bf16_decode(h)
+    assert d(0x3F80) == 1.0
+    assert d(0x4000) == 2.0
+    assert d(0xBF80) == -1.0
+    assert d(0x7F7F) == (2.0 - 2.0 ** -7) * 2.0 ** 127
+    assert d(0x0080) == 2.0 ** -126
+    assert d(0x0001) == 2.0 ** -133
+    assert d(0x3FC0) == 1.5
+    assert d(0x7F80) == math.inf
+
+
+def pin_f16_decode_matches_numpy(lib):
+    h = np.arange(65536, dtype=np.uint16)
+    mine = oracle.decode(h, "f16", lib=lib)
+    ref = h.view(np.float16).astype(np.float64)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(mine), nan)
+    assert np.array_equal(mine[~nan], ref[~nan])
+    assert np.array_equal(np.signbit(mine[~nan]), np.signbit(ref[~nan]))
+
+
+def pin_bf16_decode_matches_torch(lib):
+    import torch
+    h = np.arange(65536, dtype=np.uint16)
+    mine = oracle.decode(h, "bf16", lib=lib)
+    ref = torch.from_numpy(h.view(np.int16).copy()).view(torch.bfloat16).to(torch.float64).numpy()
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(mine), nan)
+    assert np.array_equal(mine[~nan], ref[~nan])
+
+
+def pin_codec_round_trip(lib):
+    h = np.arange(65536, dtype=np.uint16)
+    for dt in ("f16", "bf16"):
+        v = oracle.decode(h, dt, lib=lib)
+        back = oracle.encode(v, dt, lib=lib)
+        ok = ~np.isnan(v)
+        assert np.array_equal(back[ok], h[ok]), dt
+        assert np.all(np.isnan(oracle.decode(back[~ok], dt, lib=lib)))
+
+
+def pin_rne_ties(lib):
+    e16 = lambda x: lib.oracle_f16_encode(float(x))
+    eb = lambda x: lib.oracle_bf16_encode(float(x))
+    # binary16 integers above 2048 are spaced 2 apart: ties go to even significands
+    assert e16(2049) == _f16_bits(2048)[()] == 0x6800
+    assert e16(2051) == 0x6802 and lib.oracle_f16_decode(0x6802) == 2052
+    assert e16(2050) == 0x6801
+    assert e16(65519) == 0x7BFF          # below the midpoint: the largest finite
+    assert e16(65520) == 0x7C00          # the midpoint to 2^16 rounds to even -> overflow
+    assert e16(2.0 ** -25) == 0x0000     # half the smallest subnormal: tie to even (0)
+    assert e16(3 * 2.0 ** -25) == 0x0002  # 1.5 subnormal quanta: tie to even (2)
+    assert e16(-2049) == 0xE800
+    # bfloat16 integers above 256 are spaced 2 apart
+    assert eb(257) == 0x4380 and lib.oracle_bf16_decode(0x4380) == 256
+    assert eb(259) == 0x4382 and lib.oracle_bf16_decode(0x4382) == 260
+    assert eb(1.0 + 2.0 ** -8) == BF16_ONE
+    assert eb(1.0 + 3 * 2.0 ** -8) == 0x3F82
+
+
+def pin_f16_encode_matches_numpy(lib):
+    rng = np.random.default_rng(7)
+    x = np.concatenate([
+        rng.standard_normal(20000) * 10.0 ** rng.integers(-9, 5, 20000),
+        rng.uniform(-70000, 70000, 5000),
+        (rng.integers(-4096, 4096, 5000) + 0.5),            # exact ties at many scales
+        rng.integers(-2 ** 20, 2 ** 20, 5000) * 2.0 ** -34,  # subnormal range
+    ])
+    assert np.array_equal(oracle.encode(x, "f16", lib=lib), _f16_bits(x))
+
+
+def pin_bf16_encode_matches_torch(lib):
+    import torch
+    rng = np.random.default_rng(8)
+    # float32-representable inputs, so torch's float32 -> bf16 RNE is the
+    # single rounding the oracle performs from binary64
+    x = (rng.standard_normal(40000) * 10.0 ** rng.integers(-30, 30, 40000)).astype(np.float32)
+    ties = (np.arange(-2000, 2000, dtype=np.float32) * 2 + 1) * np.float32(2.0 ** -8) + 1
+    x = np.concatenate([x, ties.astype(np.float32)])
+    ref = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(oracle.encode(x.astype(np.float64), "bf16", lib=lib), ref)
+
+
+# --------------------------------------------------------------------------
+# GEMM pins
+# --------------------------------------------------------------------------
+
+def _run(lib, A_log, B_log, layoutA, layoutB, in_dtype="f16", out_dtype="f32", C=None,
+         alpha=1.0, beta=0.0, lda=None, ldb=None, ldc=None):
+    """Oracle on logical integer/float matrices (stored by numpy); returns the
+    unrounded values V, the scale S and the rounded D (as float64)."""
+    M, K = A_log.shape
+    K2, N = B_log.shape
+    assert K == K2
+    enc = _f16_bits if in_dtype == "f16" else _bf16_bits
+    A_bits, lda = _store(enc(A_log), layoutA, lda)
+    B_bits, ldb = _store(enc(B_log), layoutB, ldb)
+    Cbuf = None
+    if C is not None:
+        ldc = ldc or N
+        if out_dtype == "f32":
+            Cbuf = np.full((M, ldc), np.nan, dtype=np.float32)
+            Cbuf[:, :N] = C
+        else:
+            Cbuf = np.full((M, ldc), 0x7E00, dtype=np.uint16)
+            Cbuf[:, :N] = _f16_bits(C) if out_dtype == "f16" else _bf16_bits(C)
+    ldc = ldc or N
+    D, V, S = oracle.gemm(in_dtype, A_bits, B_bits, Cbuf, M, N, K, lda, ldb, ldc,
+                          layoutA, layoutB, out_dtype, alpha, beta, want_exact=True, lib=lib)
+    Dv = D.astype(np.float64) if out_dtype == "f32" else oracle.decode(D, out_dtype)
+    return V, S, Dv
+
+
+LAYOUTS = [("row", "row"), ("row", "col"), ("col", "row"), ("col", "col")]
+
+
+def pin_brute_force_tiles(lib):
+    """16x8x16 and 16x16x16 integer tiles, all storage orders, against numpy's
+    integer matmul of the logical matrices."""
+    rng = np.random.default_rng(11)
+    for (M, N, K) in [(16, 8, 16), (16, 16, 16), (8, 16, 16)]:
+        for la, lb in LAYOUTS:
+            A = _int_matrix(rng, M, K, -8, 8)
+            B = _int_matrix(rng, K, N, -8, 8)
+            V, S, D = _run(lib, A, B, la, lb)
+            ref = A.astype(np.int64) @ B.astype(np.int64)
+            assert np.array_equal(V, ref.astype(np.float64)), (M, N, K, la, lb)
+            assert np.array_equal(D, ref.astype(np.float64))
+            assert np.array_equal(S, (np.abs(A) @ np.abs(B)).astype(np.float64))
+
+
+def pin_non_square_padded_ld(lib):
+    """Non-square shapes with leading dimensions larger than the extent (the
+    padding holds NaN patterns that must never be read)."""
+    rng = np.random.default_rng(12)
+    M, N, K = 13, 7, 19
+    for la, lb in LAYOUTS:
+        A = _int_matrix(rng, M, K)
+        B = _int_matrix(rng, K, N)
+        lda = (K if la == "row" else M) + 5
+        ldb = (N if lb == "row" else K) + 3
+        V, S, D = _run(lib, A, B, la, lb, lda=lda, ldb=ldb)
+        assert np.array_equal(V, (A @ B).astype(np.float64)), (la, lb)
+
+
+def pin_real_valued_against_float64_matmul(lib):
+    rng = np.random.default_rng(13)
+    M, N, K = 24, 40, 136
+    for la, lb in LAYOUTS:
+        A = rng.uniform(-1, 1, (M, K))
+        B = rng.uniform(-1, 1, (K, N))
+        Ah = A.astype(np.float16).astype(np.float64)
+        Bh = B.astype(np.float16).astype(np.float64)
+        V, S, D = _run(lib, Ah, Bh, la, lb)
+        ref = Ah @ Bh
+        assert np.all(np.abs(V - ref) <= 1e-12 * (np.abs(Ah) @ np.abs(Bh))), (la, lb)
+        assert np.array_equal(D, V.astype(np.float32).astype(np.float64))
+
+
+def pin_identity(lib):
+    rng = np.random.default_rng(14)
+    for la, lb in LAYOUTS:
+        B = rng.uniform(-4, 4, (32, 24)).astype(np.float16).astype(np.float64)
+        V, _, D = _run(lib, np.eye(32), B, la, lb)
+        assert np.array_equal(V, B), (la, lb)
+        A = rng.uniform(-4, 4, (20, 32)).astype(np.float16).astype(np.float64)
+        V, _, _ = _run(lib, A, np.eye(32), la, lb)
+        assert np.array_equal(V, A), (la, lb)
+
+
+def pin_all_ones(lib):
+    for K in (1, 16, 1000, 4096):
+        V, S, D = _run(lib, np.ones((4, K)), np.ones((K, 3)), "row", "col")
+        assert np.all(V == K) and np.all(D == K) and np.all(S == K)
+    # K = 4096 rounds exactly to binary16 (a power of two)
+    _, _, D = _run(lib, np.ones((2, 4096)), np.ones((4096, 2)), "row", "row", out_dtype="f16")
+    assert np.all(D == 4096.0)
+    # exact integers above 2048 round to even in binary16
+    _, _, D = _run(lib, np.ones((1, 2049)), np.ones((2049, 1)), "row", "row", out_dtype="f16")
+    assert D[0, 0] == 2048.0
+    _, _, D = _run(lib, np.ones((1, 2051)), np.ones((2051, 1)), "row", "row", out_dtype="f16")
+    assert D[0, 0] == 2052.0
+
+
+def pin_rank_one(lib):
+    """a = u 1^T, b = 1 v^T  =>  D = K u_i v_j."""
+    u = np.array([1, -2, 3, 0.5, -0.25])
+    v = np.array([2, 1, -1, 0.125])
+    K = 48
+    for la, lb in LAYOUTS:
+        V, _, _ = _run(lib, np.outer(u, np.ones(K)), np.outer(np.ones(K), v), la, lb)
+        assert np.array_equal(V, K * np.outer(u, v)), (la, lb)
+
+
+def pin_layout_golden(lib):
+    """The 2x3 example: stored row-major as 1..6, column-major as 1,4,2,5,3,6;
+    both must be read as the same matrix (times I3 it comes back unchanged)."""
+    with open(os.path.join(GOLDEN, "layout_2x3.json")) as f:
+        g = json.load(f)
+    mat = np.array(g["matrix"], dtype=np.float64)
+    eye = _f16_bits(np.eye(3))
+    for layout, key, ld in (("row", "row_major_storage", 3), ("col", "col_major_storage", 2)):
+        store = _f16_bits(np.array(g[key], dtype=np.float64))
+        D = oracle.gemm("f16", store, eye, None, 2, 3, 3, ld, 3, 3, layout, "row", "f32", lib=lib)
+        assert np.array_equal(D.astype(np.float64), mat), layout
+    # and as the right operand: I2 x M
+    eye2 = _f16_bits(np.eye(2))
+    for layout, key, ld in (("row", "row_major_storage", 3), ("col", "col_major_storage", 2)):
+        store = _f16_bits(np.array(g[key], dtype=np.float64))
+        D = oracle.gemm("f16", eye2, store, None, 2, 3, 2, 2, ld, 3, "row", layout, "f32", lib=lib)
+        assert np.array_equal(D.astype(np.float64), mat), layout
+
+
+def pin_alpha_beta(lib):
+    """alpha = 0.5, beta = 1 on integer data: exact halves, against numpy;
+    and alpha = -1.5, beta = -2."""
+    rng = np.random.default_rng(15)
+    M, N, K = 9, 11, 33
+    for la, lb in LAYOUTS:
+        A = _int_matrix(rng, M, K)
+        B = _int_matrix(rng, K, N)
+        C = _int_matrix(rng, M, N).astype(np.float64)
+        for alpha, beta in ((0.5, 1.0), (-1.5, -2.0), (1.0, 0.25)):
+            V, S, D = _run(lib, A, B, la, lb, C=C, alpha=alpha, beta=beta, ldc=N + 2)
+            ref = alpha * (A @ B) + beta * C
+            assert np.array_equal(V, ref), (la, lb, alpha, beta)
+            assert np.array_equal(S, abs(alpha) * (np.abs(A) @ np.abs(B)) + np.abs(beta * C))
+
+
+def pin_beta_zero_ignores_c(lib):
+    A = np.ones((3, 5))
+    B = np.ones((5, 4))
+    C = np.full((3, 4), np.nan)
+    V, S, D = _run(lib, A, B, "row", "row", C=C, beta=0.0)
+    assert np.all(V == 5) and not np.any(np.isnan(D))
+
+
+def pin_k_zero(lib):
+    """K = 0: the sum is empty, D = beta * C."""
+    C = np.arange(12, dtype=np.float64).reshape(3, 4)
+    Cbuf = C.astype(np.float32)
+    D = oracle.gemm("f16", np.zeros(0, np.uint16), np.zeros(0, np.uint16), Cbuf, 3, 4, 0,
+                    1, 4, 4, "row", "row", "f32", 1.0, 2.0, lib=lib)
+    assert np.array_equal(D.astype(np.float64), 2 * C)
+
+
+def pin_bf16_inputs(lib):
+    rng = np.random.default_rng(16)
+    A = _int_matrix(rng, 16, 32)
+    B = _int_matrix(rng, 32, 24)
+    V, S, D = _run(lib, A, B, "row", "row", in_dtype="bf16", out_dtype="bf16")
+    assert np.array_equal(V, (A @ B).astype(np.float64))
+    assert np.array_equal(D, V)
+
+
+def pin_sixteen_bit_c(lib):
+    """C in the 16-bit output type is decoded, scaled and added."""
+    rng = np.random.default_rng(17)
+    A = _int_matrix(rng, 8, 16)
+    B = _int_matrix(rng, 16, 8)
+    C = _int_matrix(rng, 8, 8).astype(np.float64)
+    for out in ("f16", "bf16"):
+        V, _, _ = _run(lib, A, B, "row", "col", out_dtype=out, C=C, alpha=2.0, beta=-1.0)
+        assert np.array_equal(V, 2.0 * (A @ B) - C), out
+
+
+def pin_entries_match_full(lib):
+    rng = np.random.default_rng(18)
+    M, N, K = 20, 30, 50
+    A = _f16_bits(rng.uniform(-1, 1, (M, K)))
+    B = _f16_bits(rng.uniform(-1, 1, (N, K)))        # column-major K x N
+    C = rng.standard_normal((M, N)).astype(np.float32)
+    D, V, S = oracle.gemm("f16", A, B, C, M, N, K, K, K, N, "row", "col", "f32", 0.5, 1.0,
+                          want_exact=True, lib=lib)
+    ii = rng.integers(0, M, 64)
+    jj = rng.integers(0, N, 64)
+    De, Ve, Se = oracle.gemm_entries("f16", A, B, C, ii, jj, M, N, K, K, K, N, "row", "col",
+                                     "f32", 0.5, 1.0, lib=lib)
+    assert np.array_equal(Ve, V[ii, jj]) and np.array_equal(Se, S[ii, jj])
+    assert np.array_equal(De, D[ii, jj])
+
+
+ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

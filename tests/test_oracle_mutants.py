@@ -1,0 +1,66 @@
+"""Planted mistakes in the oracle must be caught by the pins.
+
+Each mutant is a copy of oracle.c with one plausible mistake (a transposed
+operand, a wrong leading dimension, a dropped term, a wrong sign, an
+off-by-one, a wrong rounding rule), built into a temporary library.  The
+test asserts that at least one pin of ``oracle_pins`` fails on it, i.e. the
+pins would notice that kind of error in the real oracle.
+"""
+import os
+import subprocess
+
+import pytest
+
+import oracle
+import oracle_pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
+
+MUTANTS = {
+    "A_transposed": ("k : k * g->lda + i", None),
+    "B_transposed": ("j : j * g->ldb + k", None),
+    "A_ld_ignored": ("i * g->lda + k", "i * g->K + k"),
+    "B_ld_ignored": ("j * g->ldb + k", "j * g->K + k"),
+    "C_ld_ignored": ("i * g->ldc + j", "i * g->N + j"),
+    "beta_dropped": ("v += g->beta * c;", "v += 0.0 * c;"),
+    "alpha_dropped": ("double v = g->alpha * acc;", "double v = acc;"),
+    "sign_flipped": ("acc += p;", "acc -= p;"),
+    "k_off_by_one": ("k < g->K; ++k", "k < g->K - 1; ++k"),
+    "k_starts_at_one": ("int64_t k = 0; k < g->K", "int64_t k = 1; k < g->K"),
+    "ties_not_even": ("(rem == 0.5 && fmod(fl, 2.0) != 0.0)", "(rem == 0.5)"),
+    "truncate": ("if (rem > 0.5 ||", "if (0 &&"),
+    "f16_subnormal_scale": ("ldexp((double)f, -24)", "ldexp((double)f, -25)"),
+    "bf16_bias": ("ldexp((double)(128 + f), e - 134)", "ldexp((double)(128 + f), e - 133)"),
+    "scale_without_abs": ("sabs += fabs(p);", "sabs += p;"),
+    "scale_without_alpha": ("double s = fabs(g->alpha) * sabs;", "double s = sabs;"),
+    "beta_read_when_zero": ("if (g->beta != 0.0) {", "if (g->C) {"),
+}
+
+
+def _mutate(src: str, name: str) -> str:
+    old, new = MUTANTS[name]
+    if name == "A_transposed":
+        old, new = ("i * g->lda + k : k * g->lda + i", "k * g->lda + i : i * g->lda + k")
+    if name == "B_transposed":
+        old, new = ("k * g->ldb + j : j * g->ldb + k", "j * g->ldb + k : k * g->ldb + j")
+    assert src.count(old) >= 1, f"mutation site of {name} not found"
+    return src.replace(old, new, 1)
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(tmp_path, name):
+    with open(SRC) as f:
+        src = f.read()
+    mutated = tmp_path / "oracle_mut.c"
+    mutated.write_text(_mutate(src, name))
+    so = str(tmp_path / "liboracle_mut.so")
+    oracle.build(str(mutated), so, force=True)
+    lib = oracle.load_library(so)
+    failed = []
+    for pin in oracle_pins.ALL_PINS:
+        try:
+            pin(lib)
+        except AssertionError:
+            failed.append(pin.__name__)
+            break
+    assert failed, f"no pin caught the planted mistake {name}"

@@ -1,0 +1,75 @@
+"""Seeded input generators and flop/byte accounting (CPU only)."""
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import workloads as wl
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def test_flop_accounting_matches_pages():
+    """2*M*N*K equals (number of m16n8k16 instructions) x (flops each), with
+    both figures as the pages print them."""
+    with open(os.path.join(GOLDEN, "flop_accounting.json")) as f:
+        g = json.load(f)
+    w = wl.WORKLOADS["sq4096"]
+    n_mma = w.M * w.N * w.K // g["mma_count_divisor"]
+    assert n_mma * g["mma_m16n8k16_flops"] == w.flops
+    assert 16 * 8 * 16 * 2 == g["mma_m16n8k16_flops"]
+    assert w.K // 16 == g["k_steps_4096_wmma16"]
+    gx, gy = g["grid_4096_wmma16"]
+    assert (w.N // 16, w.M // 16) == (gx, gy)
+    assert gx * gy == g["grid_blocks_4096_wmma16"]
+    assert gx * gy * 16 * 16 == g["outputs_4096"] == w.M * w.N
+
+
+def test_algorithmic_bytes():
+    assert wl.WORKLOADS["sq4096"].algorithmic_bytes() == 2 * 4096 * 4096 * 2 + 4096 * 4096 * 4
+    r = wl.WORKLOADS["ragged"]
+    assert r.algorithmic_bytes() == (4097 * 1000 + 1000 * 2055) * 2 + 2 * 4097 * 2055 * 4
+    s = wl.WORKLOADS["skinny"]
+    assert s.algorithmic_bytes() == (16 * 8192 + 8192 * 8192) * 2 + 16 * 8192 * 2
+
+
+def test_leading_dimensions():
+    r = wl.WORKLOADS["ragged"]
+    assert (r.lda, r.ldb, r.ldc) == (1000, 1000, 2055)
+    h = wl.WORKLOADS["sq4096h"]
+    assert (h.layoutA, h.layoutB, h.ldb) == ("row", "col", 4096)
+
+
+@pytest.mark.parametrize("name", ["pr1", "ragged"])
+def test_deterministic_and_distributed(name):
+    w = wl.WORKLOADS[name].with_shape(64, 48, 40) if name == "ragged" else wl.WORKLOADS[name]
+    a = wl.make_inputs(w)
+    b = wl.make_inputs(w)
+    assert torch.equal(a.A.view(torch.int16), b.A.view(torch.int16))
+    assert torch.equal(a.B.view(torch.int16), b.B.view(torch.int16))
+    assert a.A.dtype == wl.DTYPES[w.in_dtype]
+    if w.dist == "u1":
+        assert float(a.A.float().abs().max()) <= 1.0
+        assert 0.2 < float(a.A.float().std()) < 0.8
+    if w.beta != 0:
+        assert a.C is not None and a.C.shape == (w.M, w.ldc)
+
+
+def test_integer_twin_values():
+    w = wl.WORKLOADS["ragged"].with_shape(33, 17, 65)
+    t = wl.make_inputs(w, integer=True)
+    for m in (t.A, t.B, t.C):
+        vals = set(np.unique(m.float().numpy()).tolist())
+        assert vals <= {-2.0, -1.0, 0.0, 1.0, 2.0} and len(vals) == 5
+
+
+def test_storage_and_logical_views():
+    w = wl.WORKLOADS["sq4096h"].with_shape(8, 6, 5)
+    t = wl.make_inputs(w, lda=16, ldb=8)
+    assert t.A.shape == (8, 16)          # row-major M x lda
+    assert t.B.shape == (6, 8)           # column-major: N columns of ldb
+    LB = wl.logical(t.B, w.K, w.N, "col")
+    assert LB.shape == (5, 6)
+    assert LB[3, 4] == t.B[4, 3]
