@@ -1,0 +1,383 @@
+#!/usr/bin/env python3
+"""Benchmark of the sm_103a dense HGEMM: HGEMM TFLOP/s at M=N=K=4096,
+fp16 inputs, fp32 accumulate and output (row-major A, B, D; alpha=1,
+beta=0), reported against the measured tensor-core peak.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+    python bench.py --impl reference ...     # the CPU oracle on a bounded sample
+
+One step = one gemm_run over the workload (one launch of the persistent
+kernel), inputs resident in HBM.  L2 is flushed before every step by writing
+a 256 MiB buffer (outside the timed interval of the step); every step's GEMM
+is timed with CUDA events on the launching stream, and the timed loop as a
+whole is bracketed by a barrier and torch.cuda.synchronize().  With N > 1
+(torchrun, one process per GPU) every rank runs an independent replica of
+the same workload (a single GEMM of this size does not need to be sharded);
+value = the flops of all ranks / the slowest rank's time.
+
+Prints one JSON line (rank 0).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "HGEMM TFLOP/s at M=N=K=4096 fp16→fp32 acc; % of GB300 dense FP16 tensor peak"
+NOMINAL_DENSE_FP16_TFLOPS = 2250.0       # GB300 dense fp16/bf16 tensor peak (datasheet)
+FALLBACK_BF16_TFLOPS = 1900.0            # used only when no measured peak file is present
+FALLBACK_HBM_GBS = 6800.0
+L2_FLUSH_BYTES = 256 << 20
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="sq4096")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    return ap.parse_args()
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return {"bf16_tflops": FALLBACK_BF16_TFLOPS, "hbm_gbs": FALLBACK_HBM_GBS}, "fallback"
+
+
+def workload_desc(w) -> str:
+    return (f"{w.name}: M={w.M} N={w.N} K={w.K}; A {w.in_dtype} {w.layoutA}-major, B {w.in_dtype} "
+            f"{w.layoutB}-major, {w.dist}; {w.accum_dtype} accumulate, {w.out_dtype} row-major out; "
+            f"alpha={w.alpha} beta={w.beta}")
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines: list[str] = []
+        self.t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.t:
+            self.t.join(timeout=5)
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+                power.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, val in zip(names, parts[4:8]):
+                if val.lower() == "active":
+                    reasons.add(n)
+        return {
+            "sm_mhz": statistics.median(sm) if sm else None,
+            "sm_max_mhz": max(smax) if smax else None,
+            "power_w_max": max(power) if power else None,
+            "samples": len(sm),
+            "reasons": sorted(reasons),
+        }
+
+
+def cpu_baseline(w, h, target_s: float = 12.0):
+    """The oracle, as it stands, on the host cores: a bounded sample of the
+    workload (whole rows of D), in the metric's unit."""
+    import oracle
+    import workloads as wl
+    cores = os.cpu_count() or 1
+    A, B = wl.bits(h.A), wl.bits(h.B)
+    C = None if h.C is None else wl.bits(h.C)
+    rows = max(cores, 8)
+    # calibrate on a small slice, then size the sample to ~target_s
+    t0 = time.perf_counter()
+    oracle.gemm(w.in_dtype, A, B, C, min(rows, w.M), w.N, w.K, h.lda, h.ldb, h.ldc, w.layoutA, w.layoutB,
+                w.out_dtype, w.alpha, w.beta, nthreads=cores)
+    dt = time.perf_counter() - t0
+    rows = int(min(w.M, max(rows, rows * target_s / max(dt, 1e-3))))
+    rows = max(cores, rows // cores * cores)
+    t0 = time.perf_counter()
+    oracle.gemm(w.in_dtype, A, B, C, rows, w.N, w.K, h.lda, h.ldb, h.ldc, w.layoutA, w.layoutB,
+                w.out_dtype, w.alpha, w.beta, nthreads=cores)
+    dt = time.perf_counter() - t0
+    flops = 2.0 * rows * w.N * w.K
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": f"first {rows} rows of D ({rows}x{w.N}x{w.K}, {flops:.3g} flop) in {dt:.2f} s "
+                      f"on {cores} threads"}
+
+
+def traffic_from_profiles(kernel_tag: str):
+    """Per-launch DRAM bytes from the committed ncu summary, if it was taken
+    on the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    try:
+        with open(path) as f:
+            kv = dict(line.strip().split("=", 1) for line in f if "=" in line and not line.startswith("#"))
+    except OSError:
+        return None
+    from tensor_core_dense_tma_gb300 import build as tcbuild
+    import hashlib
+    hsh = hashlib.sha256()
+    for fn in tcbuild._inputs():
+        with open(fn, "rb") as f:
+            hsh.update(f.read())
+    if kv.get("sources_sha256") != hsh.hexdigest()[:16]:
+        return None
+    val = kv.get(f"{kernel_tag}.bytes_per_launch")
+    return float(val) if val else None
+
+
+def run_reference(args):
+    """The CPU oracle on the host cores, each step a bounded sample."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    import oracle
+    import workloads as wl
+    w = wl.WORKLOADS[args.workload]
+    h = wl.make_inputs(w)
+    cores = os.cpu_count() or 1
+    A, B = wl.bits(h.A), wl.bits(h.B)
+    C = None if h.C is None else wl.bits(h.C)
+    rows = cores   # one row per core per step: a few seconds per step
+    for _ in range(args.warmup):
+        oracle.gemm(w.in_dtype, A, B, C, rows, w.N, w.K, h.lda, h.ldb, h.ldc, w.layoutA, w.layoutB,
+                    w.out_dtype, w.alpha, w.beta, nthreads=cores)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.gemm(w.in_dtype, A, B, C, rows, w.N, w.K, h.lda, h.ldb, h.ldc, w.layoutA, w.layoutB,
+                    w.out_dtype, w.alpha, w.beta, nthreads=cores)
+    dt = time.perf_counter() - t0
+    flops = 2.0 * rows * w.N * w.K * args.steps
+    val = flops / dt / 1e12
+    out = {
+        "impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": workload_desc(w), "sample": f"{rows} rows of D per step"},
+        "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{rows}x{w.N}x{w.K} per step (rows of D), {args.steps} steps"},
+        "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(out), flush=True)
+    return 0
+
+
+def main():
+    args = parse()
+    if args.steps < 1 or args.warmup < 0:
+        raise SystemExit("bad --steps/--warmup")
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+    import tensor_core_dense_tma_gb300 as tc
+    import workloads as wl
+    from tensor_core_dense_tma_gb300 import build as tcbuild
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if not tcbuild.up_to_date():
+        if rank == 0:
+            tcbuild.build()
+        if dist:
+            dist.barrier()
+
+    w = wl.WORKLOADS[args.workload]
+    h = wl.make_inputs(w)
+    A = h.A.to(dev)
+    B = h.B.to(dev)
+    C = None if h.C is None else h.C.to(dev)
+    D = torch.empty((w.M, h.ldc), dtype=wl.DTYPES[w.out_dtype], device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    plan = tc.Plan(w.in_dtype, local)
+    A_l = wl.logical(A, w.M, w.K, w.layoutA)
+    B_l = wl.logical(B, w.K, w.N, w.layoutB)
+    C_l = None if C is None else C[:, :w.N]
+    D_l = D[:, :w.N]
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        plan.gemm(A_l, B_l, C_l, D_l, alpha=w.alpha, beta=w.beta, accum_dtype=w.accum_dtype,
+                  out_dtype=w.out_dtype, stream=stream.cuda_stream)
+
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        step()
+    torch.cuda.synchronize()
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    sampler = ClockSampler(dev.index if os.environ.get("CUDA_VISIBLE_DEVICES") is None else
+                           int(os.environ["CUDA_VISIBLE_DEVICES"].split(",")[local]))
+    if rank == 0:
+        sampler.start()
+        time.sleep(0.3)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    launches0 = plan.launches
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.fill_(float(i))
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    if dist:
+        dist.barrier()
+    launches = plan.launches - launches0
+    clocks = sampler.stop() if rank == 0 else None
+    assert plan.device_status() == 0, "device status word reports an error"
+
+    per_step = [s.elapsed_time(e) for s, e in zip(starts, ends)]   # ms
+    total_ms = sum(per_step)
+    if dist:
+        t = torch.tensor([total_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = w.flops * args.steps * world / (total_ms * 1e-3) / 1e12   # TFLOP/s, whole job
+
+    # end to end through the public API with host buffers (pinned), copies timed
+    e2e = None
+    if not args.no_e2e:
+        hA = h.A.pin_memory()
+        hB = h.B.pin_memory()
+        hC = None if h.C is None else h.C.pin_memory()
+        hD = torch.empty((w.M, w.N), dtype=wl.DTYPES[w.out_dtype], pin_memory=True)
+        staging = {}
+        hA_l = wl.logical(hA, w.M, w.K, w.layoutA)
+        hB_l = wl.logical(hB, w.K, w.N, w.layoutB)
+        hC_l = None if hC is None else hC[:, :w.N]
+        for _ in range(3):
+            plan.gemm_host(hA_l, hB_l, hC_l, hD, alpha=w.alpha, beta=w.beta, accum_dtype=w.accum_dtype,
+                           out_dtype=w.out_dtype, staging=staging)
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.e2e_steps):
+            plan.gemm_host(hA_l, hB_l, hC_l, hD, alpha=w.alpha, beta=w.beta, accum_dtype=w.accum_dtype,
+                           out_dtype=w.out_dtype, staging=staging)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
+        h2d = hA.numel() * hA.element_size() + hB.numel() * hB.element_size() + (
+            0 if hC is None else hC.numel() * hC.element_size())
+        d2h = hD.numel() * hD.element_size()
+        e2e = {"value": w.flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "path": "Plan.gemm_host: pinned host A,B -> device, gemm_run, D -> pinned host"}
+
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return 0
+
+    peaks, peak_src = measured_peaks()
+    avg_s = ms_per_step * 1e-3
+    achieved = w.flops / avg_s / 1e12
+    peak = float(peaks.get("bf16_tflops", FALLBACK_BF16_TFLOPS))   # fp16 dense rate = bf16 dense rate
+    kernel_tag = plan.describe(w.M, w.N, w.K, w.layoutA, w.layoutB, w.accum_dtype, w.out_dtype).split()[0]
+    traffic = traffic_from_profiles(kernel_tag)
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": traffic,
+                "peak_source": f"{peak_src} bf16 dense GEMM burst (MEASURED_PEAKS.json), fp16:bf16 = 1:1"
+                               if peak_src == "measured" else "fallback 1.9 PFLOP/s bf16 burst",
+                "kernel": kernel_tag,
+                "algorithmic": f"2*M*N*K = {w.flops:.4g} flop per launch"}
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        cpu = cpu_baseline(w, h)
+    out = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+        "config": {
+            "workload": workload_desc(w),
+            "accumulate": w.accum_dtype, "out": w.out_dtype,
+            "l2": f"flushed before every step ({L2_FLUSH_BYTES >> 20} MiB write, outside the step's events)",
+            "parallelism": "replicas" if world > 1 else "single",
+            "pct_of_nominal_dense_fp16": 100.0 * value / world / NOMINAL_DENSE_FP16_TFLOPS,
+            "nominal_dense_fp16_tflops": NOMINAL_DENSE_FP16_TFLOPS,
+            "kernel_config": plan.describe(w.M, w.N, w.K, w.layoutA, w.layoutB, w.accum_dtype, w.out_dtype),
+            "wall_s_timed_loop": wall,
+            "step_ms_min": min(per_step), "step_ms_median": statistics.median(per_step),
+        },
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": launches,
+        "clocks": clocks,
+    }
+    print(json.dumps(out), flush=True)
+    plan.close()
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

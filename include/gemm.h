@@ -1,0 +1,143 @@
+/*
+ * gemm.h -- C ABI of the GB300 (sm_103a) dense half-precision GEMM
+ *
+ *     D = alpha * A * B + beta * C
+ *
+ * The operation is the Tensor Core multiply-accumulate D = A x B + C
+ * ("CUDA算子优化(5)：WMMA矩阵乘法", WMMA API section (5) mma_sync, which also
+ * allows C and D to be the same matrix; "深入CUDA Tensor Core与WMMA",
+ * section 2.2), element by element C[i,j] = sum_k A[i,k] * B[k,j]
+ * ("矩阵乘法优化可视化学习文档", section 1), with the BLAS scaling by alpha
+ * and beta.  A is M x K, B is K x N, C and D are M x N.
+ *
+ * Storage order ("深入CUDA Tensor Core与WMMA", section 3.2; leading
+ * dimensions as the ldm of section 4.2):
+ *   A row-major:    element (i,k) at A[i*lda + k], lda >= K
+ *   A column-major: element (i,k) at A[k*lda + i], lda >= M
+ *   B row-major:    element (k,j) at B[k*ldb + j], ldb >= N
+ *   B column-major: element (k,j) at B[j*ldb + k], ldb >= K
+ *   C and D:        row-major, element (i,j) at [i*ldc + j], ldc >= N,
+ *                   both of type out_dtype (D has no separate leading
+ *                   dimension; C may be the same buffer as D).
+ *
+ * Types.  A and B are both of the plan's input type, fp16 or bf16.
+ * Supported (input, accumulator, output) combinations:
+ *   fp16: (f32 acc -> f32, f16 or bf16 out), (f16 acc -> f16 out)
+ *   bf16: (f32 acc -> f32 or bf16 out)
+ * fp32 accumulation is the standard ("深入CUDA Tensor Core与WMMA", sections
+ * 6.2 and 7.1); fp16 accumulation is the f16.f16.f16.f16 form of
+ * "hgemm_mma_m16n8k16_naive_kernel详解", section 1.1.  alpha and beta are
+ * applied in fp32 to the accumulator and to C, and the sum is rounded once,
+ * to nearest even, to the output type.  With beta == 0, C is not read and
+ * may be NULL.
+ *
+ * Memory.  A, B, C, D are DEVICE pointers owned by the caller; the library
+ * never frees or retains them after a call returns.  gemm_run is
+ * asynchronous on `stream` (a cudaStream_t; NULL = the legacy default
+ * stream) and synchronises nothing; results are visible after the caller
+ * synchronises the stream.  A plan holds device state (a status word) and
+ * must not be used from two streams at once.
+ *
+ * Alignment ("CUDA算子优化(5)：WMMA矩阵乘法", load_matrix_sync: ldm a
+ * multiple of 16 bytes): A and B must start on 16-byte boundaries and
+ * lda*2, ldb*2 must be multiples of 16 bytes (A and B are read by the
+ * tensor-memory accelerator).  C and D need only element alignment; any
+ * ldc >= N is accepted (unaligned rows take a scalar store path).
+ *
+ * Errors.  Every entry point returns a gemm_status_t and leaves its
+ * outputs untouched on failure; argument errors are detected on the host
+ * before anything is launched.  Device-side errors (a pipeline wait that
+ * ran out of time) are recorded in the plan's status word and read with
+ * gemm_plan_device_status after the caller has synchronised.
+ */
+#ifndef TCDT_GEMM_H
+#define TCDT_GEMM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct gemm_plan *gemm_plan_t;
+
+typedef enum {
+    GEMM_OK = 0,
+    GEMM_ERR_INVALID_ARG = 1,   /* null pointer, negative size, ld too small, bad enum */
+    GEMM_ERR_UNSUPPORTED = 2,   /* dtype combination or size the kernels do not cover */
+    GEMM_ERR_MISALIGNED = 3,    /* A/B base or lda/ldb not 16-byte aligned; C/D not element aligned */
+    GEMM_ERR_CUDA = 4,          /* a CUDA runtime/driver call failed (launch, tensor map, memory) */
+    GEMM_ERR_TIMEOUT = 5,       /* a device pipeline wait gave up (read via gemm_plan_device_status) */
+    GEMM_ERR_NO_DEVICE = 6      /* no usable sm_103 device */
+} gemm_status_t;
+
+typedef enum { GEMM_ROW_MAJOR = 0, GEMM_COL_MAJOR = 1 } gemm_layout_t;
+
+typedef enum { GEMM_F16 = 0, GEMM_BF16 = 1, GEMM_F32 = 2 } gemm_dtype_t;
+
+/* Create a plan for `device` (a CUDA ordinal) and input type `in_dtype`
+ * (GEMM_F16 or GEMM_BF16).  Queries the device (it must be compute
+ * capability 10.3), allocates the plan's device status word and resolves
+ * the driver's tensor-map encoder.  Makes `device` current on the calling
+ * thread.  On failure *out is set to NULL. */
+gemm_status_t gemm_plan_create(gemm_plan_t *out, int device, gemm_dtype_t in_dtype);
+
+/* Launch D = alpha*A*B + beta*C on `stream`.  Layout and pointers as in the
+ * header comment.  M == 0 or N == 0 launches nothing and returns GEMM_OK;
+ * K == 0 gives D = beta*C (zero when beta == 0).  One persistent kernel per
+ * call on the tensor-core path. */
+gemm_status_t gemm_run(gemm_plan_t plan, const void *A, const void *B, const void *C, void *D,
+                       int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
+                       gemm_layout_t layoutA, gemm_layout_t layoutB,
+                       gemm_dtype_t accum_dtype, gemm_dtype_t out_dtype,
+                       float alpha, float beta, void *stream);
+
+/* The host-side argument checks of gemm_run, without a plan or a device:
+ * returns the status gemm_run would return before launching anything. */
+gemm_status_t gemm_validate(gemm_dtype_t in_dtype, const void *A, const void *B, const void *C,
+                            void *D, int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
+                            int64_t ldc, gemm_layout_t layoutA, gemm_layout_t layoutB,
+                            gemm_dtype_t accum_dtype, gemm_dtype_t out_dtype, float beta);
+
+/* Read the plan's device status word: GEMM_OK, or the first device-side
+ * error (GEMM_ERR_TIMEOUT) recorded by any launch since the plan was
+ * created or the word last cleared.  Synchronises nothing itself (the copy
+ * is a blocking read of one word: call it after synchronising the stream).
+ * `clear` != 0 resets the word to GEMM_OK afterwards. */
+gemm_status_t gemm_plan_device_status(gemm_plan_t plan, int clear);
+
+/* Where the last recorded device error happened (a role/wait code), 0 if none. */
+int gemm_plan_device_error_site(gemm_plan_t plan);
+
+/* Limit, in nanoseconds, of every pipeline wait inside the kernels
+ * (default 2e9).  A wait that exceeds it records GEMM_ERR_TIMEOUT in the
+ * status word and the kernel winds down and returns instead of hanging. */
+gemm_status_t gemm_plan_set_timeout_ns(gemm_plan_t plan, uint64_t ns);
+
+/* Number of kernels this plan has launched so far. */
+uint64_t gemm_plan_launch_count(gemm_plan_t plan);
+
+/* Number of SMs of the plan's device. */
+int gemm_plan_sm_count(gemm_plan_t plan);
+
+/* Describe the kernel configuration gemm_run would pick for these sizes
+ * and types into buf (NUL-terminated, at most `len` bytes).  Returns the
+ * same validation status as gemm_validate (with A, B, C, D taken as
+ * aligned). */
+gemm_status_t gemm_plan_describe(gemm_plan_t plan, int64_t M, int64_t N, int64_t K,
+                                 gemm_layout_t layoutA, gemm_layout_t layoutB,
+                                 gemm_dtype_t accum_dtype, gemm_dtype_t out_dtype,
+                                 char *buf, int64_t len);
+
+/* Free the plan and its device memory.  NULL is accepted (no-op).  The
+ * caller must have synchronised any stream still running its launches. */
+gemm_status_t gemm_plan_destroy(gemm_plan_t plan);
+
+/* Static, human-readable name of a status code. */
+const char *gemm_status_string(gemm_status_t status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TCDT_GEMM_H */

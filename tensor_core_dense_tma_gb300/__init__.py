@@ -1,0 +1,318 @@
+"""Python binding of the GB300 (sm_103a) dense half-precision GEMM library.
+
+    D = alpha * A * B + beta * C
+
+The library (``_build/libtcdt_gemm.so``, built by ``build.build()``) exposes
+the C ABI of ``include/gemm.h``.  This module only marshals arguments: every
+step of the computation runs in the library's CUDA kernels.  PyTorch is used
+for device memory and streams.  There is no fallback: if the library is not
+built, or no sm_103 device is present, the calls raise.
+
+Low-level names mirror the C ABI (``gemm_plan_create``, ``gemm_run``,
+``gemm_plan_destroy`` ...; see ``abi``).  ``Plan`` wraps a plan handle and
+``Plan.gemm`` takes torch tensors, reading the storage order and leading
+dimensions from their strides:
+
+* ``A`` is the logical M x K matrix: row-major if ``A.stride(1) == 1``
+  (lda = ``A.stride(0)``), column-major if ``A.stride(0) == 1``
+  (lda = ``A.stride(1)``); ``B`` (K x N) likewise;
+* ``C`` and ``D`` are row-major M x N with the same row stride (ldc).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import build as _build_mod
+
+__all__ = [
+    "abi", "load", "Plan", "GemmError", "STATUS", "DTYPE", "LAYOUT",
+    "gemm_plan_create", "gemm_run", "gemm_validate", "gemm_plan_device_status",
+    "gemm_plan_device_error_site", "gemm_plan_set_timeout_ns", "gemm_plan_launch_count",
+    "gemm_plan_sm_count", "gemm_plan_describe", "gemm_plan_destroy", "gemm_status_string",
+]
+
+STATUS = {
+    0: "GEMM_OK", 1: "GEMM_ERR_INVALID_ARG", 2: "GEMM_ERR_UNSUPPORTED", 3: "GEMM_ERR_MISALIGNED",
+    4: "GEMM_ERR_CUDA", 5: "GEMM_ERR_TIMEOUT", 6: "GEMM_ERR_NO_DEVICE",
+}
+DTYPE = {"f16": 0, "bf16": 1, "f32": 2}
+LAYOUT = {"row": 0, "col": 1}
+
+_lock = threading.Lock()
+_lib: ctypes.CDLL | None = None
+
+
+class GemmError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        super().__init__(f"{what}: {STATUS.get(status, status)}" if what else STATUS.get(status, str(status)))
+
+
+def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
+    p, i64, i32, u64, f32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_uint64, ctypes.c_float
+    lib.gemm_plan_create.argtypes = [ctypes.POINTER(p), i32, i32]
+    lib.gemm_plan_create.restype = i32
+    lib.gemm_run.argtypes = [p, p, p, p, p, i64, i64, i64, i64, i64, i64, i32, i32, i32, i32, f32, f32, p]
+    lib.gemm_run.restype = i32
+    lib.gemm_validate.argtypes = [i32, p, p, p, p, i64, i64, i64, i64, i64, i64, i32, i32, i32, i32, f32]
+    lib.gemm_validate.restype = i32
+    lib.gemm_plan_device_status.argtypes = [p, i32]
+    lib.gemm_plan_device_status.restype = i32
+    lib.gemm_plan_device_error_site.argtypes = [p]
+    lib.gemm_plan_device_error_site.restype = i32
+    lib.gemm_plan_set_timeout_ns.argtypes = [p, u64]
+    lib.gemm_plan_set_timeout_ns.restype = i32
+    lib.gemm_plan_launch_count.argtypes = [p]
+    lib.gemm_plan_launch_count.restype = u64
+    lib.gemm_plan_sm_count.argtypes = [p]
+    lib.gemm_plan_sm_count.restype = i32
+    lib.gemm_plan_describe.argtypes = [p, i64, i64, i64, i32, i32, i32, i32, ctypes.c_char_p, i64]
+    lib.gemm_plan_describe.restype = i32
+    lib.gemm_plan_destroy.argtypes = [p]
+    lib.gemm_plan_destroy.restype = i32
+    lib.gemm_status_string.argtypes = [i32]
+    lib.gemm_status_string.restype = ctypes.c_char_p
+    return lib
+
+
+def library_path() -> str:
+    return _build_mod.LIB_PATH
+
+
+def load(path: str | None = None) -> ctypes.CDLL:
+    """Load the built library (no silent rebuild, no fallback)."""
+    global _lib
+    if path is not None:
+        return _declare(ctypes.CDLL(path))
+    with _lock:
+        if _lib is None:
+            lp = library_path()
+            if not os.path.exists(lp):
+                raise RuntimeError(
+                    f"the sm_103a GEMM library is not built ({lp} missing); "
+                    "run tensor_core_dense_tma_gb300.build.build() first")
+            _lib = _declare(ctypes.CDLL(lp))
+        return _lib
+
+
+def abi() -> ctypes.CDLL:
+    """The ctypes handle of the C ABI."""
+    return load()
+
+
+# Same-named thin wrappers over the C ABI -----------------------------------
+
+def gemm_plan_create(device: int, in_dtype: str) -> int:
+    h = ctypes.c_void_p()
+    st = load().gemm_plan_create(ctypes.byref(h), device, DTYPE[in_dtype])
+    if st != 0:
+        raise GemmError(st, "gemm_plan_create")
+    return h.value
+
+
+def gemm_run(plan, A, B, C, D, M, N, K, lda, ldb, ldc, layoutA, layoutB, accum_dtype, out_dtype,
+             alpha, beta, stream) -> int:
+    return load().gemm_run(plan, A, B, C, D, M, N, K, lda, ldb, ldc, LAYOUT[layoutA], LAYOUT[layoutB],
+                           DTYPE[accum_dtype], DTYPE[out_dtype], alpha, beta, stream)
+
+
+def gemm_validate(in_dtype, A, B, C, D, M, N, K, lda, ldb, ldc, layoutA, layoutB, accum_dtype,
+                  out_dtype, beta) -> int:
+    return load().gemm_validate(DTYPE[in_dtype] if isinstance(in_dtype, str) else in_dtype, A, B, C, D,
+                                M, N, K, lda, ldb, ldc,
+                                LAYOUT[layoutA] if isinstance(layoutA, str) else layoutA,
+                                LAYOUT[layoutB] if isinstance(layoutB, str) else layoutB,
+                                DTYPE[accum_dtype] if isinstance(accum_dtype, str) else accum_dtype,
+                                DTYPE[out_dtype] if isinstance(out_dtype, str) else out_dtype, beta)
+
+
+def gemm_plan_device_status(plan, clear: bool = False) -> int:
+    return load().gemm_plan_device_status(plan, 1 if clear else 0)
+
+
+def gemm_plan_device_error_site(plan) -> int:
+    return load().gemm_plan_device_error_site(plan)
+
+
+def gemm_plan_set_timeout_ns(plan, ns: int) -> int:
+    return load().gemm_plan_set_timeout_ns(plan, ns)
+
+
+def gemm_plan_launch_count(plan) -> int:
+    return load().gemm_plan_launch_count(plan)
+
+
+def gemm_plan_sm_count(plan) -> int:
+    return load().gemm_plan_sm_count(plan)
+
+
+def gemm_plan_describe(plan, M, N, K, layoutA="row", layoutB="row", accum_dtype="f32",
+                       out_dtype="f32") -> str:
+    buf = ctypes.create_string_buffer(256)
+    st = load().gemm_plan_describe(plan, M, N, K, LAYOUT[layoutA], LAYOUT[layoutB], DTYPE[accum_dtype],
+                                   DTYPE[out_dtype], buf, 256)
+    if st != 0:
+        raise GemmError(st, "gemm_plan_describe")
+    return buf.value.decode()
+
+
+def gemm_plan_destroy(plan) -> int:
+    return load().gemm_plan_destroy(plan)
+
+
+def gemm_status_string(status: int) -> str:
+    return load().gemm_status_string(status).decode()
+
+
+# torch-facing convenience -----------------------------------------------------
+
+_TORCH_DT = {"f16": "float16", "bf16": "bfloat16", "f32": "float32"}
+
+
+def _dt_name(t) -> str:
+    import torch
+    return {torch.float16: "f16", torch.bfloat16: "bf16", torch.float32: "f32"}[t.dtype]
+
+
+def _operand_layout(t, what: str):
+    """(layout, ld) of a logical 2-D matrix view from its strides."""
+    if t.dim() != 2:
+        raise ValueError(f"{what} must be 2-D")
+    r, c = t.shape
+    s0, s1 = t.stride()
+    if s1 == 1 and (s0 >= c or r <= 1):
+        return "row", max(s0, c)
+    if s0 == 1 and (s1 >= r or c <= 1):
+        return "col", max(s1, r)
+    raise ValueError(f"{what} must be row- or column-major (strides {t.stride()})")
+
+
+class Plan:
+    """A gemm plan bound to one device and one input type."""
+
+    def __init__(self, in_dtype: str = "f16", device: int | None = None):
+        import torch
+        if device is None:
+            device = torch.cuda.current_device()
+        self.device = device
+        self.in_dtype = in_dtype
+        self.handle = gemm_plan_create(device, in_dtype)
+
+    def close(self):
+        if self.handle:
+            gemm_plan_destroy(self.handle)
+            self.handle = None
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    @property
+    def launches(self) -> int:
+        return gemm_plan_launch_count(self.handle)
+
+    @property
+    def sm_count(self) -> int:
+        return gemm_plan_sm_count(self.handle)
+
+    def device_status(self, clear: bool = False) -> int:
+        return gemm_plan_device_status(self.handle, clear)
+
+    def set_timeout_ns(self, ns: int):
+        st = gemm_plan_set_timeout_ns(self.handle, ns)
+        if st != 0:
+            raise GemmError(st, "gemm_plan_set_timeout_ns")
+
+    def describe(self, M, N, K, layoutA="row", layoutB="row", accum_dtype="f32", out_dtype="f32") -> str:
+        return gemm_plan_describe(self.handle, M, N, K, layoutA, layoutB, accum_dtype, out_dtype)
+
+    def run_raw(self, A_ptr, B_ptr, C_ptr, D_ptr, M, N, K, lda, ldb, ldc, layoutA, layoutB,
+                accum_dtype, out_dtype, alpha=1.0, beta=0.0, stream=None) -> None:
+        """gemm_run on raw device addresses; raises GemmError on a bad status."""
+        st = gemm_run(self.handle, A_ptr, B_ptr, C_ptr, D_ptr, M, N, K, lda, ldb, ldc, layoutA, layoutB,
+                      accum_dtype, out_dtype, float(alpha), float(beta), stream)
+        if st != 0:
+            raise GemmError(st, "gemm_run")
+
+    def gemm(self, A, B, C=None, D=None, *, alpha: float = 1.0, beta: float = 0.0,
+             accum_dtype: str = "f32", out_dtype: str | None = None, stream=None):
+        """D = alpha*A@B + beta*C on device tensors; returns D (allocated if
+        not given).  Layouts and leading dimensions come from the strides."""
+        import torch
+        M, K = A.shape
+        K2, N = B.shape
+        if K2 != K:
+            raise ValueError("inner dimensions differ")
+        if _dt_name(A) != self.in_dtype or _dt_name(B) != self.in_dtype:
+            raise ValueError(f"A and B must be {self.in_dtype}")
+        la, lda = _operand_layout(A, "A")
+        lb, ldb = _operand_layout(B, "B")
+        if out_dtype is None:
+            out_dtype = _dt_name(D) if D is not None else (_dt_name(C) if C is not None else "f32")
+        if D is None:
+            D = torch.empty((M, N), dtype=getattr(torch, _TORCH_DT[out_dtype]), device=A.device)
+        if D.dim() != 2 or D.shape != (M, N) or (N > 1 and D.stride(1) != 1):
+            raise ValueError("D must be a row-major M x N matrix")
+        ldc = D.stride(0) if M > 1 else N
+        if C is not None:
+            if C.shape != (M, N) or (N > 1 and C.stride(1) != 1) or (M > 1 and C.stride(0) != ldc):
+                raise ValueError("C must be row-major M x N with the same row stride as D")
+            if _dt_name(C) != out_dtype:
+                raise ValueError("C must have the output type")
+        if stream is None:
+            stream = torch.cuda.current_stream(A.device).cuda_stream
+        self.run_raw(A.data_ptr(), B.data_ptr(), C.data_ptr() if C is not None else None, D.data_ptr(),
+                     M, N, K, lda, ldb, max(ldc, N), la, lb, accum_dtype, out_dtype, alpha, beta, stream)
+        return D
+
+    def gemm_host(self, A, B, C=None, D=None, *, alpha: float = 1.0, beta: float = 0.0,
+                  accum_dtype: str = "f32", out_dtype: str | None = None, stream=None,
+                  staging: dict | None = None):
+        """End-to-end call on HOST tensors (pinned for asynchronous copies):
+        copies A, B (and C) to the device, runs gemm_run, copies D back into
+        the host tensor ``D`` (allocated pinned if not given) and returns it
+        once the stream has finished.  ``staging`` may carry device buffers
+        between calls (keys "A", "B", "C", "D"); they are (re)allocated when
+        missing or of the wrong size."""
+        import torch
+        dev = torch.device("cuda", self.device)
+        st = staging if staging is not None else {}
+        s = torch.cuda.current_stream(dev) if stream is None else stream
+
+        def stage(key, t):
+            buf = st.get(key)
+            if buf is None or buf.shape != t.shape or buf.dtype != t.dtype or buf.stride() != t.stride():
+                buf = torch.empty_strided(t.shape, t.stride(), dtype=t.dtype, device=dev)
+                st[key] = buf
+            buf.copy_(t, non_blocking=True)
+            return buf
+
+        with torch.cuda.stream(s):
+            Ad = stage("A", A)
+            Bd = stage("B", B)
+            Cd = stage("C", C) if C is not None else None
+            M, N = A.shape[0], B.shape[1]
+            if out_dtype is None:
+                out_dtype = _dt_name(D) if D is not None else (_dt_name(C) if C is not None else "f32")
+            tdt = getattr(torch, _TORCH_DT[out_dtype])
+            Dd = st.get("D")
+            if Dd is None or Dd.shape != (M, N) or Dd.dtype != tdt:
+                Dd = torch.empty((M, N), dtype=tdt, device=dev)
+                st["D"] = Dd
+            self.gemm(Ad, Bd, Cd, Dd, alpha=alpha, beta=beta, accum_dtype=accum_dtype,
+                      out_dtype=out_dtype, stream=s.cuda_stream)
+            if D is None:
+                D = torch.empty((M, N), dtype=tdt, pin_memory=True)
+            D.copy_(Dd, non_blocking=True)
+        s.synchronize()
+        return D
