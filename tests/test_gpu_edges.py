@@ -65,7 +65,7 @@ def test_k_zero_is_beta_c(plan, beta):
 
 
 def test_beta_zero_never_reads_c(plan):
-    w = W(200, 300, 136)
+    w = W(200, 304, 136)
     h = wl.make_inputs(w, integer=True)
     A, B = h.A.cuda(), h.B.cuda()
     C = torch.full((w.M, w.N), float("nan"), device="cuda")
