@@ -49,7 +49,30 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--flush", choices=["write", "write_read", "none"], default="write_read",
+                    help="L2 hygiene between steps: write a 256 MiB buffer (leaves it dirty in L2), "
+                         "write then read it back (L2 left clean, holding none of the inputs), or none")
+    # overrides of the workload (exploration; the JSON config records the result)
+    ap.add_argument("--M", type=int)
+    ap.add_argument("--N", type=int)
+    ap.add_argument("--K", type=int)
+    ap.add_argument("--layoutA", choices=["row", "col"])
+    ap.add_argument("--layoutB", choices=["row", "col"])
+    ap.add_argument("--accum", choices=["f32", "f16"])
+    ap.add_argument("--out", choices=["f32", "f16", "bf16"])
     return ap.parse_args()
+
+
+def select_workload(args):
+    import dataclasses
+    import workloads as wl
+    w = wl.WORKLOADS[args.workload]
+    over = {k: v for k, v in (("M", args.M), ("N", args.N), ("K", args.K), ("layoutA", args.layoutA),
+                              ("layoutB", args.layoutB), ("accum_dtype", args.accum),
+                              ("out_dtype", args.out)) if v is not None}
+    if over:
+        w = dataclasses.replace(w, name=w.name + "+" + ",".join(f"{k}={v}" for k, v in over.items()), **over)
+    return w
 
 
 def measured_peaks():
@@ -185,7 +208,7 @@ def run_reference(args):
         return 0
     import oracle
     import workloads as wl
-    w = wl.WORKLOADS[args.workload]
+    w = select_workload(args)
     h = wl.make_inputs(w)
     cores = os.cpu_count() or 1
     A, B = wl.bits(h.A), wl.bits(h.B)
@@ -243,13 +266,21 @@ def main():
         if dist:
             dist.barrier()
 
-    w = wl.WORKLOADS[args.workload]
+    w = select_workload(args)
     h = wl.make_inputs(w)
     A = h.A.to(dev)
     B = h.B.to(dev)
     C = None if h.C is None else h.C.to(dev)
     D = torch.empty((w.M, h.ldc), dtype=wl.DTYPES[w.out_dtype], device=dev)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flush_sink = torch.empty((), dtype=torch.float32, device=dev)
+
+    def flush_l2(i):
+        if args.flush == "none":
+            return
+        flush.fill_(float(i))                 # evicts everything else from L2 ...
+        if args.flush == "write_read":
+            torch.sum(flush, dim=0, out=flush_sink)  # ... and leaves it clean (written back, re-read)
     plan = tc.Plan(w.in_dtype, local)
     A_l = wl.logical(A, w.M, w.K, w.layoutA)
     B_l = wl.logical(B, w.K, w.N, w.layoutB)
@@ -261,8 +292,8 @@ def main():
         plan.gemm(A_l, B_l, C_l, D_l, alpha=w.alpha, beta=w.beta, accum_dtype=w.accum_dtype,
                   out_dtype=w.out_dtype, stream=stream.cuda_stream)
 
-    for _ in range(args.warmup):
-        flush.fill_(1.0)
+    for i in range(args.warmup):
+        flush_l2(i)
         step()
     torch.cuda.synchronize()
 
@@ -279,7 +310,7 @@ def main():
     launches0 = plan.launches
     wall0 = time.perf_counter()
     for i in range(args.steps):
-        flush.fill_(float(i))
+        flush_l2(i)
         starts[i].record(stream)
         step()
         ends[i].record(stream)
@@ -358,7 +389,12 @@ def main():
         "config": {
             "workload": workload_desc(w),
             "accumulate": w.accum_dtype, "out": w.out_dtype,
-            "l2": f"flushed before every step ({L2_FLUSH_BYTES >> 20} MiB write, outside the step's events)",
+            "l2": {"write": f"flushed before every step by a {L2_FLUSH_BYTES >> 20} MiB write (outside the "
+                            "step's events; the dirty lines are written back during the step)",
+                   "write_read": f"flushed before every step by a {L2_FLUSH_BYTES >> 20} MiB write followed by "
+                                 "a read of the same buffer (outside the step's events): L2 holds no input "
+                                 "and no dirty line when the step starts",
+                   "none": "not flushed (inputs may be L2-resident)"}[args.flush],
             "parallelism": "replicas" if world > 1 else "single",
             "pct_of_nominal_dense_fp16": 100.0 * value / world / NOMINAL_DENSE_FP16_TFLOPS,
             "nominal_dense_fp16_tflops": NOMINAL_DENSE_FP16_TFLOPS,

@@ -114,6 +114,28 @@ int gemm_plan_device_error_site(gemm_plan_t plan);
  * status word and the kernel winds down and returns instead of hanging. */
 gemm_status_t gemm_plan_set_timeout_ns(gemm_plan_t plan, uint64_t ns);
 
+/* Kernel configurations (tile rows x columns, CTAs per tile).  The plan
+ * normally picks one per call from the problem shape; these values name them
+ * for gemm_plan_force_config and appear in gemm_plan_describe's text. */
+typedef enum {
+    GEMM_CONFIG_AUTO = -1,
+    GEMM_CONFIG_SINGLE_128x16 = 0,    /* transposed product, at most 16 rows */
+    GEMM_CONFIG_SINGLE_128x64 = 1,    /* transposed product, at most 64 rows */
+    GEMM_CONFIG_SINGLE_128x256 = 2,   /* one CTA per 128 x 256 tile */
+    GEMM_CONFIG_PAIR_256x256 = 3,     /* a CTA pair per 256 x 256 tile */
+    GEMM_CONFIG_PAIR_256x224 = 4      /* a CTA pair per 256 x 224 tile */
+} gemm_config_t;
+
+/* Pin the kernel configuration and the number of K splits (1..16) used by
+ * this plan's later gemm_run calls (GEMM_CONFIG_AUTO restores the automatic
+ * choice; `splits` <= 0 lets the plan pick the split count for the pinned
+ * configuration).  The two transposed-product configurations apply only to
+ * problems with M <= 16 (resp. 64) and the others only to M > 64; a call
+ * whose shape does not fit the pinned configuration, or whose K has fewer
+ * 64-deep blocks than `splits`, returns GEMM_ERR_UNSUPPORTED.  fp16
+ * accumulation is never split. */
+gemm_status_t gemm_plan_force_config(gemm_plan_t plan, gemm_config_t config, int splits);
+
 /* Number of kernels this plan has launched so far. */
 uint64_t gemm_plan_launch_count(gemm_plan_t plan);
 

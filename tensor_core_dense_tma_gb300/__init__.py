@@ -31,6 +31,7 @@ __all__ = [
     "gemm_plan_create", "gemm_run", "gemm_validate", "gemm_plan_device_status",
     "gemm_plan_device_error_site", "gemm_plan_set_timeout_ns", "gemm_plan_launch_count",
     "gemm_plan_sm_count", "gemm_plan_describe", "gemm_plan_destroy", "gemm_status_string",
+    "gemm_plan_force_config", "CONFIG",
 ]
 
 STATUS = {
@@ -64,6 +65,8 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.gemm_plan_device_error_site.restype = i32
     lib.gemm_plan_set_timeout_ns.argtypes = [p, u64]
     lib.gemm_plan_set_timeout_ns.restype = i32
+    lib.gemm_plan_force_config.argtypes = [p, i32, i32]
+    lib.gemm_plan_force_config.restype = i32
     lib.gemm_plan_launch_count.argtypes = [p]
     lib.gemm_plan_launch_count.restype = u64
     lib.gemm_plan_sm_count.argtypes = [p]
@@ -138,6 +141,14 @@ def gemm_plan_device_error_site(plan) -> int:
 
 def gemm_plan_set_timeout_ns(plan, ns: int) -> int:
     return load().gemm_plan_set_timeout_ns(plan, ns)
+
+
+CONFIG = {"auto": -1, "single_128x16": 0, "single_128x64": 1, "single_128x256": 2, "pair_256x256": 3,
+          "pair_256x224": 4}
+
+
+def gemm_plan_force_config(plan, config: str | int = "auto", splits: int = 0) -> int:
+    return load().gemm_plan_force_config(plan, CONFIG[config] if isinstance(config, str) else config, splits)
 
 
 def gemm_plan_launch_count(plan) -> int:
@@ -232,6 +243,13 @@ class Plan:
         st = gemm_plan_set_timeout_ns(self.handle, ns)
         if st != 0:
             raise GemmError(st, "gemm_plan_set_timeout_ns")
+
+    def force_config(self, config: str | int = "auto", splits: int = 0):
+        """Pin the kernel configuration (and split count) of later calls;
+        "auto" restores the automatic choice."""
+        st = gemm_plan_force_config(self.handle, config, splits)
+        if st != 0:
+            raise GemmError(st, "gemm_plan_force_config")
 
     def describe(self, M, N, K, layoutA="row", layoutB="row", accum_dtype="f32", out_dtype="f32") -> str:
         return gemm_plan_describe(self.handle, M, N, K, layoutA, layoutB, accum_dtype, out_dtype)

@@ -1,11 +1,14 @@
 """Compile the sm_103a GEMM library (``_build/libtcdt_gemm.so``) with nvcc.
 
-One translation unit, one ``-gencode`` (compute_103a -> sm_103a), the CUDA
-runtime linked statically so the library loads on a machine without a GPU
-driver (the tests that only inspect its exports run there).
+One ``-gencode`` (compute_103a -> sm_103a).  The C-ABI translation unit and
+one translation unit per kernel tile configuration are compiled in parallel
+and linked into one shared library, with the CUDA runtime linked statically
+so the library loads on a machine without a GPU driver (the tests that only
+inspect its exports run there).
 """
 from __future__ import annotations
 
+import concurrent.futures
 import glob
 import os
 import shutil
@@ -19,14 +22,14 @@ OUT_DIR = os.path.join(PKG, "_build")
 LIB_NAME = "libtcdt_gemm.so"
 LIB_PATH = os.path.join(OUT_DIR, LIB_NAME)
 
-SOURCES = [os.path.join(CSRC, "gemm_api.cu")]
+SOURCES = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
 
-NVCC_FLAGS = [
+COMPILE_FLAGS = [
     "-gencode", "arch=compute_103a,code=sm_103a",
     "-O3", "-lineinfo", "-std=c++17",
-    "-Xcompiler", "-fPIC", "-shared",
-    "-cudart", "static",
+    "-Xcompiler", "-fPIC",
 ]
+LINK_FLAGS = ["-shared", "-gencode", "arch=compute_103a,code=sm_103a", "-cudart", "static"]
 
 
 def nvcc_path() -> str:
@@ -56,13 +59,32 @@ def build(force: bool = False, extra_flags: list[str] | None = None, out: str = 
     if not force and not extra_flags and up_to_date(out):
         return out
     os.makedirs(os.path.dirname(out), exist_ok=True)
+    nvcc = nvcc_path()
+    obj_dir = os.path.join(os.path.dirname(out), f"obj{os.getpid()}")
+    os.makedirs(obj_dir, exist_ok=True)
+
+    def compile_one(src):
+        obj = os.path.join(obj_dir, os.path.basename(src) + ".o")
+        cmd = [nvcc, *COMPILE_FLAGS, *(extra_flags or []), "-I", INCLUDE, "-I", CSRC, "-c", "-o", obj, src]
+        if verbose:
+            print(" ".join(cmd), flush=True)
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError(f"nvcc failed on {src}:\n{r.stdout}\n{r.stderr}")
+        return obj
+
+    workers = max(1, min(len(SOURCES), os.cpu_count() or 1))
+    with concurrent.futures.ThreadPoolExecutor(workers) as ex:
+        objs = list(ex.map(compile_one, SOURCES))
     tmp = out + f".tmp{os.getpid()}"
-    cmd = [nvcc_path(), *NVCC_FLAGS, *(extra_flags or []), "-I", INCLUDE, "-I", CSRC,
-           "-o", tmp, *SOURCES]
+    cmd = [nvcc, *LINK_FLAGS, "-o", tmp, *objs]
     if verbose:
         print(" ".join(cmd), flush=True)
     subprocess.run(cmd, check=True)
     os.replace(tmp, out)
+    for o in objs:
+        os.remove(o)
+    os.rmdir(obj_dir)
     return out
 
 

@@ -1,34 +1,23 @@
-// gemm_api.cu -- the C ABI (include/gemm.h): argument checks, plans, TMA
-// tensor maps, kernel-configuration choice and launch.
+// gemm_api.cu -- the C ABI (include/gemm.h): argument checks, plans, the
+// choice of kernel configuration, and dispatch to the per-configuration
+// translation units.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
 #include <cstdio>
 #include <cstring>
-#include <mutex>
 #include <new>
+#include <string>
 
 #include "gemm.h"
-#include "gemm_kernel.cuh"
+#include "gemm_internal.cuh"
+
+using namespace tcdt_host;
 
 namespace {
 
-using tcdt::KernelParams;
-
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
 constexpr int64_t kMaxDim = 0x7FFFF000;   // TMA coordinates are int32; keep tile origins in range
-
-// Kernel configurations.  BM is fixed at 128 (one CTA, 128 TMEM lanes);
-// BN = 256 with 4 pipeline stages of 48 KB.
-using CfgF32F32 = tcdt::TileConfig<128, 256, 4, false, tcdt::kOutF32>;
-using CfgF32F16 = tcdt::TileConfig<128, 256, 4, false, tcdt::kOutF16>;
-using CfgF32BF16 = tcdt::TileConfig<128, 256, 4, false, tcdt::kOutBF16>;
-using CfgF16F16 = tcdt::TileConfig<128, 256, 4, true, tcdt::kOutF16>;
 
 bool valid_dtype(int d) { return d == GEMM_F16 || d == GEMM_BF16 || d == GEMM_F32; }
 bool valid_layout(int l) { return l == GEMM_ROW_MAJOR || l == GEMM_COL_MAJOR; }
@@ -66,7 +55,7 @@ gemm_status_t validate(gemm_dtype_t in, const void* A, const void* B, const void
         if (beta != 0.0f && reinterpret_cast<uintptr_t>(C) % esz) return GEMM_ERR_MISALIGNED;
     }
     if (ldc > (int64_t(1) << 40)) return GEMM_ERR_UNSUPPORTED;
-    const int64_t nm = (M + 127) / 128, nn = (N + 63) / 64;
+    const int64_t nm = (M + 15) / 16, nn = (N + 15) / 16;
     if (nm * nn > 0x7FFFFFFF) return GEMM_ERR_UNSUPPORTED;
     if (K == 0) return GEMM_OK;              // D = beta * C; A and B unused
     const int64_t lda_min = la == GEMM_ROW_MAJOR ? K : M;
@@ -96,100 +85,99 @@ struct DeviceGuard {
     }
 };
 
-}  // namespace
-
-struct gemm_plan {
-    int device = 0;
-    int sm_count = 0;
-    gemm_dtype_t in_dtype = GEMM_F16;
-    int* d_status = nullptr;      // [0] status, [1] site
-    uint64_t timeout_ns = 2000000000ull;
-    uint64_t launches = 0;
-    EncodeTiledFn encode = nullptr;
-    bool smem_attr_set[4] = {false, false, false, false};
-};
-
-namespace {
-
-// 2-D tensor map over a matrix whose contiguous dimension has `inner`
-// elements (rows of `ld` elements), 128-byte swizzle, zero fill outside.
-gemm_status_t encode_map(const gemm_plan* plan, CUtensorMap* map, const void* ptr, uint64_t inner,
-                         uint64_t outer, uint64_t ld, uint32_t box_inner, uint32_t box_outer) {
-    const cuuint64_t dims[2] = {inner, outer};
-    const cuuint64_t strides[1] = {ld * 2};
-    const cuuint32_t box[2] = {box_inner, box_outer};
-    const cuuint32_t estr[2] = {1, 1};
-    const CUtensorMapDataType dt = plan->in_dtype == GEMM_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
-                                                              : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-    CUresult r = plan->encode(map, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr,
-                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_CUDA;
+// The problem the kernel computes (see Problem).
+Problem make_problem(bool swap, const void* A, const void* B, int64_t M, int64_t N, int64_t K, int64_t lda,
+                     int64_t ldb, gemm_layout_t la, gemm_layout_t lb) {
+    auto flip = [](gemm_layout_t l) { return l == GEMM_ROW_MAJOR ? GEMM_COL_MAJOR : GEMM_ROW_MAJOR; };
+    if (!swap) return Problem{false, A, B, M, N, K, lda, ldb, la, lb};
+    return Problem{true, B, A, N, M, K, ldb, lda, flip(lb), flip(la)};
 }
 
-// tcgen05 instruction descriptor, kind::f16:
-//   [4,6) D type (0 f16, 1 f32)   [7,10) A type (0 f16, 1 bf16)   [10,13) B type
-//   [15] A MN-major   [16] B MN-major   [17,23) N >> 3   [24,29) M >> 4
-uint32_t make_idesc(bool acc_f32, bool bf16, bool a_mn, bool b_mn, int mma_m, int mma_n) {
-    uint32_t d = 0;
-    d |= (acc_f32 ? 1u : 0u) << 4;
-    d |= (bf16 ? 1u : 0u) << 7;
-    d |= (bf16 ? 1u : 0u) << 10;
-    d |= (a_mn ? 1u : 0u) << 15;
-    d |= (b_mn ? 1u : 0u) << 16;
-    d |= static_cast<uint32_t>(mma_n >> 3) << 17;
-    d |= static_cast<uint32_t>(mma_m >> 4) << 24;
-    return d;
+int default_units(const gemm_plan* plan, int kind) {
+    const int u = plan->units[kind];
+    return u > 0 ? u : plan->sm_count / kCfgCtas[kind];
 }
 
-template <class Cfg>
-gemm_status_t launch_tc(gemm_plan* plan, int cfg_slot, const void* A, const void* B, const void* C,
-                        void* D, int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
-                        int64_t ldc, gemm_layout_t la, gemm_layout_t lb, float alpha, float beta,
-                        cudaStream_t stream) {
-    const bool a_mn = la == GEMM_COL_MAJOR;   // column-major A is M-contiguous
-    const bool b_mn = lb == GEMM_ROW_MAJOR;   // row-major B is N-contiguous
-    CUtensorMap tmA, tmB;
-    gemm_status_t st;
-    if (a_mn) st = encode_map(plan, &tmA, A, M, K, lda, 64, 64);
-    else st = encode_map(plan, &tmA, A, K, M, lda, 64, Cfg::BM);
-    if (st != GEMM_OK) return st;
-    if (b_mn) st = encode_map(plan, &tmB, B, N, K, ldb, 64, 64);
-    else st = encode_map(plan, &tmB, B, K, N, ldb, 64, Cfg::BN);
-    if (st != GEMM_OK) return st;
-
-    KernelParams p{};
-    p.M = static_cast<int32_t>(M);
-    p.N = static_cast<int32_t>(N);
-    p.K = static_cast<int32_t>(K);
-    p.num_m_blocks = static_cast<int32_t>((M + Cfg::BM - 1) / Cfg::BM);
-    p.num_n_blocks = static_cast<int32_t>((N + Cfg::BN - 1) / Cfg::BN);
-    p.num_k_blocks = static_cast<int32_t>((K + Cfg::BK - 1) / Cfg::BK);
-    p.num_tiles = p.num_m_blocks * p.num_n_blocks;
-    p.group_m = 8;
-    p.ldc = ldc;
-    p.C = C;
-    p.D = D;
-    p.alpha = alpha;
-    p.beta = beta;
-    p.idesc = make_idesc(!Cfg::ACC_F16, plan->in_dtype == GEMM_BF16, a_mn, b_mn, Cfg::BM, Cfg::BN);
-    p.a_mn_major = a_mn;
-    p.b_mn_major = b_mn;
-    p.status = plan->d_status;
-    p.timeout_ns = plan->timeout_ns;
-
-    auto kern = tcdt::gemm_sm103_kernel<Cfg>;
-    if (!plan->smem_attr_set[cfg_slot]) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES) !=
-            cudaSuccess)
-            return GEMM_ERR_CUDA;
-        plan->smem_attr_set[cfg_slot] = true;
+// Configuration, K-split count and orientation with the smallest modelled
+// time: waves of work items times the per-item cost times the tile width.
+// The per-item cost, in 64-deep k-blocks, is the item's k-blocks plus a
+// fixed per-item overhead of 4, plus for a split the partial-sum traffic
+// (2 + splits * BN / 64: every split writes its fp32 partial and the last
+// one reads them all back).  One CTA per 128 x 256 tile is charged 15 %
+// more per column than a CTA pair (it re-reads B for every 128 rows).
+// `valid` is false when a pinned configuration does not fit the problem.
+Choice choose(const gemm_plan* plan, int64_t M, int64_t N, int64_t K, gemm_dtype_t acc, bool* valid) {
+    Choice best;
+    *valid = true;
+    const bool swap = M <= 64 && N > M;
+    const int64_t Mk = swap ? N : M, Nk = swap ? M : N;
+    const int64_t kb = (K + 63) / 64;
+    int cands[3];
+    int nc = 0;
+    if (plan->forced_kind >= 0) {
+        const int f = plan->forced_kind;
+        const bool f_swap = f == kCfgSingle16 || f == kCfgSingle64;
+        if (f_swap != swap || (f_swap && Nk > kCfgTileN[f])) {
+            *valid = false;
+            return best;
+        }
+        cands[nc++] = f;
+    } else if (swap) {
+        cands[nc++] = Nk <= 16 ? kCfgSingle16 : kCfgSingle64;
+    } else {
+        cands[nc++] = kCfgPair256;
+        cands[nc++] = kCfgPair224;
+        cands[nc++] = kCfgSingle256;
     }
-    const int grid = p.num_tiles < plan->sm_count ? p.num_tiles : plan->sm_count;
-    kern<<<grid, Cfg::NUM_THREADS, Cfg::SMEM_BYTES, stream>>>(tmA, tmB, p);
-    if (cudaGetLastError() != cudaSuccess) return GEMM_ERR_CUDA;
-    ++plan->launches;
-    return GEMM_OK;
+    double best_cost = -1.0;
+    for (int ci = 0; ci < nc; ++ci) {
+        const int kind = cands[ci];
+        const int64_t units = default_units(plan, kind);
+        const int64_t tiles = ((Mk + kCfgTileM[kind] - 1) / kCfgTileM[kind]) *
+                              ((Nk + kCfgTileN[kind] - 1) / kCfgTileN[kind]);
+        const int64_t tile_bytes = int64_t(kCfgCtas[kind]) * 128 * kCfgTileN[kind] * 4;
+        int64_t smax = acc == GEMM_F16 ? 1 : kMaxSplits;       // fp16 accumulation is never split
+        if (smax > kb) smax = kb;
+        while (smax > 1 && (tiles * smax * tile_bytes > static_cast<int64_t>(kWorkspaceBytes) ||
+                            tiles * kCfgCtas[kind] > kNumCounters))
+            --smax;
+        int64_t smin = 1;
+        if (plan->forced_kind >= 0 && plan->forced_splits > 0) {
+            if (plan->forced_splits > smax) {
+                *valid = false;
+                return best;
+            }
+            smin = smax = plan->forced_splits;
+        } else if (smax > 1 && tiles >= units) {
+            smax = 1;                                          // enough tiles: no split
+        }
+        const double eff = kind == kCfgSingle256 ? 1.15 : 1.0;
+        for (int64_t s = smin; s <= smax; ++s) {
+            const int64_t work = tiles * s;
+            const int64_t waves = (work + units - 1) / units;
+            const double reduce = s > 1 ? 2.0 + static_cast<double>(s) * kCfgTileN[kind] / 64.0 : 0.0;
+            const double per_item = static_cast<double>((kb + s - 1) / s + 4) + reduce;
+            const double cost = static_cast<double>(waves) * per_item * kCfgTileN[kind] * eff;
+            if (best_cost < 0 || cost < best_cost) {
+                best_cost = cost;
+                best.kind = kind;
+                best.splits = static_cast<int>(s);
+                best.swap = swap;
+                best.tiles = tiles;
+                best.units = static_cast<int>(units);
+            }
+        }
+    }
+    return best;
+}
+
+gemm_status_t prepare_all(gemm_plan* plan) {
+    gemm_status_t st = prepare_single16(plan, 0);
+    if (st == GEMM_OK) st = prepare_single64(plan, 0);
+    if (st == GEMM_OK) st = prepare_single256(plan, 0);
+    if (st == GEMM_OK) st = prepare_pair256(plan, 0);
+    if (st == GEMM_OK) st = prepare_pair224(plan, 0);
+    return st;
 }
 
 gemm_status_t launch_scale(gemm_plan* plan, const void* C, void* D, int64_t M, int64_t N, int64_t ldc,
@@ -206,11 +194,13 @@ gemm_status_t launch_scale(gemm_plan* plan, const void* C, void* D, int64_t M, i
     return GEMM_OK;
 }
 
-const char* config_name(gemm_dtype_t acc, gemm_dtype_t out) {
-    if (acc == GEMM_F16) return "tc128x256s4_acc16_out16";
-    if (out == GEMM_F32) return "tc128x256s4_acc32_out32";
-    if (out == GEMM_F16) return "tc128x256s4_acc32_out16";
-    return "tc128x256s4_acc32_outbf16";
+std::string config_name(const Choice& ch, gemm_dtype_t acc, gemm_dtype_t out) {
+    static const char* outs[4] = {"acc32_out32", "acc32_out16", "acc32_outbf16", "acc16_out16"};
+    std::string s = "tc" + std::to_string(kCfgCtas[ch.kind]) + "cta_" + std::to_string(kCfgTileM[ch.kind]) + "x" +
+                    std::to_string(kCfgTileN[ch.kind]) + "_" + outs[out_slot(acc, out)];
+    if (ch.swap) s += "_swapAB";
+    if (ch.splits > 1) s += "_splitk" + std::to_string(ch.splits);
+    return s;
 }
 
 }  // namespace
@@ -250,9 +240,17 @@ gemm_status_t gemm_plan_create(gemm_plan_t* out, int device, gemm_dtype_t in_dty
         return GEMM_ERR_CUDA;
     }
     plan->encode = reinterpret_cast<EncodeTiledFn>(fn);
-    if (cudaMalloc(&plan->d_status, 2 * sizeof(int)) != cudaSuccess ||
-        cudaMemset(plan->d_status, 0, 2 * sizeof(int)) != cudaSuccess) {
+    bool ok = cudaMalloc(&plan->d_status, 2 * sizeof(int)) == cudaSuccess &&
+              cudaMemset(plan->d_status, 0, 2 * sizeof(int)) == cudaSuccess &&
+              cudaMalloc(&plan->d_ws, kWorkspaceBytes) == cudaSuccess &&
+              cudaMalloc(&plan->d_counters, kNumCounters * sizeof(int)) == cudaSuccess &&
+              cudaMemset(plan->d_counters, 0, kNumCounters * sizeof(int)) == cudaSuccess &&
+              prepare_all(plan) == GEMM_OK;
+    if (!ok) {
+        cudaGetLastError();
         if (plan->d_status) cudaFree(plan->d_status);
+        if (plan->d_ws) cudaFree(plan->d_ws);
+        if (plan->d_counters) cudaFree(plan->d_counters);
         delete plan;
         return GEMM_ERR_CUDA;
     }
@@ -281,17 +279,18 @@ gemm_status_t gemm_run(gemm_plan_t plan, const void* A, const void* B, const voi
     if (!guard.ok) return GEMM_ERR_CUDA;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (K == 0) return launch_scale(plan, C, D, M, N, ldc, out_dtype, beta, s);
-    if (accum_dtype == GEMM_F16)
-        return launch_tc<CfgF16F16>(plan, 3, A, B, C, D, M, N, K, lda, ldb, ldc, layoutA, layoutB, alpha,
-                                    beta, s);
-    if (out_dtype == GEMM_F32)
-        return launch_tc<CfgF32F32>(plan, 0, A, B, C, D, M, N, K, lda, ldb, ldc, layoutA, layoutB, alpha,
-                                    beta, s);
-    if (out_dtype == GEMM_F16)
-        return launch_tc<CfgF32F16>(plan, 1, A, B, C, D, M, N, K, lda, ldb, ldc, layoutA, layoutB, alpha,
-                                    beta, s);
-    return launch_tc<CfgF32BF16>(plan, 2, A, B, C, D, M, N, K, lda, ldb, ldc, layoutA, layoutB, alpha, beta,
-                                 s);
+    bool valid = true;
+    const Choice ch = choose(plan, M, N, K, accum_dtype, &valid);
+    if (!valid) return GEMM_ERR_UNSUPPORTED;
+    const Problem pr = make_problem(ch.swap, A, B, M, N, K, lda, ldb, layoutA, layoutB);
+    const int slot = out_slot(accum_dtype, out_dtype);
+    switch (ch.kind) {
+        case kCfgSingle16: return launch_single16(plan, slot, ch, pr, C, D, ldc, alpha, beta, s);
+        case kCfgSingle64: return launch_single64(plan, slot, ch, pr, C, D, ldc, alpha, beta, s);
+        case kCfgSingle256: return launch_single256(plan, slot, ch, pr, C, D, ldc, alpha, beta, s);
+        case kCfgPair224: return launch_pair224(plan, slot, ch, pr, C, D, ldc, alpha, beta, s);
+        default: return launch_pair256(plan, slot, ch, pr, C, D, ldc, alpha, beta, s);
+    }
 }
 
 gemm_status_t gemm_plan_device_status(gemm_plan_t plan, int clear) {
@@ -299,7 +298,12 @@ gemm_status_t gemm_plan_device_status(gemm_plan_t plan, int clear) {
     DeviceGuard guard(plan->device);
     int h[2] = {0, 0};
     if (cudaMemcpy(h, plan->d_status, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return GEMM_ERR_CUDA;
-    if (clear && cudaMemset(plan->d_status, 0, sizeof(h)) != cudaSuccess) return GEMM_ERR_CUDA;
+    if (clear) {
+        // an aborted launch can leave split-K counters behind: clear them too
+        if (cudaMemset(plan->d_status, 0, sizeof(h)) != cudaSuccess ||
+            cudaMemset(plan->d_counters, 0, kNumCounters * sizeof(int)) != cudaSuccess)
+            return GEMM_ERR_CUDA;
+    }
     return static_cast<gemm_status_t>(h[0]);
 }
 
@@ -317,6 +321,16 @@ gemm_status_t gemm_plan_set_timeout_ns(gemm_plan_t plan, uint64_t ns) {
     return GEMM_OK;
 }
 
+gemm_status_t gemm_plan_force_config(gemm_plan_t plan, gemm_config_t config, int splits) {
+    if (!plan) return GEMM_ERR_INVALID_ARG;
+    if (config != GEMM_CONFIG_AUTO && (static_cast<int>(config) < 0 || static_cast<int>(config) >= kNumCfgKinds))
+        return GEMM_ERR_INVALID_ARG;
+    if (splits > kMaxSplits) return GEMM_ERR_INVALID_ARG;
+    plan->forced_kind = config == GEMM_CONFIG_AUTO ? -1 : static_cast<int>(config);
+    plan->forced_splits = config == GEMM_CONFIG_AUTO ? 0 : (splits > 0 ? splits : 0);
+    return GEMM_OK;
+}
+
 uint64_t gemm_plan_launch_count(gemm_plan_t plan) { return plan ? plan->launches : 0; }
 
 int gemm_plan_sm_count(gemm_plan_t plan) { return plan ? plan->sm_count : 0; }
@@ -330,11 +344,22 @@ gemm_status_t gemm_plan_describe(gemm_plan_t plan, int64_t M, int64_t N, int64_t
                                 lda < 8 ? 8 : (lda + 7) / 8 * 8, ldb < 8 ? 8 : (ldb + 7) / 8 * 8, N,
                                 layoutA, layoutB, accum_dtype, out_dtype, 0.0f, false);
     if (st != GEMM_OK) return st;
-    const char* name = K == 0 ? "scale_c" : config_name(accum_dtype, out_dtype);
-    const int64_t tiles = ((M + 127) / 128) * ((N + 255) / 256);
-    const int64_t grid = tiles < plan->sm_count ? tiles : plan->sm_count;
-    std::snprintf(buf, static_cast<size_t>(len), "%s tiles=%lld grid=%lld sms=%d", name,
-                  static_cast<long long>(tiles), static_cast<long long>(grid), plan->sm_count);
+    if (M == 0 || N == 0) {
+        std::snprintf(buf, static_cast<size_t>(len), "none (empty output)");
+        return GEMM_OK;
+    }
+    if (K == 0) {
+        std::snprintf(buf, static_cast<size_t>(len), "scale_c (K = 0)");
+        return GEMM_OK;
+    }
+    bool valid = true;
+    const Choice ch = choose(plan, M, N, K, accum_dtype, &valid);
+    if (!valid) return GEMM_ERR_UNSUPPORTED;
+    const int64_t work = ch.tiles * ch.splits;
+    const int64_t units = work < ch.units ? work : ch.units;
+    std::snprintf(buf, static_cast<size_t>(len), "%s tiles=%lld splits=%d ctas=%lld sms=%d",
+                  config_name(ch, accum_dtype, out_dtype).c_str(), static_cast<long long>(ch.tiles), ch.splits,
+                  static_cast<long long>(units * kCfgCtas[ch.kind]), plan->sm_count);
     return GEMM_OK;
 }
 
@@ -343,6 +368,8 @@ gemm_status_t gemm_plan_destroy(gemm_plan_t plan) {
     {
         DeviceGuard guard(plan->device);
         if (plan->d_status) cudaFree(plan->d_status);
+        if (plan->d_ws) cudaFree(plan->d_ws);
+        if (plan->d_counters) cudaFree(plan->d_counters);
     }
     delete plan;
     return GEMM_OK;

@@ -1,0 +1,273 @@
+// gemm_internal.cuh -- shared by the C-ABI translation unit and the per-
+// configuration kernel translation units: the plan, the configuration
+// table, the chosen launch (Choice, Problem) and the launch templates.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <string>
+
+#include "gemm.h"
+#include "gemm_kernel.cuh"
+
+namespace tcdt_host {
+
+using tcdt::KernelParams;
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// Split-K scratch owned by a plan: fp32 partial tiles and arrival counters.
+constexpr size_t kWorkspaceBytes = size_t(32) << 20;
+constexpr int kNumCounters = 8192;
+constexpr int kMaxSplits = 16;
+
+// Kernel configurations (tile rows x tile columns, CTAs per tile, stages):
+//  single16 / single64 : one CTA, 128 x 16 / 128 x 64, 8 stages -- the
+//                        transposed product of problems with at most 16 / 64
+//                        rows (D^T = B^T A^T puts the long N side on the
+//                        128-row MMA dimension);
+//  single256           : one CTA, 128 x 256, 4 stages of 48 KB;
+//  pair256             : CTA pair (cta_group::2), 256 x 256, 7 stages of 32 KB per CTA;
+//  pair224             : CTA pair, 256 x 224 (fills whole waves where 256 leaves a
+//                        partial one, e.g. N = 4096: 19 column tiles x 16 = 4 x 76 pairs).
+template <bool ACC16, int OUT>
+using CfgSingle16 = tcdt::TileConfig<16, 8, 1, ACC16, OUT>;
+template <bool ACC16, int OUT>
+using CfgSingle64 = tcdt::TileConfig<64, 8, 1, ACC16, OUT>;
+template <bool ACC16, int OUT>
+using CfgSingle256 = tcdt::TileConfig<256, 4, 1, ACC16, OUT>;
+template <bool ACC16, int OUT>
+using CfgPair256 = tcdt::TileConfig<256, 7, 2, ACC16, OUT>;
+template <bool ACC16, int OUT>
+using CfgPair224 = tcdt::TileConfig<224, 7, 2, ACC16, OUT>;
+
+enum ConfigId : int {
+    kCfgSingle16 = 0,
+    kCfgSingle64 = 1,
+    kCfgSingle256 = 2,
+    kCfgPair256 = 3,
+    kCfgPair224 = 4,
+    kNumCfgKinds = 5
+};
+constexpr int kCfgTileM[kNumCfgKinds] = {128, 128, 128, 256, 256};
+constexpr int kCfgTileN[kNumCfgKinds] = {16, 64, 256, 256, 224};
+constexpr int kCfgCtas[kNumCfgKinds] = {1, 1, 1, 2, 2};
+
+inline int out_slot(gemm_dtype_t acc, gemm_dtype_t out) {
+    if (acc == GEMM_F16) return 3;
+    return out == GEMM_F32 ? 0 : out == GEMM_F16 ? 1 : 2;
+}
+
+}  // namespace tcdt_host
+
+struct gemm_plan {
+    int device = 0;
+    int sm_count = 0;
+    gemm_dtype_t in_dtype = GEMM_F16;
+    int* d_status = nullptr;      // [0] status, [1] site
+    float* d_ws = nullptr;        // split-K partials
+    int* d_counters = nullptr;    // split-K arrival counters (kept zero between launches)
+    uint64_t timeout_ns = 2000000000ull;
+    uint64_t launches = 0;
+    tcdt_host::EncodeTiledFn encode = nullptr;
+    bool attr_set[tcdt_host::kNumCfgKinds][4] = {};
+    int units[tcdt_host::kNumCfgKinds] = {};  // co-resident CTAs (single) or CTA pairs (pair)
+    int forced_kind = -1;         // gemm_plan_force_config
+    int forced_splits = 0;
+};
+
+namespace tcdt_host {
+
+// The problem the kernel computes: (M, N) as given, or transposed with the
+// operands swapped and their storage orders flipped (B^T is a column-major
+// N x K matrix when B is a row-major K x N one, and so on).
+struct Problem {
+    bool swap;
+    const void *A, *B;
+    int64_t M, N, K, lda, ldb;
+    gemm_layout_t la, lb;
+};
+
+struct Choice {
+    int kind = kCfgPair256;
+    int splits = 1;
+    bool swap = false;
+    int64_t tiles = 0;
+    int units = 0;
+};
+
+// Per-configuration entry points (one translation unit each).
+#define TCDT_DECLARE_KIND(name)                                                                          \
+    gemm_status_t prepare_##name(gemm_plan* plan, int slot);                                             \
+    gemm_status_t launch_##name(gemm_plan* plan, int slot, const Choice& ch, const Problem& pr,          \
+                                const void* C, void* D, int64_t ldc, float alpha, float beta, cudaStream_t s);
+TCDT_DECLARE_KIND(single16)
+TCDT_DECLARE_KIND(single64)
+TCDT_DECLARE_KIND(single256)
+TCDT_DECLARE_KIND(pair256)
+TCDT_DECLARE_KIND(pair224)
+#undef TCDT_DECLARE_KIND
+
+// 2-D tensor map over a matrix whose contiguous dimension has `inner`
+// elements (rows of `ld` elements), 128-byte swizzle, zero fill outside.
+inline gemm_status_t encode_map(const gemm_plan* plan, CUtensorMap* map, const void* ptr, uint64_t inner,
+                         uint64_t outer, uint64_t ld, uint32_t box_inner, uint32_t box_outer) {
+    const cuuint64_t dims[2] = {inner, outer};
+    const cuuint64_t strides[1] = {ld * 2};
+    const cuuint32_t box[2] = {box_inner, box_outer};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUtensorMapDataType dt = plan->in_dtype == GEMM_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                              : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    CUresult r = plan->encode(map, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_CUDA;
+}
+
+// tcgen05 instruction descriptor, kind::f16:
+//   [4,6) D type (0 f16, 1 f32)   [7,10) A type (0 f16, 1 bf16)   [10,13) B type
+//   [15] A MN-major   [16] B MN-major   [17,23) N >> 3   [24,29) M >> 4
+inline uint32_t make_idesc(bool acc_f32, bool bf16, bool a_mn, bool b_mn, int mma_m, int mma_n) {
+    uint32_t d = 0;
+    d |= (acc_f32 ? 1u : 0u) << 4;
+    d |= (bf16 ? 1u : 0u) << 7;
+    d |= (bf16 ? 1u : 0u) << 10;
+    d |= (a_mn ? 1u : 0u) << 15;
+    d |= (b_mn ? 1u : 0u) << 16;
+    d |= static_cast<uint32_t>(mma_n >> 3) << 17;
+    d |= static_cast<uint32_t>(mma_m >> 4) << 24;
+    return d;
+}
+
+template <class Cfg>
+void fill_launch_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr, cudaStream_t stream) {
+    cfg = cudaLaunchConfig_t{};
+    cfg.blockDim = dim3(Cfg::NUM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
+    cfg.stream = stream;
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = Cfg::CG;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = Cfg::CG > 1 ? 1 : 0;    // the single-CTA kernels are not cluster launches
+}
+
+// Shared-memory opt-in and co-residency of one kernel instantiation.
+template <class Cfg>
+gemm_status_t prepare(gemm_plan* plan, int kind, int slot) {
+    if (plan->attr_set[kind][slot]) return GEMM_OK;
+    auto kern = tcdt::gemm_sm103_kernel<Cfg>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
+    cudaLaunchConfig_t cfg;
+    cudaLaunchAttribute attr[1];
+    fill_launch_config<Cfg>(cfg, attr, nullptr);
+    cfg.gridDim = dim3(Cfg::CG * (plan->sm_count / Cfg::CG), 1, 1);
+    int units = 0;
+    if (Cfg::CG > 1) {
+        if (cudaOccupancyMaxActiveClusters(&units, kern, &cfg) != cudaSuccess) units = 0;
+    } else {
+        int per_sm = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, Cfg::NUM_THREADS, Cfg::SMEM_BYTES) ==
+            cudaSuccess)
+            units = per_sm * plan->sm_count;
+    }
+    cudaGetLastError();
+    if (units <= 0) units = plan->sm_count / Cfg::CG;
+    if (plan->units[kind] == 0 || units < plan->units[kind]) plan->units[kind] = units;
+    plan->attr_set[kind][slot] = true;
+    return GEMM_OK;
+}
+
+template <class Cfg>
+gemm_status_t launch_tc(gemm_plan* plan, const Choice& ch, const Problem& pr, const void* C, void* D,
+                        int64_t ldc, float alpha, float beta, cudaStream_t stream) {
+    const bool a_mn = pr.la == GEMM_COL_MAJOR;   // column-major A is M-contiguous
+    const bool b_mn = pr.lb == GEMM_ROW_MAJOR;   // row-major B is N-contiguous
+    CUtensorMap tmA, tmB;
+    gemm_status_t st;
+    if (a_mn) st = encode_map(plan, &tmA, pr.A, pr.M, pr.K, pr.lda, 64, 64);
+    else st = encode_map(plan, &tmA, pr.A, pr.K, pr.M, pr.lda, 64, Cfg::BM);
+    if (st != GEMM_OK) return st;
+    if (b_mn) st = encode_map(plan, &tmB, pr.B, pr.N, pr.K, pr.ldb, 64, 64);
+    else st = encode_map(plan, &tmB, pr.B, pr.K, pr.N, pr.ldb, 64, Cfg::BN_CTA);
+    if (st != GEMM_OK) return st;
+
+    KernelParams p{};
+    p.M = static_cast<int32_t>(pr.M);
+    p.N = static_cast<int32_t>(pr.N);
+    p.K = static_cast<int32_t>(pr.K);
+    p.num_m_blocks = static_cast<int32_t>((pr.M + Cfg::UMMA_M - 1) / Cfg::UMMA_M);
+    p.num_n_blocks = static_cast<int32_t>((pr.N + Cfg::BN - 1) / Cfg::BN);
+    p.num_k_blocks = static_cast<int32_t>((pr.K + Cfg::BK - 1) / Cfg::BK);
+    p.num_tiles = p.num_m_blocks * p.num_n_blocks;
+    p.splits = ch.splits;
+    p.group_m = 8;
+    p.ldc = ldc;
+    p.C = C;
+    p.D = D;
+    p.alpha = alpha;
+    p.beta = beta;
+    p.idesc = make_idesc(!Cfg::ACC_F16, plan->in_dtype == GEMM_BF16, a_mn, b_mn, Cfg::UMMA_M, Cfg::BN);
+    p.a_mn_major = a_mn;
+    p.b_mn_major = b_mn;
+    p.trans_out = pr.swap ? 1u : 0u;
+    p.ws = plan->d_ws;
+    p.counters = plan->d_counters;
+    p.status = plan->d_status;
+    p.timeout_ns = plan->timeout_ns;
+
+    cudaLaunchConfig_t cfg;
+    cudaLaunchAttribute attr[1];
+    fill_launch_config<Cfg>(cfg, attr, stream);
+    const int64_t work = static_cast<int64_t>(p.num_tiles) * p.splits;
+    const int units = work < ch.units ? static_cast<int>(work) : ch.units;
+    cfg.gridDim = dim3(Cfg::CG * units, 1, 1);
+    if (cudaLaunchKernelEx(&cfg, tcdt::gemm_sm103_kernel<Cfg>, tmA, tmB, p) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
+    ++plan->launches;
+    return GEMM_OK;
+}
+
+template <template <bool, int> class CfgT>
+gemm_status_t prepare_kind(gemm_plan* plan, int kind, int slot) {
+    switch (slot) {
+        case 0: return prepare<CfgT<false, tcdt::kOutF32>>(plan, kind, slot);
+        case 1: return prepare<CfgT<false, tcdt::kOutF16>>(plan, kind, slot);
+        case 2: return prepare<CfgT<false, tcdt::kOutBF16>>(plan, kind, slot);
+        default: return prepare<CfgT<true, tcdt::kOutF16>>(plan, kind, slot);
+    }
+}
+
+template <template <bool, int> class CfgT>
+gemm_status_t launch_kind(gemm_plan* plan, int slot, const Choice& ch, const Problem& pr, const void* C, void* D,
+                          int64_t ldc, float alpha, float beta, cudaStream_t s) {
+    gemm_status_t st = prepare_kind<CfgT>(plan, ch.kind, slot);
+    if (st != GEMM_OK) return st;
+    switch (slot) {
+        case 0: return launch_tc<CfgT<false, tcdt::kOutF32>>(plan, ch, pr, C, D, ldc, alpha, beta, s);
+        case 1: return launch_tc<CfgT<false, tcdt::kOutF16>>(plan, ch, pr, C, D, ldc, alpha, beta, s);
+        case 2: return launch_tc<CfgT<false, tcdt::kOutBF16>>(plan, ch, pr, C, D, ldc, alpha, beta, s);
+        default: return launch_tc<CfgT<true, tcdt::kOutF16>>(plan, ch, pr, C, D, ldc, alpha, beta, s);
+    }
+}
+
+#define TCDT_DEFINE_KIND(name, CfgT, kind_id)                                                           \
+    gemm_status_t prepare_##name(gemm_plan* plan, int slot) { return prepare_kind<CfgT>(plan, kind_id, slot); } \
+    gemm_status_t launch_##name(gemm_plan* plan, int slot, const Choice& ch, const Problem& pr,          \
+                                const void* C, void* D, int64_t ldc, float alpha, float beta,            \
+                                cudaStream_t s) {                                                         \
+        return launch_kind<CfgT>(plan, slot, ch, pr, C, D, ldc, alpha, beta, s);                        \
+    }
+
+}  // namespace tcdt_host

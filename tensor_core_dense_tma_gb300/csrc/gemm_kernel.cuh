@@ -1,30 +1,37 @@
 // gemm_kernel.cuh -- the sm_103a tensor-core GEMM kernel
 //
-//   D = alpha * A * B + beta * C      (A: M x K, B: K x N, C/D: M x N row-major)
+//   D = alpha * A * B + beta * C      (A: M x K, B: K x N, C/D: M x N)
 //
 // The method is the tiled multiply-accumulate the pages build up: the output
-// is cut into BM x BN tiles, each tile sweeps K in BK-thick slices of A and B
+// is cut into tiles, each tile sweeps K in BK-thick slices of A and B
 // ("矩阵乘法优化可视化学习文档", section 4, Tiling), slices are staged in
-// shared memory and the next slice is fetched while the current one is
+// shared memory and the next slices are fetched while the current one is
 // multiplied ("深入CUDA Tensor Core与WMMA", sections 5.2 and 5.4), and the
 // multiply-accumulate D = A x B + C runs on the tensor cores (same page,
 // section 2.2).  Out-of-range rows, columns and K-slices read as zero and
 // out-of-range outputs are not written ("深入CUDA Tensor Core与WMMA",
-// section 5.2 and 7.2 item 5; "矩阵乘法优化可视化学习文档", section 8 masks).
+// sections 5.2 and 7.2 item 5; "矩阵乘法优化可视化学习文档", section 8 masks).
 //
 // How it maps onto sm_103a (the pages' WMMA / mma.sync kernels are prior art
 // for older GPUs; this is a Blackwell design):
-//   * one persistent CTA per SM walks output tiles in a grouped raster;
+//   * persistent CTAs (or CTA pairs) walk work items in a grouped raster; a
+//     work item is an output tile, or one of `splits` contiguous K ranges of
+//     a tile when there are too few tiles to fill the GPU;
 //   * warp 0, one thread: TMA loads of 128-byte-swizzled A and B slices into a
 //     STAGES-deep shared-memory ring, each stage guarded by a "full" and an
 //     "empty" mbarrier;
-//   * warp 1: allocates tensor memory (two BM x BN fp32 accumulators); one
-//     thread issues tcgen05.mma (kind::f16) for every 16-deep K step and
-//     tcgen05.commit frees the stage / publishes the finished accumulator;
+//   * warp 1: allocates tensor memory (two 128 x BN fp32 accumulators per
+//     CTA); one thread of the pair's leader issues tcgen05.mma (kind::f16)
+//     for every 16-deep K step, and tcgen05.commit frees the stage / publishes
+//     the finished accumulator;
 //   * warps 2..5: epilogue -- tcgen05.ld of the accumulator, alpha/beta*C in
-//     fp32, RNE cast, 16-byte stores where the row segment is aligned and in
-//     bounds, masked scalar stores elsewhere.  Two accumulators let the
-//     epilogue of tile t overlap the main loop of tile t+1.
+//     fp32, RNE cast, 16-byte stores for the aligned part of each row segment
+//     and element stores for the unaligned head/tail and the masked edges.
+//     Split K: every split writes its fp32 partial to a workspace; the last
+//     split to arrive adds all partials in split order (a fixed order, so the
+//     result does not depend on which split finishes last) and stores.
+//   * `trans_out`: the kernel computes the transposed product (used for
+//     D^T = B^T A^T when M is small) and stores element (r, c) at D[c*ldc + r].
 // Every mbarrier wait is bounded: when a wait exceeds the plan's limit the
 // kernel records GEMM_ERR_TIMEOUT and a site code in the status word, raises
 // a CTA-wide abort flag, waits (bounded) for its own copies and MMAs in
@@ -53,43 +60,58 @@ enum WaitSite : int {
 };
 
 struct KernelParams {
-    int32_t M, N, K;
+    int32_t M, N, K;          // of the product the kernel computes (swapped when trans_out)
     int32_t num_m_blocks, num_n_blocks, num_k_blocks, num_tiles;
+    int32_t splits;           // K ranges per tile (1: whole K)
     int32_t group_m;          // m-blocks per raster group
     int64_t ldc;
     const void* C;            // may alias D; unread when beta == 0
     void* D;
     float alpha, beta;
     uint32_t idesc;           // tcgen05 instruction descriptor
-    uint32_t a_mn_major;      // 1: A is M-contiguous (column-major)
-    uint32_t b_mn_major;      // 1: B is N-contiguous (row-major)
+    uint32_t a_mn_major;      // 1: A is M-contiguous
+    uint32_t b_mn_major;      // 1: B is N-contiguous
+    uint32_t trans_out;       // 1: element (r, c) goes to D[c*ldc + r]
+    float* ws;                // split partials, [tile][split][cta][128][BN] fp32
+    int* counters;            // [tile][cta] split arrivals; zero on entry, left zero
     int* status;              // [0] status code, [1] site
     uint64_t timeout_ns;
 };
 
-template <int BM_, int BN_, int STAGES_, bool ACC_F16_, int OUT_>
+// One output tile is UMMA_M x BN (UMMA_M = 128 * CG).  With CG == 2 a
+// cluster of two CTAs on two SMs computes it with one tcgen05.mma stream:
+// each CTA stages 128 rows of A and BN/2 columns of B and receives 128
+// rows of the accumulator in its own tensor memory.
+template <int BN_, int STAGES_, int CG_, bool ACC_F16_, int OUT_>
 struct TileConfig {
-    static constexpr int BM = BM_;
-    static constexpr int BN = BN_;
-    static constexpr int BK = 64;                 // 64 x 2 bytes = one 128-byte swizzle row
-    static constexpr int UMMA_K = 16;             // K per tcgen05.mma kind::f16
+    static constexpr int CG = CG_;                 // CTAs per MMA (1 or 2)
+    static constexpr int BM = 128;                 // accumulator rows per CTA (TMEM lanes)
+    static constexpr int UMMA_M = 128 * CG;        // tile rows
+    static constexpr int BN = BN_;                 // tile columns (MMA N)
+    static constexpr int BN_CTA = BN / CG;         // B columns staged per CTA
+    static constexpr int BK = 64;                  // 64 x 2 bytes = one 128-byte swizzle row
+    static constexpr int UMMA_K = 16;              // K per tcgen05.mma kind::f16
     static constexpr int STAGES = STAGES_;
     static constexpr bool ACC_F16 = ACC_F16_;
     static constexpr int OUT = OUT_;
+    static constexpr int W = BN < 32 ? BN : 32;    // accumulator columns per tcgen05.ld
+    static constexpr uint32_t MN_CHUNK_BYTES = 64 * BK * 2;    // 64 MN-elements x BK rows
+    static constexpr int B_CHUNKS = (BN_CTA + 63) / 64;        // MN-major B: 64-column TMA boxes
     static constexpr int A_BYTES = BM * BK * 2;
-    static constexpr int B_BYTES = BN * BK * 2;
+    static constexpr int B_BYTES = B_CHUNKS * 64 * BK * 2;     // room for whole MN-major chunks
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr int ACC_COLS = BN;           // one 32-bit TMEM column per output column
+    static constexpr int ACC_COLS = BN;            // one 32-bit TMEM column per output column
     static constexpr int TMEM_COLS = 2 * ACC_COLS <= 32 ? 32 : 2 * ACC_COLS <= 64 ? 64
                                    : 2 * ACC_COLS <= 128 ? 128 : 2 * ACC_COLS <= 256 ? 256 : 512;
     static constexpr int NUM_EPI_WARPS = 4;
     static constexpr int NUM_THREADS = 32 * (2 + NUM_EPI_WARPS);
     static constexpr int NUM_BARRIERS = 2 * STAGES + 2 + 2 + 1;
-    static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + NUM_BARRIERS * 8 + 16;
-    // swizzle-atom geometry (128-byte rows, 8-row / 1024-byte atoms)
-    static constexpr uint32_t MN_CHUNK_BYTES = 64 * BK * 2;   // 64 MN-elements x BK rows
-    static_assert(BM == 128, "one CTA drives a 128-lane accumulator");
-    static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "N tile");
+    // after the barriers: TMEM address, abort flag, 2 wait flags, 2 split flags
+    static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + NUM_BARRIERS * 8 + 32;
+    static_assert(CG == 1 || CG == 2, "CTA group");
+    static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N");
+    static_assert(BN % W == 0, "whole tcgen05.ld chunks");
+    static_assert(BN_CTA % 8 == 0, "K-major B tile rows come in 8-row swizzle atoms");
     static_assert(2 * ACC_COLS <= 512, "two accumulators must fit tensor memory");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
 };
@@ -106,6 +128,30 @@ __device__ __forceinline__ void tile_coords(const KernelParams& p, int tile, int
     nb = t / rows;
 }
 
+// Largest divisor of n that is at most cap (n >= 1).
+__host__ __device__ constexpr int largest_divisor_upto(int n, int cap) {
+    int best = 1;
+    for (int d = 1; d <= cap && d <= n; ++d)
+        if (n % d == 0) best = d;
+    return best;
+}
+
+// Work item w: split (w % splits) of tile (w / splits); the splits of a
+// tile are consecutive items, so they run at the same time on neighbouring
+// units.  Each split covers k-blocks [kb0, kb1), never empty (splits <= k-blocks).
+struct WorkItem {
+    int tile, split, kb0, kb1;
+};
+
+__device__ __forceinline__ WorkItem work_item(const KernelParams& p, int w) {
+    WorkItem x;
+    x.tile = w / p.splits;
+    x.split = w - x.tile * p.splits;
+    x.kb0 = static_cast<int>(static_cast<int64_t>(p.num_k_blocks) * x.split / p.splits);
+    x.kb1 = static_cast<int>(static_cast<int64_t>(p.num_k_blocks) * (x.split + 1) / p.splits);
+    return x;
+}
+
 struct WaitCtx {
     int* status;
     uint64_t timeout_ns;
@@ -114,13 +160,17 @@ struct WaitCtx {
 
 // Bounded wait on an mbarrier phase.  Returns false if the CTA is aborting
 // or the wait ran past the limit (then the error is recorded).
+template <bool kClusterScope = false>
 __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, const WaitCtx& w, int site) {
-    if (mbar_try_wait(bar, parity)) return true;
+    auto try_once = [&]() {
+        return kClusterScope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
+    };
+    if (try_once()) return true;
     const uint64_t t0 = globaltimer_ns();
     while (true) {
 #pragma unroll 1
         for (int i = 0; i < 64; ++i)
-            if (mbar_try_wait(bar, parity)) return true;
+            if (try_once()) return true;
         if (*w.abort_flag) return false;
         if (globaltimer_ns() - t0 > w.timeout_ns) {
             *w.abort_flag = 1;
@@ -150,14 +200,14 @@ __device__ __forceinline__ float acc_value(uint32_t r) {
 }
 
 template <int OUT>
-__device__ __forceinline__ float load_c_scalar(const void* C, int64_t off) {
+__device__ __forceinline__ float load_elem(const void* C, int64_t off) {
     if constexpr (OUT == kOutF32) return static_cast<const float*>(C)[off];
     else if constexpr (OUT == kOutF16) return __half2float(static_cast<const __half*>(C)[off]);
     else return __bfloat162float(static_cast<const __nv_bfloat16*>(C)[off]);
 }
 
 template <int OUT>
-__device__ __forceinline__ void store_scalar(void* D, int64_t off, float v) {
+__device__ __forceinline__ void store_elem(void* D, int64_t off, float v) {
     if constexpr (OUT == kOutF32) static_cast<float*>(D)[off] = v;
     else if constexpr (OUT == kOutF16) static_cast<__half*>(D)[off] = __float2half_rn(v);
     else static_cast<__nv_bfloat16*>(D)[off] = __float2bfloat16_rn(v);
@@ -174,51 +224,205 @@ __device__ __forceinline__ uint32_t pack2(float a, float b) {
     }
 }
 
-// 32 consecutive C elements of one row into v (vector loads: 16-byte aligned).
 template <int OUT>
-__device__ __forceinline__ void load_c_vec32(const void* ptr, float (&c)[32]) {
+__device__ __forceinline__ float unpack_lo(uint32_t w) {
+    const unsigned short h = static_cast<unsigned short>(w & 0xFFFFu);
+    if constexpr (OUT == kOutF16) return __half2float(__ushort_as_half(h));
+    else return __bfloat162float(__ushort_as_bfloat16(h));
+}
+
+template <int OUT>
+__device__ __forceinline__ float unpack_hi(uint32_t w) {
+    const unsigned short h = static_cast<unsigned short>(w >> 16);
+    if constexpr (OUT == kOutF16) return __half2float(__ushort_as_half(h));
+    else return __bfloat162float(__ushort_as_bfloat16(h));
+}
+
+// Elements per 16-byte access.
+template <int OUT>
+struct Vec {
+    static constexpr int N = OUT == kOutF32 ? 4 : 8;
+    static constexpr int ESZ = OUT == kOutF32 ? 4 : 2;
+};
+
+// 16 bytes of C (one aligned group) into c[i0 .. i0+VEC).
+template <int OUT, int W>
+__device__ __forceinline__ void load_group(const char* ptr, float (&c)[W], int i0) {
     if constexpr (OUT == kOutF32) {
-        const float4* q = static_cast<const float4*>(ptr);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            float4 x = q[j];
-            c[4 * j + 0] = x.x; c[4 * j + 1] = x.y; c[4 * j + 2] = x.z; c[4 * j + 3] = x.w;
-        }
+        const float4 x = *reinterpret_cast<const float4*>(ptr);
+        c[i0] = x.x; c[i0 + 1] = x.y; c[i0 + 2] = x.z; c[i0 + 3] = x.w;
     } else {
-        const uint4* q = static_cast<const uint4*>(ptr);
+        const uint4 x = *reinterpret_cast<const uint4*>(ptr);
+        const uint32_t w4[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            uint4 x = q[j];
-            uint32_t w[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-            for (int h = 0; h < 4; ++h) {
-                const unsigned short lo = static_cast<unsigned short>(w[h] & 0xFFFFu);
-                const unsigned short hi = static_cast<unsigned short>(w[h] >> 16);
-                if constexpr (OUT == kOutF16) {
-                    c[8 * j + 2 * h] = __half2float(__ushort_as_half(lo));
-                    c[8 * j + 2 * h + 1] = __half2float(__ushort_as_half(hi));
-                } else {
-                    c[8 * j + 2 * h] = __bfloat162float(__ushort_as_bfloat16(lo));
-                    c[8 * j + 2 * h + 1] = __bfloat162float(__ushort_as_bfloat16(hi));
-                }
-            }
+        for (int h = 0; h < 4; ++h) {
+            c[i0 + 2 * h] = unpack_lo<OUT>(w4[h]);
+            c[i0 + 2 * h + 1] = unpack_hi<OUT>(w4[h]);
         }
     }
 }
 
-template <int OUT>
-__device__ __forceinline__ void store_vec32(void* ptr, const float (&v)[32]) {
+template <int OUT, int W>
+__device__ __forceinline__ void store_group(char* ptr, const float (&v)[W], int i0) {
     if constexpr (OUT == kOutF32) {
-        float4* q = static_cast<float4*>(ptr);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) q[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+        *reinterpret_cast<float4*>(ptr) = make_float4(v[i0], v[i0 + 1], v[i0 + 2], v[i0 + 3]);
     } else {
-        uint4* q = static_cast<uint4*>(ptr);
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-            q[j] = make_uint4(pack2<OUT>(v[8 * j + 0], v[8 * j + 1]), pack2<OUT>(v[8 * j + 2], v[8 * j + 3]),
-                              pack2<OUT>(v[8 * j + 4], v[8 * j + 5]), pack2<OUT>(v[8 * j + 6], v[8 * j + 7]));
+        *reinterpret_cast<uint4*>(ptr) =
+            make_uint4(pack2<OUT>(v[i0], v[i0 + 1]), pack2<OUT>(v[i0 + 2], v[i0 + 3]),
+                       pack2<OUT>(v[i0 + 4], v[i0 + 5]), pack2<OUT>(v[i0 + 6], v[i0 + 7]));
     }
+}
+
+// A row segment of W elements starting at `base`, of which the first `n`
+// are in bounds, whose first 16-byte boundary is H elements in: element
+// accesses for the head and the tail, 16-byte accesses in between.
+template <int OUT, int W, int H, bool kStore>
+__device__ __forceinline__ void row_segment(char* base, float (&v)[W], int n) {
+    constexpr int VEC = Vec<OUT>::N, ESZ = Vec<OUT>::ESZ;
+    constexpr int NG = (W - H) / VEC;
+#pragma unroll
+    for (int i = 0; i < H; ++i)
+        if (i < n) {
+            if constexpr (kStore) store_elem<OUT>(base, i, v[i]);
+            else v[i] = load_elem<OUT>(base, i);
+        }
+#pragma unroll
+    for (int g = 0; g < NG; ++g) {
+        const int i0 = H + g * VEC;
+        if (i0 + VEC <= n) {
+            if constexpr (kStore) store_group<OUT, W>(base + i0 * ESZ, v, i0);
+            else load_group<OUT, W>(base + i0 * ESZ, v, i0);
+        } else {
+#pragma unroll
+            for (int j = 0; j < VEC; ++j)
+                if (i0 + j < n) {
+                    if constexpr (kStore) store_elem<OUT>(base, i0 + j, v[i0 + j]);
+                    else v[i0 + j] = load_elem<OUT>(base, i0 + j);
+                }
+        }
+    }
+#pragma unroll
+    for (int i = H + NG * VEC; i < W; ++i)
+        if (i < n) {
+            if constexpr (kStore) store_elem<OUT>(base, i, v[i]);
+            else v[i] = load_elem<OUT>(base, i);
+        }
+}
+
+template <int OUT, int W, bool kStore>
+__device__ __forceinline__ void row_segment_dispatch(char* base, float (&v)[W], int n) {
+    constexpr int VEC = Vec<OUT>::N, ESZ = Vec<OUT>::ESZ;
+    const int head = static_cast<int>(((16u - (reinterpret_cast<uintptr_t>(base) & 15u)) & 15u) / ESZ);
+    if constexpr (VEC == 4) {
+        switch (head) {
+            case 0: row_segment<OUT, W, 0, kStore>(base, v, n); break;
+            case 1: row_segment<OUT, W, 1, kStore>(base, v, n); break;
+            case 2: row_segment<OUT, W, 2, kStore>(base, v, n); break;
+            default: row_segment<OUT, W, 3, kStore>(base, v, n); break;
+        }
+    } else {
+        switch (head) {
+            case 0: row_segment<OUT, W, 0, kStore>(base, v, n); break;
+            case 1: row_segment<OUT, W, 1, kStore>(base, v, n); break;
+            case 2: row_segment<OUT, W, 2, kStore>(base, v, n); break;
+            case 3: row_segment<OUT, W, 3, kStore>(base, v, n); break;
+            case 4: row_segment<OUT, W, 4, kStore>(base, v, n); break;
+            case 5: row_segment<OUT, W, 5, kStore>(base, v, n); break;
+            case 6: row_segment<OUT, W, 6, kStore>(base, v, n); break;
+            default: row_segment<OUT, W, 7, kStore>(base, v, n); break;
+        }
+    }
+}
+
+// alpha * acc (+ beta * C) for W consecutive accumulator columns of one
+// accumulator row, written to D (row-major, or transposed with trans_out).
+template <class Cfg>
+__device__ __forceinline__ void epilogue_chunk(const KernelParams& p, const float (&acc)[Cfg::W], int row,
+                                               int col0) {
+    constexpr int W = Cfg::W;
+    constexpr int ESZ = Vec<Cfg::OUT>::ESZ;
+    const int n = min(W, p.N - col0);
+    float v[W];
+#pragma unroll
+    for (int i = 0; i < W; ++i) v[i] = p.alpha * acc[i];
+    if (p.trans_out) {
+        // element (row, col0+i) -> D[(col0+i)*ldc + row]; lanes hold consecutive rows
+#pragma unroll
+        for (int i = 0; i < W; ++i)
+            if (i < n) {
+                const int64_t off = static_cast<int64_t>(col0 + i) * p.ldc + row;
+                float x = v[i];
+                if (p.beta != 0.0f) x = fmaf(p.alpha, acc[i], p.beta * load_elem<Cfg::OUT>(p.C, off));
+                store_elem<Cfg::OUT>(p.D, off, x);
+            }
+        return;
+    }
+    const int64_t off = static_cast<int64_t>(row) * p.ldc + col0;
+    if (p.beta != 0.0f) {
+        float c[W];
+#pragma unroll
+        for (int i = 0; i < W; ++i) c[i] = 0.0f;
+        row_segment_dispatch<Cfg::OUT, W, false>(
+            const_cast<char*>(static_cast<const char*>(p.C)) + off * ESZ, c, n);
+#pragma unroll
+        for (int i = 0; i < W; ++i) v[i] = fmaf(p.alpha, acc[i], p.beta * c[i]);
+    }
+    row_segment_dispatch<Cfg::OUT, W, true>(static_cast<char*>(p.D) + off * ESZ, v, n);
+}
+
+// alpha * acc (+ beta * C) for 4 consecutive columns of one row (used by the
+// split-K reduction, whose threads own consecutive column quads of a row).
+template <class Cfg>
+__device__ __forceinline__ void epilogue_quad(const KernelParams& p, const float4& a, int row, int col) {
+    constexpr int ESZ = Vec<Cfg::OUT>::ESZ;
+    const float acc[4] = {a.x, a.y, a.z, a.w};
+    const int n = min(4, p.N - col);
+    float v[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) v[i] = p.alpha * acc[i];
+    if (p.trans_out) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            if (i < n) {
+                const int64_t off = static_cast<int64_t>(col + i) * p.ldc + row;
+                float x = v[i];
+                if (p.beta != 0.0f) x = fmaf(p.alpha, acc[i], p.beta * load_elem<Cfg::OUT>(p.C, off));
+                store_elem<Cfg::OUT>(p.D, off, x);
+            }
+        return;
+    }
+    const int64_t off = static_cast<int64_t>(row) * p.ldc + col;
+    if (p.beta != 0.0f) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            if (i < n) v[i] = fmaf(p.alpha, acc[i], p.beta * load_elem<Cfg::OUT>(p.C, off + i));
+    }
+    char* dp = static_cast<char*>(p.D) + off * ESZ;
+    if (n == 4 && (reinterpret_cast<uintptr_t>(dp) & (4 * ESZ - 1)) == 0) {
+        if constexpr (Cfg::OUT == kOutF32) {
+            *reinterpret_cast<float4*>(dp) = make_float4(v[0], v[1], v[2], v[3]);
+        } else {
+            *reinterpret_cast<uint2*>(dp) = make_uint2(pack2<Cfg::OUT>(v[0], v[1]), pack2<Cfg::OUT>(v[2], v[3]));
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            if (i < n) store_elem<Cfg::OUT>(p.D, off + i, v[i]);
+    }
+}
+
+// Prefetch the C row segment [col0, col0 + cols) of one row into L2: the
+// 16-byte-aligned bytes strictly inside the segment (never outside C).
+template <class Cfg>
+__device__ __forceinline__ void prefetch_c_row(const KernelParams& p, int row, int col0, int cols) {
+    constexpr int ESZ = Vec<Cfg::OUT>::ESZ;
+    const int n = min(cols, p.N - col0);
+    if (n <= 0) return;
+    const uintptr_t first = reinterpret_cast<uintptr_t>(p.C) + (static_cast<uintptr_t>(row) * p.ldc + col0) * ESZ;
+    const uintptr_t last = first + static_cast<uintptr_t>(n) * ESZ;   // one past the segment
+    const uintptr_t a = (first + 15u) & ~uintptr_t(15);
+    const uintptr_t b = last & ~uintptr_t(15);
+    if (b > a) prefetch_l2_bulk(reinterpret_cast<const void*>(a), static_cast<uint32_t>(b - a));
 }
 
 // ---------------------------------------------------------------------------
@@ -228,6 +432,8 @@ template <class Cfg>
 __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
 gemm_sm103_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                   const KernelParams p) {
+    constexpr int CG = Cfg::CG;
+    constexpr int W = Cfg::W;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;   // 128B-swizzle atoms need 1024-byte alignment
@@ -242,9 +448,17 @@ gemm_sm103_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     uint32_t* tmem_slot =
         reinterpret_cast<uint32_t*>(base_ptr + Cfg::STAGES * Cfg::STAGE_BYTES + 8 * Cfg::NUM_BARRIERS);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    volatile int* epi_ok_flag = reinterpret_cast<volatile int*>(tmem_slot + 2);     // [2]
+    volatile int* epi_last_flag = reinterpret_cast<volatile int*>(tmem_slot + 4);   // [2]
 
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
+    // position of this CTA in its pair, and of the pair in the grid
+    const uint32_t rank = CG == 1 ? 0u : cluster_ctarank();
+    const int unit = CG == 1 ? static_cast<int>(blockIdx.x) : static_cast<int>(cluster_id_x());
+    const int num_units = CG == 1 ? static_cast<int>(gridDim.x) : static_cast<int>(num_clusters_x());
+    const bool leader = rank == 0;
+    const int num_work = p.num_tiles * p.splits;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < Cfg::STAGES; ++s) {
@@ -253,7 +467,7 @@ gemm_sm103_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(accf_bar(b), 1);
-            mbar_init(acce_bar(b), Cfg::NUM_EPI_WARPS);
+            mbar_init(acce_bar(b), Cfg::NUM_EPI_WARPS * CG);
         }
         mbar_init(drain_bar, 1);
         *abort_flag = 0;
@@ -264,51 +478,75 @@ gemm_sm103_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         tma_prefetch_desc(&tmB);
     }
     if (warp == 1) {
-        tmem_alloc(smem_addr(tmem_slot), Cfg::TMEM_COLS);
-        tmem_relinquish_alloc_permit();
+        tmem_alloc<CG>(smem_addr(tmem_slot), Cfg::TMEM_COLS);
+        tmem_relinquish_alloc_permit<CG>();
     }
     tc_fence_before_sync();
-    __syncthreads();
+    if constexpr (CG == 1) __syncthreads();
+    else cluster_sync_all();              // peer barriers initialised before any remote use
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
     const WaitCtx wctx{p.status, p.timeout_ns, abort_flag};
 
     if (warp == 0) {
         // ------------------------------------------------------------------
-        // TMA producer
+        // TMA producer (one thread per CTA)
         // ------------------------------------------------------------------
         if (lane == 0) {
             int stage = 0;
             uint32_t phase = 0;
             int64_t issued = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+            const uint32_t b_tx = p.b_mn_major ? static_cast<uint32_t>(Cfg::B_BYTES)
+                                               : static_cast<uint32_t>(Cfg::BN_CTA * Cfg::BK * 2);
+            const uint32_t stage_tx = CG * (Cfg::A_BYTES + b_tx);
+            for (int w = unit; ok && w < num_work; w += num_units) {
+                const WorkItem x = work_item(p, w);
                 int mb, nb;
-                tile_coords(p, tile, mb, nb);
-                const int m0 = mb * Cfg::BM, n0 = nb * Cfg::BN;
-                for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+                tile_coords(p, x.tile, mb, nb);
+                const int m0 = mb * Cfg::UMMA_M + Cfg::BM * static_cast<int>(rank);
+                const int n0 = nb * Cfg::BN + Cfg::BN_CTA * static_cast<int>(rank);
+                for (int kb = x.kb0; kb < x.kb1; ++kb) {
                     if (!wait_phase(empty_bar(stage), phase ^ 1u, wctx, kSiteProducerEmpty)) {
                         ok = false;
                         break;
                     }
                     const uint32_t sa = base + stage * Cfg::STAGE_BYTES;
                     const uint32_t sb = sa + Cfg::A_BYTES;
-                    const uint32_t fb = full_bar(stage);
+                    const uint32_t fb_local = full_bar(stage);
                     const int k0 = kb * Cfg::BK;
-                    mbar_arrive_expect_tx(fb, Cfg::STAGE_BYTES);
-                    if (p.a_mn_major) {
+                    if (leader) mbar_arrive_expect_tx(fb_local, stage_tx);
+                    if constexpr (CG == 1) {
+                        if (p.a_mn_major) {
 #pragma unroll
-                        for (int c = 0; c < Cfg::BM / 64; ++c)
-                            tma_load_2d(sa + c * Cfg::MN_CHUNK_BYTES, &tmA, fb, m0 + 64 * c, k0);
-                    } else {
-                        tma_load_2d(sa, &tmA, fb, k0, m0);
-                    }
-                    if (p.b_mn_major) {
+                            for (int c = 0; c < Cfg::BM / 64; ++c)
+                                tma_load_2d(sa + c * Cfg::MN_CHUNK_BYTES, &tmA, fb_local, m0 + 64 * c, k0);
+                        } else {
+                            tma_load_2d(sa, &tmA, fb_local, k0, m0);
+                        }
+                        if (p.b_mn_major) {
 #pragma unroll
-                        for (int c = 0; c < Cfg::BN / 64; ++c)
-                            tma_load_2d(sb + c * Cfg::MN_CHUNK_BYTES, &tmB, fb, n0 + 64 * c, k0);
+                            for (int c = 0; c < Cfg::B_CHUNKS; ++c)
+                                tma_load_2d(sb + c * Cfg::MN_CHUNK_BYTES, &tmB, fb_local, n0 + 64 * c, k0);
+                        } else {
+                            tma_load_2d(sb, &tmB, fb_local, k0, n0);
+                        }
                     } else {
-                        tma_load_2d(sb, &tmB, fb, k0, n0);
+                        const uint32_t fb = map_to_cta(fb_local, 0);   // the leader's barrier
+                        if (p.a_mn_major) {
+#pragma unroll
+                            for (int c = 0; c < Cfg::BM / 64; ++c)
+                                tma_load_2d_pair(sa + c * Cfg::MN_CHUNK_BYTES, &tmA, fb, m0 + 64 * c, k0);
+                        } else {
+                            tma_load_2d_pair(sa, &tmA, fb, k0, m0);
+                        }
+                        if (p.b_mn_major) {
+#pragma unroll
+                            for (int c = 0; c < Cfg::B_CHUNKS; ++c)
+                                tma_load_2d_pair(sb + c * Cfg::MN_CHUNK_BYTES, &tmB, fb, n0 + 64 * c, k0);
+                        } else {
+                            tma_load_2d_pair(sb, &tmB, fb, k0, n0);
+                        }
                     }
                     ++issued;
                     if (++stage == Cfg::STAGES) {
@@ -317,7 +555,7 @@ gemm_sm103_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                     }
                 }
             }
-            if (!ok) {
+            if (!ok && leader) {
                 // wind down: let the copies already issued land before exiting
                 int s = stage;
                 uint32_t ph = phase;
@@ -332,14 +570,15 @@ gemm_sm103_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------------
-        // MMA issuer (one thread)
+        // MMA issuer: one thread of the leader CTA
         // ------------------------------------------------------------------
-        if (lane == 0) {
+        if (lane == 0 && leader) {
             int stage = 0;
             uint32_t phase = 0;
             int buf = 0;
             uint32_t acc_phase = 0;
             bool ok = true;
+            constexpr uint16_t kPair = CG == 1 ? 1 : 3;
             // K-major operands: 128-byte rows, 8-row atoms 1024 bytes apart;
             // a 16-deep K step is 32 bytes along the row.
             // MN-major operands: 64-element chunks MN_CHUNK_BYTES apart (LBO),
@@ -348,14 +587,18 @@ gemm_sm103_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             const uint32_t b_lbo = p.b_mn_major ? Cfg::MN_CHUNK_BYTES : 16u;
             const uint32_t a_kstep = p.a_mn_major ? 16u * 128u : 32u;
             const uint32_t b_kstep = p.b_mn_major ? 16u * 128u : 32u;
-            for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
-                if (!wait_phase(acce_bar(buf), acc_phase ^ 1u, wctx, kSiteMmaAccEmpty)) {
+            for (int w = unit; ok && w < num_work; w += num_units) {
+                const WorkItem x = work_item(p, w);
+                bool got;
+                if constexpr (CG == 1) got = wait_phase(acce_bar(buf), acc_phase ^ 1u, wctx, kSiteMmaAccEmpty);
+                else got = wait_phase<true>(acce_bar(buf), acc_phase ^ 1u, wctx, kSiteMmaAccEmpty);
+                if (!got) {
                     ok = false;
                     break;
                 }
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + buf * Cfg::ACC_COLS;
-                for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+                for (int kb = x.kb0; kb < x.kb1; ++kb) {
                     if (!wait_phase(full_bar(stage), phase, wctx, kSiteMmaFull)) {
                         ok = false;
                         break;
@@ -367,88 +610,149 @@ gemm_sm103_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                     for (int k = 0; k < Cfg::BK / Cfg::UMMA_K; ++k) {
                         const uint64_t adesc = smem_desc_sw128(sa + k * a_kstep, a_lbo, 1024u);
                         const uint64_t bdesc = smem_desc_sw128(sb + k * b_kstep, b_lbo, 1024u);
-                        umma_f16_ss(d_tmem, adesc, bdesc, p.idesc, (kb | k) != 0 ? 1u : 0u);
+                        umma_f16_ss<CG>(d_tmem, adesc, bdesc, p.idesc, (kb != x.kb0 || k != 0) ? 1u : 0u);
                     }
-                    umma_commit(empty_bar(stage));   // stage reusable once these MMAs finish
+                    umma_commit<CG>(empty_bar(stage), kPair);   // stage reusable once these MMAs finish
                     if (++stage == Cfg::STAGES) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
                 if (!ok) break;
-                umma_commit(accf_bar(buf));          // accumulator complete
+                umma_commit<CG>(accf_bar(buf), kPair);          // accumulator complete
                 if (++buf == 2) {
                     buf = 0;
                     acc_phase ^= 1u;
                 }
             }
             if (!ok) {
-                umma_commit(drain_bar);              // wait for every MMA issued so far
+                umma_commit<CG>(drain_bar, 1);                  // wait for every MMA issued so far
                 wait_phase_drain(drain_bar, 0, 100000000ull);
             }
         }
     } else {
         // ------------------------------------------------------------------
-        // epilogue warps: warp w reads TMEM lanes [32*(w%4), 32*(w%4)+32)
+        // epilogue warps: warp w reads TMEM lanes [32*(w%4), 32*(w%4)+32).
+        // Thread 64 waits for each accumulator and broadcasts the outcome, so
+        // the four warps leave the loop together (they share named barrier 1).
         // ------------------------------------------------------------------
         const int quad = warp % 4;
+        const int row_local = 32 * quad + lane;
         int buf = 0;
         uint32_t acc_phase = 0;
-        for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
+        int iter = 0;
+        for (int w = unit; w < num_work; w += num_units, ++iter) {
+            const WorkItem x = work_item(p, w);
             int mb, nb;
-            tile_coords(p, tile, mb, nb);
-            const int m0 = mb * Cfg::BM, n0 = nb * Cfg::BN;
-            int ok = 1;
-            if (lane == 0) ok = wait_phase(accf_bar(buf), acc_phase, wctx, kSiteEpilogueAccFull) ? 1 : 0;
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-            if (!ok) break;
+            tile_coords(p, x.tile, mb, nb);
+            const int m0 = mb * Cfg::UMMA_M + Cfg::BM * static_cast<int>(rank);
+            const int n0 = nb * Cfg::BN;
+            // warm L2 with this thread's C row while the main loop runs
+            if (p.beta != 0.0f && !p.trans_out && m0 + row_local < p.M)
+                prefetch_c_row<Cfg>(p, m0 + row_local, n0, Cfg::BN);
+            if (threadIdx.x == 64)
+                epi_ok_flag[iter & 1] = wait_phase(accf_bar(buf), acc_phase, wctx, kSiteEpilogueAccFull) ? 1 : 0;
+            named_bar_sync(1, 32 * Cfg::NUM_EPI_WARPS);
+            if (!epi_ok_flag[iter & 1]) break;
             tc_fence_after_sync();
-            const int row = m0 + 32 * quad + lane;
+            const int row = m0 + row_local;
             const bool row_ok = row < p.M;
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(32 * quad) << 16) + buf * Cfg::ACC_COLS;
+            if (p.splits == 1) {
 #pragma unroll 1
-            for (int c = 0; c < Cfg::BN / 32; ++c) {
-                const int col0 = n0 + 32 * c;
-                if (col0 >= p.N) break;   // warp-uniform
-                __syncwarp();             // tcgen05.ld is .sync.aligned: converge the warp
-                uint32_t r[32];
-                tmem_ld_32x32b_x32(t_row + 32 * c, r);
-                tmem_ld_wait();
-                if (!row_ok) continue;
-                float v[32];
+                for (int c = 0; c < Cfg::BN / W; ++c) {
+                    const int col0 = n0 + W * c;
+                    if (col0 >= p.N) break;   // warp-uniform
+                    __syncwarp();             // tcgen05.ld is .sync.aligned: converge the warp
+                    uint32_t r[W];
+                    tmem_ld_row<W>(t_row + W * c, r);
+                    tmem_ld_wait();
+                    if (!row_ok) continue;
+                    float acc[W];
 #pragma unroll
-                for (int i = 0; i < 32; ++i) v[i] = p.alpha * acc_value<Cfg::ACC_F16>(r[i]);
-                const int64_t off = static_cast<int64_t>(row) * p.ldc + col0;
-                constexpr int esz = Cfg::OUT == kOutF32 ? 4 : 2;
-                const bool full_cols = col0 + 32 <= p.N;
-                if (p.beta != 0.0f) {
-                    const char* cp = static_cast<const char*>(p.C) + off * esz;
-                    if (full_cols && (reinterpret_cast<uintptr_t>(cp) & 15u) == 0) {
-                        float cv[32];
-                        load_c_vec32<Cfg::OUT>(cp, cv);
-#pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            v[i] = fmaf(p.alpha, acc_value<Cfg::ACC_F16>(r[i]), p.beta * cv[i]);
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            if (col0 + i < p.N)
-                                v[i] = fmaf(p.alpha, acc_value<Cfg::ACC_F16>(r[i]),
-                                            p.beta * load_c_scalar<Cfg::OUT>(p.C, off + i));
-                    }
+                    for (int i = 0; i < W; ++i) acc[i] = acc_value<Cfg::ACC_F16>(r[i]);
+                    epilogue_chunk<Cfg>(p, acc, row, col0);
                 }
-                char* dp = static_cast<char*>(p.D) + off * esz;
-                if (full_cols && (reinterpret_cast<uintptr_t>(dp) & 15u) == 0) {
-                    store_vec32<Cfg::OUT>(dp, v);
-                } else {
+            } else {
+                // 1. this split's fp32 partial -> workspace ([128][BN] per CTA)
+                const int64_t tile_elems = static_cast<int64_t>(Cfg::BM) * Cfg::BN;
+                auto slot = [&](int split) {
+                    return p.ws + ((static_cast<int64_t>(x.tile) * p.splits + split) * CG + rank) * tile_elems;
+                };
+                float* mine = slot(x.split) + static_cast<int64_t>(row_local) * Cfg::BN;
+#pragma unroll 1
+                for (int c = 0; c < Cfg::BN / W; ++c) {
+                    __syncwarp();
+                    uint32_t r[W];
+                    tmem_ld_row<W>(t_row + W * c, r);
+                    tmem_ld_wait();
 #pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        if (col0 + i < p.N) store_scalar<Cfg::OUT>(p.D, off + i, v[i]);
+                    for (int i = 0; i < W; i += 4)
+                        __stcg(reinterpret_cast<float4*>(mine + W * c + i),
+                               make_float4(__uint_as_float(r[i]), __uint_as_float(r[i + 1]),
+                                           __uint_as_float(r[i + 2]), __uint_as_float(r[i + 3])));
+                }
+                // 2. count arrivals; the last split of the tile reduces
+                __threadfence();
+                named_bar_sync(1, 32 * Cfg::NUM_EPI_WARPS);
+                if (threadIdx.x == 64) {
+                    int* ctr = p.counters + static_cast<int64_t>(x.tile) * CG + rank;
+                    const int old = atomicAdd(ctr, 1);
+                    const int last = old == p.splits - 1;
+                    if (last) atomicExch(ctr, 0);   // ready for the next launch
+                    __threadfence();
+                    epi_last_flag[iter & 1] = last;
+                }
+                named_bar_sync(1, 32 * Cfg::NUM_EPI_WARPS);
+                if (epi_last_flag[iter & 1]) {
+                    __threadfence();
+                    // 3. sum the partials in split order (a fixed order: deterministic).
+                    // Thread t takes float4 t, t+128, ... of the [128][BN] tile, so a
+                    // warp reads and writes 512 contiguous bytes at a time; each thread
+                    // keeps BATCH independent loads in flight per split.
+                    constexpr int QUADS_PER_ROW = Cfg::BN / 4;
+                    constexpr int QUADS = Cfg::BM * QUADS_PER_ROW;
+                    constexpr int NT = 32 * Cfg::NUM_EPI_WARPS;
+                    constexpr int BATCH = largest_divisor_upto(QUADS / NT, 16);
+                    static_assert(QUADS % (NT * BATCH) == 0, "whole batches");
+                    const int t = threadIdx.x - 64;
+#pragma unroll 1
+                    for (int q0 = t; q0 < QUADS; q0 += NT * BATCH) {
+                        float4 acc[BATCH];
+                        const float4* s0 = reinterpret_cast<const float4*>(slot(0));
+#pragma unroll
+                        for (int j = 0; j < BATCH; ++j) acc[j] = __ldcg(s0 + q0 + NT * j);
+#pragma unroll 1
+                        for (int sp = 1; sp < p.splits; ++sp) {
+                            const float4* sq = reinterpret_cast<const float4*>(slot(sp));
+                            float4 o[BATCH];
+#pragma unroll
+                            for (int j = 0; j < BATCH; ++j) o[j] = __ldcg(sq + q0 + NT * j);
+#pragma unroll
+                            for (int j = 0; j < BATCH; ++j) {
+                                acc[j].x += o[j].x;
+                                acc[j].y += o[j].y;
+                                acc[j].z += o[j].z;
+                                acc[j].w += o[j].w;
+                            }
+                        }
+#pragma unroll
+                        for (int j = 0; j < BATCH; ++j) {
+                            const int q = q0 + NT * j;
+                            const int r = q / QUADS_PER_ROW;
+                            const int col = (q - r * QUADS_PER_ROW) * 4;
+                            const int grow = m0 + r, gcol = n0 + col;
+                            if (grow < p.M && gcol < p.N) epilogue_quad<Cfg>(p, acc[j], grow, gcol);
+                        }
+                    }
                 }
             }
             tc_fence_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive(acce_bar(buf));
+            if (lane == 0) {
+                if constexpr (CG == 1) mbar_arrive(acce_bar(buf));
+                else mbar_arrive_cluster(map_to_cta(acce_bar(buf), 0));   // the leader's barrier
+            }
             if (++buf == 2) {
                 buf = 0;
                 acc_phase ^= 1u;
@@ -457,11 +761,12 @@ gemm_sm103_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     }
 
     tc_fence_before_sync();
-    __syncthreads();
+    if constexpr (CG == 1) __syncthreads();
+    else cluster_sync_all();              // the leader's MMAs into the peer's TMEM are finished
     if (warp == 1) {
         __syncwarp();
         tc_fence_after_sync();
-        tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+        tmem_dealloc<CG>(tmem_base, Cfg::TMEM_COLS);
     }
 }
 
@@ -473,8 +778,8 @@ __global__ void scale_c_kernel(int32_t M, int32_t N, const void* C, void* D, int
          e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
         const int64_t i = e / N, j = e % N;
         const int64_t off = i * ldc + j;
-        const float v = beta != 0.0f ? beta * load_c_scalar<OUT>(C, off) : 0.0f;
-        store_scalar<OUT>(D, off, v);
+        const float v = beta != 0.0f ? beta * load_elem<OUT>(C, off) : 0.0f;
+        store_elem<OUT>(D, off, v);
     }
 }
 

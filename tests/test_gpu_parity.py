@@ -74,7 +74,8 @@ def test_types_and_layouts(plans, combo, layouts, integer):
     check_full(base, h, D, integer)
 
 
-FULL = ["sq4096", "sq4096h", "ragged", "bf16_1024", "bf16_2048", "bf16_8192", "bf16_16384", "skinny"]
+FULL = ["sq4096", "sq4096h", "ragged", "bf16_1024", "bf16_2048", "bf16_8192", "bf16_16384", "skinny",
+        "sq8192"]
 
 
 @pytest.mark.parametrize("name", FULL)

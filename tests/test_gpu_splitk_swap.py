@@ -1,0 +1,153 @@
+"""Split-K and the transposed (swap-AB) path, through the C ABI (GB300).
+
+Problems with few output tiles are split along K: each split writes an fp32
+partial and the last split to arrive adds them in split order.  Problems with
+at most 64 rows are computed as D^T = B^T A^T.  Integer twins make every
+partial sum exact, so the result must match the oracle bit for bit whatever
+the split; random data must be within the fp32-accumulate tolerance and
+identical from call to call (the reduction order is fixed).
+"""
+import numpy as np
+import pytest
+import torch
+
+import workloads as wl
+from gpu_util import check_full, run_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def plans():
+    from tensor_core_dense_tma_gb300 import build as tcbuild
+    tcbuild.build()
+    import tensor_core_dense_tma_gb300 as tc
+    p = {"f16": tc.Plan("f16", 0), "bf16": tc.Plan("bf16", 0)}
+    yield p
+    torch.cuda.synchronize()
+    for v in p.values():
+        assert v.device_status() == 0
+        v.close()
+
+
+def W(M, N, K, la="row", lb="row", dt="f16", out="f32", alpha=1.0, beta=0.0):
+    return wl.Workload(f"sk{M}x{N}x{K}", 11, M, N, K, dt, la, lb, "f32", out, alpha, beta, "u1")
+
+
+def padded(w):
+    return -(-w.lda // 8) * 8, -(-w.ldb // 8) * 8
+
+
+SHAPES = [(16, 1104, 520), (1, 2048, 256), (7, 600, 1000), (33, 712, 1000), (64, 512, 2048),
+          (64, 64, 640), (300, 264, 2048), (1024, 1024, 1024), (520, 1000, 3000)]
+LAYOUTS = [("row", "row"), ("row", "col"), ("col", "row"), ("col", "col")]
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("layouts", LAYOUTS, ids=lambda l: "".join(x[0] for x in l))
+def test_integer_twin_bit_exact(plans, shape, layouts):
+    w = W(*shape, *layouts, alpha=0.5, beta=1.0)
+    lda, ldb = padded(w)
+    h = wl.make_inputs(w, integer=True, lda=lda, ldb=ldb)
+    D = run_gpu(plans["f16"], w, h)
+    torch.cuda.synchronize()
+    check_full(w, h, D, integer=True)
+
+
+@pytest.mark.parametrize("shape", [(16, 8192, 8192), (48, 1024, 4096), (1024, 1024, 1024)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_bf16_out_random(plans, shape):
+    w = W(*shape, dt="bf16", out="bf16")
+    h = wl.make_inputs(w)
+    D = run_gpu(plans["bf16"], w, h)
+    torch.cuda.synchronize()
+    if w.M * w.N * w.K <= 2e9:
+        check_full(w, h, D, integer=False)
+    else:
+        from gpu_util import check_sampled
+        check_sampled(w, h, D, integer=False, n_random=4096)
+
+
+@pytest.mark.parametrize("shape", [(16, 4096, 4096), (1024, 1024, 16384)], ids=lambda s: "x".join(map(str, s)))
+def test_split_results_repeat_bitwise(plans, shape):
+    w = W(*shape)
+    h = wl.make_inputs(w)
+    A, B = h.A.cuda(), h.B.cuda()
+    plan = plans["f16"]
+    desc = plan.describe(w.M, w.N, w.K)
+    assert "splitk" in desc, desc
+    D0 = plan.gemm(A, B)
+    for _ in range(10):
+        D1 = plan.gemm(A, B)
+        torch.cuda.synchronize()
+        assert torch.equal(D0, D1)
+
+
+def test_configuration_choice(plans):
+    plan = plans["bf16"]
+    assert "swapAB" in plan.describe(16, 8192, 8192, "row", "row", "f32", "bf16")
+    assert "tc2cta" in plan.describe(8192, 8192, 8192, "row", "row", "f32", "bf16")
+    # few tiles and a deep K: split
+    assert "splitk" in plan.describe(1024, 1024, 16384, "row", "row", "f32", "bf16")
+    # fp16 accumulation is never split
+    assert "splitk" not in plans["f16"].describe(1024, 1024, 1024, "row", "row", "f16", "f16")
+
+
+def test_swapped_in_place_beta(plans):
+    """Transposed store with C read through the same transposed addressing."""
+    w = W(40, 600, 520, "row", "col", alpha=0.5, beta=1.0)
+    h = wl.make_inputs(w, integer=True)
+    A, B = h.A.cuda(), h.B.cuda()
+    CD = h.C.cuda()
+    plans["f16"].gemm(wl.logical(A, w.M, w.K, "row"), wl.logical(B, w.K, w.N, "col"), CD, CD,
+                      alpha=0.5, beta=1.0)
+    torch.cuda.synchronize()
+    check_full(w, h, CD, integer=True)
+
+
+ALL_CONFIGS = ["single_128x256", "pair_256x256", "pair_256x224"]
+
+
+@pytest.mark.parametrize("config", ALL_CONFIGS)
+@pytest.mark.parametrize("splits", [1, 2, 3, 5])
+@pytest.mark.parametrize("shape", [(300, 520, 1000), (129, 264, 640)], ids=lambda s: "x".join(map(str, s)))
+def test_every_config_and_split(plans, config, splits, shape):
+    """Each configuration and split count, pinned, on ragged shapes."""
+    w = W(*shape, "row", "col", out="f32", alpha=0.5, beta=1.0)
+    h = wl.make_inputs(w, integer=True)
+    plan = plans["f16"]
+    plan.force_config(config, splits)
+    try:
+        D = run_gpu(plan, w, h)
+        torch.cuda.synchronize()
+    finally:
+        plan.force_config("auto")
+    check_full(w, h, D, integer=True)
+
+
+@pytest.mark.parametrize("config", ["single_128x16", "single_128x64"])
+@pytest.mark.parametrize("splits", [1, 3])
+def test_transposed_configs_pinned(plans, config, splits):
+    w = W(16, 1000, 1000, "col", "row", dt="bf16", out="bf16")
+    h = wl.make_inputs(w, integer=True)
+    plan = plans["bf16"]
+    plan.force_config(config, splits)
+    try:
+        D = run_gpu(plan, w, h)
+        torch.cuda.synchronize()
+    finally:
+        plan.force_config("auto")
+    check_full(w, h, D, integer=True)
+
+
+def test_pinned_config_that_does_not_fit(plans):
+    import tensor_core_dense_tma_gb300 as tc
+    plan = plans["f16"]
+    plan.force_config("single_128x16", 1)
+    try:
+        with pytest.raises(tc.GemmError) as e:
+            plan.gemm(torch.zeros((256, 64), dtype=torch.float16, device="cuda"),
+                      torch.zeros((64, 256), dtype=torch.float16, device="cuda"))
+        assert e.value.status == 2
+    finally:
+        plan.force_config("auto")

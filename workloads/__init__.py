@@ -18,6 +18,8 @@ The workloads are the ones the pages measure or describe, made synthetic
 * ``bf16_<n>`` -- bf16 square sweep n in {1024, 2048, 8192, 16384}, row-major,
   U[-1,1], fp32 accumulate, bf16 output.
 * ``skinny``   -- bf16 M=16, N=K=8192, same recipe (memory-bound).
+* ``sq8192``   -- 8192^3 with the ``sq4096`` recipe (the second size of the
+  throughput target).
 
 Every workload also has an integer twin: entries drawn uniformly from
 {-2,-1,0,1,2} (and C too, where beta != 0), for which every partial sum is an
@@ -94,6 +96,8 @@ WORKLOADS: dict[str, Workload] = {
         Workload("bf16_8192", 5, 8192, 8192, 8192, "bf16", "row", "row", "f32", "bf16", 1.0, 0.0, "u1"),
         Workload("bf16_16384", 5, 16384, 16384, 16384, "bf16", "row", "row", "f32", "bf16", 1.0, 0.0, "u1"),
         Workload("skinny", 5, 16, 8192, 8192, "bf16", "row", "row", "f32", "bf16", 1.0, 0.0, "u1"),
+        # the second square size the throughput target names (fp16 -> fp32 at 8192^3)
+        Workload("sq8192", 6, 8192, 8192, 8192, "f16", "row", "row", "f32", "f32", 1.0, 0.0, "u1"),
     ]
 }
 
