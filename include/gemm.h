@@ -151,6 +151,47 @@ gemm_status_t gemm_plan_describe(gemm_plan_t plan, int64_t M, int64_t N, int64_t
                                  gemm_dtype_t accum_dtype, gemm_dtype_t out_dtype,
                                  char *buf, int64_t len);
 
+/* gemm_run for callers that cannot allocate device memory.  The paper has no
+ * counterpart to this entry point: its kernels need no workspace at all.
+ *
+ * Who needs it: code hosted by a framework that owns all of the device's
+ * memory and hands a kernel only its inputs and outputs (so the caller has
+ * nowhere to get a plan's workspace from), and code that must keep
+ * cudaMalloc, with its device-wide synchronisation, off its path.  A plan
+ * allocates its split-K workspace and status word with cudaMalloc; this
+ * entry point takes no plan and calls no allocation routine (no cudaMalloc,
+ * no cudaFree, no allocating library call).  Instead its split-K partials, split counters and status word live
+ * in one 4 MiB array that the library defines in device memory; every GPU
+ * that loads the library holds that array until the process exits.
+ *
+ * Arguments are those of gemm_run, plus `device` (CUDA ordinal, which the
+ * call makes current while it runs and then restores), `in_dtype` (GEMM_F16
+ * or GEMM_BF16) and `splits` (1..16): the number of K ranges each output
+ * tile is split into, with the kernel configuration gemm_run would pick.
+ * Split partials take tiles x splits x (128 x tile-width x 4 bytes) per CTA
+ * of a tile; when that exceeds the array's 4,177,664 bytes for partials, or
+ * the tiles exceed its 4096 split counters, the call returns
+ * GEMM_ERR_UNSUPPORTED and launches nothing (example: M = 16, N = K = 8192
+ * uses 64 tiles of 128 x 16, i.e. 1 MiB at splits = 2; 1024^3 with splits
+ * = 2 needs 8 MiB and is rejected).  splits > 1 with fp16 accumulation, or
+ * more splits than 64-deep K blocks, also returns GEMM_ERR_UNSUPPORTED.
+ *
+ * The first call on a device sets that device up (it finds the array's
+ * device address and prepares the kernels); make that first call before
+ * any stream capture.  Every call on a device shares the array, which
+ * keeps the previous call's contents: each call first clears the status
+ * word and the split counters on `stream`.  Calls whose kernels overlap on
+ * the GPU (other streams, other threads) race on the array and must be
+ * serialised by the caller.  A device-side timeout is recorded in the
+ * array's status word, which this entry point does not report; results of
+ * a call are valid once `stream` has been synchronised. */
+gemm_status_t gemm_run_static_scratch(int device, gemm_dtype_t in_dtype, const void *A, const void *B,
+                                      const void *C, void *D, int64_t M, int64_t N, int64_t K,
+                                      int64_t lda, int64_t ldb, int64_t ldc, gemm_layout_t layoutA,
+                                      gemm_layout_t layoutB, gemm_dtype_t accum_dtype,
+                                      gemm_dtype_t out_dtype, float alpha, float beta, int splits,
+                                      void *stream);
+
 /* Free the plan and its device memory.  NULL is accepted (no-op).  The
  * caller must have synchronised any stream still running its launches. */
 gemm_status_t gemm_plan_destroy(gemm_plan_t plan);

@@ -31,7 +31,7 @@ __all__ = [
     "gemm_plan_create", "gemm_run", "gemm_validate", "gemm_plan_device_status",
     "gemm_plan_device_error_site", "gemm_plan_set_timeout_ns", "gemm_plan_launch_count",
     "gemm_plan_sm_count", "gemm_plan_describe", "gemm_plan_destroy", "gemm_status_string",
-    "gemm_plan_force_config", "CONFIG",
+    "gemm_plan_force_config", "CONFIG", "gemm_run_static_scratch",
 ]
 
 STATUS = {
@@ -75,6 +75,9 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.gemm_plan_describe.restype = i32
     lib.gemm_plan_destroy.argtypes = [p]
     lib.gemm_plan_destroy.restype = i32
+    lib.gemm_run_static_scratch.argtypes = [i32, i32, p, p, p, p, i64, i64, i64, i64, i64, i64, i32, i32, i32,
+                                            i32, f32, f32, i32, p]
+    lib.gemm_run_static_scratch.restype = i32
     lib.gemm_status_string.argtypes = [i32]
     lib.gemm_status_string.restype = ctypes.c_char_p
     return lib
@@ -171,6 +174,15 @@ def gemm_plan_describe(plan, M, N, K, layoutA="row", layoutB="row", accum_dtype=
 
 def gemm_plan_destroy(plan) -> int:
     return load().gemm_plan_destroy(plan)
+
+
+def gemm_run_static_scratch(device, in_dtype, A, B, C, D, M, N, K, lda, ldb, ldc, layoutA, layoutB,
+                            accum_dtype, out_dtype, alpha, beta, splits, stream) -> int:
+    """gemm_run without a plan, for callers that cannot allocate device
+    memory: its scratch is a fixed array inside the library (see gemm.h)."""
+    return load().gemm_run_static_scratch(device, DTYPE[in_dtype], A, B, C, D, M, N, K, lda, ldb, ldc,
+                                          LAYOUT[layoutA], LAYOUT[layoutB], DTYPE[accum_dtype],
+                                          DTYPE[out_dtype], alpha, beta, splits, stream)
 
 
 def gemm_status_string(status: int) -> str:

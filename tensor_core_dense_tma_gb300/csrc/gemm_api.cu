@@ -7,6 +7,7 @@
 #include <cstdint>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 #include <new>
 #include <string>
 
@@ -389,3 +390,137 @@ const char* gemm_status_string(gemm_status_t status) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// gemm_run_static_scratch: the same kernels for callers that may not allocate
+// device memory.  Their split-K partials, split counters and status word live
+// in one fixed-size array that the library defines at file scope; every GPU
+// that loads the library holds it until the process exits.
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr size_t kStaticScratchBytes = size_t(4) << 20;          // 4 MiB in all
+constexpr size_t kStaticStatusOffset = 0;                         // 2 ints
+constexpr size_t kStaticCountersOffset = 256;                     // kStaticCounters ints
+constexpr int kStaticCounters = 4096;
+constexpr size_t kStaticPartialsOffset = kStaticCountersOffset + kStaticCounters * sizeof(int);
+constexpr size_t kStaticPartialsBytes = kStaticScratchBytes - kStaticPartialsOffset;
+static_assert(kStaticPartialsOffset % 256 == 0, "partials start on a 256-byte boundary");
+
+static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+
+constexpr int kMaxStaticDevices = 64;
+
+// Per-device state of the entry point, set up once by its first call on
+// that device.  Host storage is static too: the entry point allocates
+// nothing, on the device or on the host.
+struct StaticDeviceState {
+    bool ready = false;
+    gemm_plan plan[2];              // one per input type; the device pointers point into g_static_scratch
+    unsigned char* scratch = nullptr;
+};
+StaticDeviceState g_static_state[kMaxStaticDevices];
+std::mutex g_static_mutex;
+
+// Device set-up, with `device` current: the array's device address, the
+// tensor-map encoder, and each kernel's shared-memory opt-in.
+gemm_status_t static_setup(int device, StaticDeviceState& st) {
+    int count = 0;
+    if (cudaGetDeviceCount(&count) != cudaSuccess || count <= 0) {
+        cudaGetLastError();
+        return GEMM_ERR_NO_DEVICE;
+    }
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess)
+        return GEMM_ERR_CUDA;
+    if (major != 10 || minor != 3) return GEMM_ERR_NO_DEVICE;
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_static_scratch) != cudaSuccess || ptr == nullptr) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn)
+        return GEMM_ERR_CUDA;
+    st.scratch = static_cast<unsigned char*>(ptr);
+    for (int t = 0; t < 2; ++t) {
+        gemm_plan& pl = st.plan[t];
+        pl.device = device;
+        pl.sm_count = sms;
+        pl.in_dtype = t == 0 ? GEMM_F16 : GEMM_BF16;
+        pl.d_status = reinterpret_cast<int*>(st.scratch + kStaticStatusOffset);
+        pl.d_counters = reinterpret_cast<int*>(st.scratch + kStaticCountersOffset);
+        pl.d_ws = reinterpret_cast<float*>(st.scratch + kStaticPartialsOffset);
+        pl.encode = reinterpret_cast<EncodeTiledFn>(fn);
+        if (prepare_all(&pl) != GEMM_OK) return GEMM_ERR_CUDA;
+    }
+    st.ready = true;
+    return GEMM_OK;
+}
+
+}  // namespace
+
+extern "C" gemm_status_t gemm_run_static_scratch(int device, gemm_dtype_t in_dtype, const void* A, const void* B,
+                                                 const void* C, void* D, int64_t M, int64_t N, int64_t K,
+                                                 int64_t lda, int64_t ldb, int64_t ldc, gemm_layout_t layoutA,
+                                                 gemm_layout_t layoutB, gemm_dtype_t accum_dtype,
+                                                 gemm_dtype_t out_dtype, float alpha, float beta, int splits,
+                                                 void* stream) {
+    if (device < 0 || device >= kMaxStaticDevices) return GEMM_ERR_INVALID_ARG;
+    if (in_dtype != GEMM_F16 && in_dtype != GEMM_BF16)
+        return valid_dtype(in_dtype) ? GEMM_ERR_UNSUPPORTED : GEMM_ERR_INVALID_ARG;
+    gemm_status_t st = validate(in_dtype, A, B, C, D, M, N, K, lda, ldb, ldc, layoutA, layoutB, accum_dtype,
+                                out_dtype, beta, true);
+    if (st != GEMM_OK) return st;
+    if (splits < 1 || splits > kMaxSplits) return GEMM_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return GEMM_OK;
+    DeviceGuard guard(device);
+    if (!guard.ok) return GEMM_ERR_CUDA;
+    StaticDeviceState& ds = g_static_state[device];
+    {
+        std::lock_guard<std::mutex> lock(g_static_mutex);
+        if (!ds.ready) {
+            st = static_setup(device, ds);
+            if (st != GEMM_OK) return st;
+        }
+    }
+    gemm_plan* plan = &ds.plan[in_dtype == GEMM_F16 ? 0 : 1];
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (K == 0) return launch_scale(plan, C, D, M, N, ldc, out_dtype, beta, s);
+
+    // the configuration gemm_run would pick, with the caller's split count
+    bool valid = true;
+    Choice ch = choose(plan, M, N, K, accum_dtype, &valid);
+    if (!valid) return GEMM_ERR_UNSUPPORTED;
+    const int64_t kb = (K + 63) / 64;
+    if (splits > kb || (accum_dtype == GEMM_F16 && splits > 1)) return GEMM_ERR_UNSUPPORTED;
+    ch.splits = splits;
+    // the size limit: split partials and counters must fit the fixed array
+    if (splits > 1) {
+        const int64_t ctas = kCfgCtas[ch.kind];
+        const int64_t partial_bytes = ch.tiles * splits * ctas * 128 * kCfgTileN[ch.kind] * 4;
+        if (ch.tiles * ctas > kStaticCounters || partial_bytes > static_cast<int64_t>(kStaticPartialsBytes))
+            return GEMM_ERR_UNSUPPORTED;
+    }
+    // the array keeps the previous call's contents: start from a clear
+    // status word and zero split counters (stream-ordered, no allocation)
+    if (cudaMemsetAsync(plan->d_status, 0, 2 * sizeof(int), s) != cudaSuccess ||
+        cudaMemsetAsync(plan->d_counters, 0, kStaticCounters * sizeof(int), s) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
+    const Problem pr = make_problem(ch.swap, A, B, M, N, K, lda, ldb, layoutA, layoutB);
+    const int slot = out_slot(accum_dtype, out_dtype);
+    switch (ch.kind) {
+        case kCfgSingle16: return launch_single16(plan, slot, ch, pr, C, D, ldc, alpha, beta, s);
+        case kCfgSingle64: return launch_single64(plan, slot, ch, pr, C, D, ldc, alpha, beta, s);
+        case kCfgSingle256: return launch_single256(plan, slot, ch, pr, C, D, ldc, alpha, beta, s);
+        case kCfgPair224: return launch_pair224(plan, slot, ch, pr, C, D, ldc, alpha, beta, s);
+        default: return launch_pair256(plan, slot, ch, pr, C, D, ldc, alpha, beta, s);
+    }
+}
