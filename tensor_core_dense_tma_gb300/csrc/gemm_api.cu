@@ -99,15 +99,27 @@ int default_units(const gemm_plan* plan, int kind) {
     return u > 0 ? u : plan->sm_count / kCfgCtas[kind];
 }
 
+// Columns of B one tile loads per K step: the tile width, or whole 64-column
+// boxes per CTA when B is N-contiguous (row-major B, or A of a swapped problem
+// stored column-major) and the per-CTA width is not a multiple of 64.
+int64_t loaded_cols(int kind, bool b_mn_major) {
+    const int64_t per_cta = kCfgTileN[kind] / kCfgCtas[kind];
+    if (!b_mn_major) return kCfgTileN[kind];
+    return ((per_cta + 63) / 64) * 64 * kCfgCtas[kind];
+}
+
 // Configuration, K-split count and orientation with the smallest modelled
-// time: waves of work items times the per-item cost times the tile width.
-// The per-item cost, in 64-deep k-blocks, is the item's k-blocks plus a
-// fixed per-item overhead of 4, plus for a split the partial-sum traffic
-// (2 + splits * BN / 64: every split writes its fp32 partial and the last
-// one reads them all back).  One CTA per 128 x 256 tile is charged 15 %
-// more per column than a CTA pair (it re-reads B for every 128 rows).
+// time.  A tile costs (k-blocks + 4 fixed) x the B columns it loads per K
+// step (the operand feed, not the MMA width, sets the pace); one CTA per
+// 128 x 256 tile is charged 15 % more (it re-reads B for every 128 rows).
+// Whole waves of tiles run unsplit; when tiles are left over for a partial
+// last wave (or there are fewer tiles than units), those tiles are split
+// into `s` K ranges, each split costing its k-blocks + 4, plus the partial-sum
+// traffic (2 + s * BN / 64: every split writes its fp32 partial and the last
+// one reads them all back).
 // `valid` is false when a pinned configuration does not fit the problem.
-Choice choose(const gemm_plan* plan, int64_t M, int64_t N, int64_t K, gemm_dtype_t acc, bool* valid) {
+Choice choose(const gemm_plan* plan, int64_t M, int64_t N, int64_t K, gemm_dtype_t acc, bool b_mn_major,
+              bool* valid) {
     Choice best;
     *valid = true;
     const bool swap = M <= 64 && N > M;
@@ -136,33 +148,44 @@ Choice choose(const gemm_plan* plan, int64_t M, int64_t N, int64_t K, gemm_dtype
         const int64_t units = default_units(plan, kind);
         const int64_t tiles = ((Mk + kCfgTileM[kind] - 1) / kCfgTileM[kind]) *
                               ((Nk + kCfgTileN[kind] - 1) / kCfgTileN[kind]);
+        const int64_t dp = tiles >= units ? (tiles / units) * units : 0;   // tiles of whole waves
+        const int64_t rest = tiles - dp;                                      // the partial wave
         const int64_t tile_bytes = int64_t(kCfgCtas[kind]) * 128 * kCfgTileN[kind] * 4;
         int64_t smax = acc == GEMM_F16 ? 1 : kMaxSplits;       // fp16 accumulation is never split
         if (smax > kb) smax = kb;
-        while (smax > 1 && (tiles * smax * tile_bytes > static_cast<int64_t>(kWorkspaceBytes) ||
-                            tiles * kCfgCtas[kind] > kNumCounters))
+        if (rest == 0) smax = 1;
+        while (smax > 1 && (rest * smax * tile_bytes > static_cast<int64_t>(kWorkspaceBytes) ||
+                            rest * kCfgCtas[kind] > kNumCounters))
             --smax;
         int64_t smin = 1;
         if (plan->forced_kind >= 0 && plan->forced_splits > 0) {
-            if (plan->forced_splits > smax) {
+            if (plan->forced_splits > 1 && (plan->forced_splits > kb || acc == GEMM_F16 ||
+                                            tiles * plan->forced_splits * tile_bytes >
+                                                static_cast<int64_t>(kWorkspaceBytes) ||
+                                            tiles * kCfgCtas[kind] > kNumCounters)) {
                 *valid = false;
                 return best;
             }
             smin = smax = plan->forced_splits;
-        } else if (smax > 1 && tiles >= units) {
-            smax = 1;                                          // enough tiles: no split
         }
-        const double eff = kind == kCfgSingle256 ? 1.15 : 1.0;
+        const double width = static_cast<double>(loaded_cols(kind, swap ? false : b_mn_major)) *
+                             (kind == kCfgSingle256 ? 1.15 : 1.0);
         for (int64_t s = smin; s <= smax; ++s) {
-            const int64_t work = tiles * s;
-            const int64_t waves = (work + units - 1) / units;
+            // a pinned split count splits every tile (dp = 0), as documented
+            const bool pinned = plan->forced_kind >= 0 && plan->forced_splits > 0;
+            const int64_t dp_s = s == 1 ? tiles : (pinned ? 0 : dp);
+            const int64_t split_tiles = tiles - dp_s;
+            const int64_t waves_dp = (dp_s + units - 1) / units;
+            const int64_t waves_split = (split_tiles * s + units - 1) / units;
             const double reduce = s > 1 ? 2.0 + static_cast<double>(s) * kCfgTileN[kind] / 64.0 : 0.0;
-            const double per_item = static_cast<double>((kb + s - 1) / s + 4) + reduce;
-            const double cost = static_cast<double>(waves) * per_item * kCfgTileN[kind] * eff;
+            const double cost = (static_cast<double>(waves_dp) * static_cast<double>(kb + 4) +
+                                 static_cast<double>(waves_split) *
+                                     (static_cast<double>((kb + s - 1) / s + 4) + reduce)) * width;
             if (best_cost < 0 || cost < best_cost) {
                 best_cost = cost;
                 best.kind = kind;
                 best.splits = static_cast<int>(s);
+                best.dp_tiles = dp_s;
                 best.swap = swap;
                 best.tiles = tiles;
                 best.units = static_cast<int>(units);
@@ -244,6 +267,7 @@ gemm_status_t gemm_plan_create(gemm_plan_t* out, int device, gemm_dtype_t in_dty
     bool ok = cudaMalloc(&plan->d_status, 2 * sizeof(int)) == cudaSuccess &&
               cudaMemset(plan->d_status, 0, 2 * sizeof(int)) == cudaSuccess &&
               cudaMalloc(&plan->d_ws, kWorkspaceBytes) == cudaSuccess &&
+              (plan->ws_bytes = kWorkspaceBytes) > 0 &&
               cudaMalloc(&plan->d_counters, kNumCounters * sizeof(int)) == cudaSuccess &&
               cudaMemset(plan->d_counters, 0, kNumCounters * sizeof(int)) == cudaSuccess &&
               prepare_all(plan) == GEMM_OK;
@@ -281,7 +305,7 @@ gemm_status_t gemm_run(gemm_plan_t plan, const void* A, const void* B, const voi
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (K == 0) return launch_scale(plan, C, D, M, N, ldc, out_dtype, beta, s);
     bool valid = true;
-    const Choice ch = choose(plan, M, N, K, accum_dtype, &valid);
+    const Choice ch = choose(plan, M, N, K, accum_dtype, layoutB == GEMM_ROW_MAJOR, &valid);
     if (!valid) return GEMM_ERR_UNSUPPORTED;
     const Problem pr = make_problem(ch.swap, A, B, M, N, K, lda, ldb, layoutA, layoutB);
     const int slot = out_slot(accum_dtype, out_dtype);
@@ -354,12 +378,13 @@ gemm_status_t gemm_plan_describe(gemm_plan_t plan, int64_t M, int64_t N, int64_t
         return GEMM_OK;
     }
     bool valid = true;
-    const Choice ch = choose(plan, M, N, K, accum_dtype, &valid);
+    const Choice ch = choose(plan, M, N, K, accum_dtype, layoutB == GEMM_ROW_MAJOR, &valid);
     if (!valid) return GEMM_ERR_UNSUPPORTED;
-    const int64_t work = ch.tiles * ch.splits;
+    const int64_t work = ch.splits > 1 ? ch.dp_tiles + (ch.tiles - ch.dp_tiles) * ch.splits : ch.tiles;
     const int64_t units = work < ch.units ? work : ch.units;
-    std::snprintf(buf, static_cast<size_t>(len), "%s tiles=%lld splits=%d ctas=%lld sms=%d",
-                  config_name(ch, accum_dtype, out_dtype).c_str(), static_cast<long long>(ch.tiles), ch.splits,
+    std::snprintf(buf, static_cast<size_t>(len), "%s tiles=%lld split_tiles=%lld splits=%d ctas=%lld sms=%d",
+                  config_name(ch, accum_dtype, out_dtype).c_str(), static_cast<long long>(ch.tiles),
+                  static_cast<long long>(ch.splits > 1 ? ch.tiles - ch.dp_tiles : 0), ch.splits,
                   static_cast<long long>(units * kCfgCtas[ch.kind]), plan->sm_count);
     return GEMM_OK;
 }
@@ -456,6 +481,7 @@ gemm_status_t static_setup(int device, StaticDeviceState& st) {
         pl.d_status = reinterpret_cast<int*>(st.scratch + kStaticStatusOffset);
         pl.d_counters = reinterpret_cast<int*>(st.scratch + kStaticCountersOffset);
         pl.d_ws = reinterpret_cast<float*>(st.scratch + kStaticPartialsOffset);
+        pl.ws_bytes = kStaticPartialsBytes;
         pl.encode = reinterpret_cast<EncodeTiledFn>(fn);
         if (prepare_all(&pl) != GEMM_OK) return GEMM_ERR_CUDA;
     }
@@ -495,11 +521,12 @@ extern "C" gemm_status_t gemm_run_static_scratch(int device, gemm_dtype_t in_dty
 
     // the configuration gemm_run would pick, with the caller's split count
     bool valid = true;
-    Choice ch = choose(plan, M, N, K, accum_dtype, &valid);
+    Choice ch = choose(plan, M, N, K, accum_dtype, layoutB == GEMM_ROW_MAJOR, &valid);
     if (!valid) return GEMM_ERR_UNSUPPORTED;
     const int64_t kb = (K + 63) / 64;
     if (splits > kb || (accum_dtype == GEMM_F16 && splits > 1)) return GEMM_ERR_UNSUPPORTED;
     ch.splits = splits;
+    ch.dp_tiles = 0;   // every tile is split `splits` ways
     // the size limit: split partials and counters must fit the fixed array
     if (splits > 1) {
         const int64_t ctas = kCfgCtas[ch.kind];

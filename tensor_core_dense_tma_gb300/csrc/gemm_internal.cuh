@@ -7,6 +7,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <cstring>
 #include <string>
 
 #include "gemm.h"
@@ -32,7 +33,7 @@ constexpr int kMaxSplits = 16;
 //                        rows (D^T = B^T A^T puts the long N side on the
 //                        128-row MMA dimension);
 //  single256           : one CTA, 128 x 256, 4 stages of 48 KB;
-//  pair256             : CTA pair (cta_group::2), 256 x 256, 7 stages of 32 KB per CTA;
+//  pair256             : CTA pair (cta_group::2), 256 x 256, 6 stages of 32 KB per CTA;
 //  pair224             : CTA pair, 256 x 224 (fills whole waves where 256 leaves a
 //                        partial one, e.g. N = 4096: 19 column tiles x 16 = 4 x 76 pairs).
 template <bool ACC16, int OUT>
@@ -42,9 +43,9 @@ using CfgSingle64 = tcdt::TileConfig<64, 8, 1, ACC16, OUT>;
 template <bool ACC16, int OUT>
 using CfgSingle256 = tcdt::TileConfig<256, 4, 1, ACC16, OUT>;
 template <bool ACC16, int OUT>
-using CfgPair256 = tcdt::TileConfig<256, 7, 2, ACC16, OUT>;
+using CfgPair256 = tcdt::TileConfig<256, 6, 2, ACC16, OUT>;
 template <bool ACC16, int OUT>
-using CfgPair224 = tcdt::TileConfig<224, 7, 2, ACC16, OUT>;
+using CfgPair224 = tcdt::TileConfig<224, 6, 2, ACC16, OUT>;
 
 enum ConfigId : int {
     kCfgSingle16 = 0,
@@ -77,6 +78,7 @@ struct gemm_plan {
     tcdt_host::EncodeTiledFn encode = nullptr;
     bool attr_set[tcdt_host::kNumCfgKinds][4] = {};
     int units[tcdt_host::kNumCfgKinds] = {};  // co-resident CTAs (single) or CTA pairs (pair)
+    size_t ws_bytes = 0;          // capacity of d_ws
     int forced_kind = -1;         // gemm_plan_force_config
     int forced_splits = 0;
 };
@@ -96,6 +98,7 @@ struct Problem {
 struct Choice {
     int kind = kCfgPair256;
     int splits = 1;
+    int64_t dp_tiles = 0;      // whole tiles before the split ones (see KernelParams)
     bool swap = false;
     int64_t tiles = 0;
     int units = 0;
@@ -116,16 +119,19 @@ TCDT_DECLARE_KIND(pair224)
 // 2-D tensor map over a matrix whose contiguous dimension has `inner`
 // elements (rows of `ld` elements), 128-byte swizzle, zero fill outside.
 inline gemm_status_t encode_map(const gemm_plan* plan, CUtensorMap* map, const void* ptr, uint64_t inner,
-                         uint64_t outer, uint64_t ld, uint32_t box_inner, uint32_t box_outer) {
+                                uint64_t outer, uint64_t ld, uint32_t box_inner, uint32_t box_outer,
+                                gemm_dtype_t dtype, CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
+    const uint64_t esz = dtype == GEMM_F32 ? 4 : 2;
     const cuuint64_t dims[2] = {inner, outer};
-    const cuuint64_t strides[1] = {ld * 2};
+    const cuuint64_t strides[1] = {ld * esz};
     const cuuint32_t box[2] = {box_inner, box_outer};
     const cuuint32_t estr[2] = {1, 1};
-    const CUtensorMapDataType dt = plan->in_dtype == GEMM_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
-                                                              : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const CUtensorMapDataType dt = dtype == GEMM_F32   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                   : dtype == GEMM_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                       : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     CUresult r = plan->encode(map, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr,
-                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
@@ -189,17 +195,37 @@ gemm_status_t prepare(gemm_plan* plan, int kind, int slot) {
 
 template <class Cfg>
 gemm_status_t launch_tc(gemm_plan* plan, const Choice& ch, const Problem& pr, const void* C, void* D,
-                        int64_t ldc, float alpha, float beta, cudaStream_t stream) {
+                        int64_t ldc, float alpha, float beta, gemm_dtype_t out_dtype, cudaStream_t stream) {
     const bool a_mn = pr.la == GEMM_COL_MAJOR;   // column-major A is M-contiguous
     const bool b_mn = pr.lb == GEMM_ROW_MAJOR;   // row-major B is N-contiguous
     CUtensorMap tmA, tmB;
     gemm_status_t st;
-    if (a_mn) st = encode_map(plan, &tmA, pr.A, pr.M, pr.K, pr.lda, 64, 64);
-    else st = encode_map(plan, &tmA, pr.A, pr.K, pr.M, pr.lda, 64, Cfg::BM);
+    const gemm_dtype_t in_dt = plan->in_dtype;
+    if (a_mn) st = encode_map(plan, &tmA, pr.A, pr.M, pr.K, pr.lda, 64, 64, in_dt);
+    else st = encode_map(plan, &tmA, pr.A, pr.K, pr.M, pr.lda, 64, Cfg::BM, in_dt);
     if (st != GEMM_OK) return st;
-    if (b_mn) st = encode_map(plan, &tmB, pr.B, pr.N, pr.K, pr.ldb, 64, 64);
-    else st = encode_map(plan, &tmB, pr.B, pr.K, pr.N, pr.ldb, 64, Cfg::BN_CTA);
+    if (b_mn) st = encode_map(plan, &tmB, pr.B, pr.N, pr.K, pr.ldb, 64, 64, in_dt);
+    else st = encode_map(plan, &tmB, pr.B, pr.K, pr.N, pr.ldb, 64, Cfg::BN_CTA, in_dt);
     if (st != GEMM_OK) return st;
+    // D through TMA stores: 32 x 32 boxes, rows of 128 bytes (fp32, 128-byte
+    // swizzle) or 64 bytes (16-bit, 64-byte swizzle); needs 16-byte aligned rows
+    const int64_t out_esz = out_dtype == GEMM_F32 ? 4 : 2;
+    const bool d_tma = Cfg::W == 32 && !pr.swap && (reinterpret_cast<uintptr_t>(D) % 16) == 0 &&
+                       (ldc * out_esz) % 16 == 0;
+    CUtensorMap tmD, tmW;
+    std::memset(&tmD, 0, sizeof(tmD));
+    std::memset(&tmW, 0, sizeof(tmW));
+    if (d_tma) {
+        st = encode_map(plan, &tmD, D, pr.N, pr.M, ldc, 32, 32, out_dtype,
+                        out_esz == 4 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
+        if (st != GEMM_OK) return st;
+    }
+    if (ch.splits > 1 && Cfg::W == 32) {
+        // the workspace as a [rows][BN] fp32 matrix; a split's partial is 128 rows of it
+        const uint64_t ws_rows = plan->ws_bytes / (static_cast<uint64_t>(Cfg::BN) * 4);
+        st = encode_map(plan, &tmW, plan->d_ws, Cfg::BN, ws_rows, Cfg::BN, 32, 32, GEMM_F32);
+        if (st != GEMM_OK) return st;
+    }
 
     KernelParams p{};
     p.M = static_cast<int32_t>(pr.M);
@@ -210,6 +236,7 @@ gemm_status_t launch_tc(gemm_plan* plan, const Choice& ch, const Problem& pr, co
     p.num_k_blocks = static_cast<int32_t>((pr.K + Cfg::BK - 1) / Cfg::BK);
     p.num_tiles = p.num_m_blocks * p.num_n_blocks;
     p.splits = ch.splits;
+    p.dp_tiles = static_cast<int32_t>(ch.splits > 1 ? ch.dp_tiles : p.num_tiles);
     p.group_m = 8;
     p.ldc = ldc;
     p.C = C;
@@ -220,6 +247,7 @@ gemm_status_t launch_tc(gemm_plan* plan, const Choice& ch, const Problem& pr, co
     p.a_mn_major = a_mn;
     p.b_mn_major = b_mn;
     p.trans_out = pr.swap ? 1u : 0u;
+    p.d_tma = d_tma ? 1u : 0u;
     p.ws = plan->d_ws;
     p.counters = plan->d_counters;
     p.status = plan->d_status;
@@ -228,10 +256,10 @@ gemm_status_t launch_tc(gemm_plan* plan, const Choice& ch, const Problem& pr, co
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[1];
     fill_launch_config<Cfg>(cfg, attr, stream);
-    const int64_t work = static_cast<int64_t>(p.num_tiles) * p.splits;
+    const int64_t work = p.dp_tiles + static_cast<int64_t>(p.num_tiles - p.dp_tiles) * p.splits;
     const int units = work < ch.units ? static_cast<int>(work) : ch.units;
     cfg.gridDim = dim3(Cfg::CG * units, 1, 1);
-    if (cudaLaunchKernelEx(&cfg, tcdt::gemm_sm103_kernel<Cfg>, tmA, tmB, p) != cudaSuccess) {
+    if (cudaLaunchKernelEx(&cfg, tcdt::gemm_sm103_kernel<Cfg>, tmA, tmB, tmD, tmW, p) != cudaSuccess) {
         cudaGetLastError();
         return GEMM_ERR_CUDA;
     }
@@ -255,10 +283,10 @@ gemm_status_t launch_kind(gemm_plan* plan, int slot, const Choice& ch, const Pro
     gemm_status_t st = prepare_kind<CfgT>(plan, ch.kind, slot);
     if (st != GEMM_OK) return st;
     switch (slot) {
-        case 0: return launch_tc<CfgT<false, tcdt::kOutF32>>(plan, ch, pr, C, D, ldc, alpha, beta, s);
-        case 1: return launch_tc<CfgT<false, tcdt::kOutF16>>(plan, ch, pr, C, D, ldc, alpha, beta, s);
-        case 2: return launch_tc<CfgT<false, tcdt::kOutBF16>>(plan, ch, pr, C, D, ldc, alpha, beta, s);
-        default: return launch_tc<CfgT<true, tcdt::kOutF16>>(plan, ch, pr, C, D, ldc, alpha, beta, s);
+        case 0: return launch_tc<CfgT<false, tcdt::kOutF32>>(plan, ch, pr, C, D, ldc, alpha, beta, GEMM_F32, s);
+        case 1: return launch_tc<CfgT<false, tcdt::kOutF16>>(plan, ch, pr, C, D, ldc, alpha, beta, GEMM_F16, s);
+        case 2: return launch_tc<CfgT<false, tcdt::kOutBF16>>(plan, ch, pr, C, D, ldc, alpha, beta, GEMM_BF16, s);
+        default: return launch_tc<CfgT<true, tcdt::kOutF16>>(plan, ch, pr, C, D, ldc, alpha, beta, GEMM_F16, s);
     }
 }
 

@@ -62,7 +62,8 @@ enum WaitSite : int {
 struct KernelParams {
     int32_t M, N, K;          // of the product the kernel computes (swapped when trans_out)
     int32_t num_m_blocks, num_n_blocks, num_k_blocks, num_tiles;
-    int32_t splits;           // K ranges per tile (1: whole K)
+    int32_t dp_tiles;         // tiles [0, dp_tiles) are whole work items ...
+    int32_t splits;           // ... the rest are split into this many K ranges
     int32_t group_m;          // m-blocks per raster group
     int64_t ldc;
     const void* C;            // may alias D; unread when beta == 0
@@ -72,8 +73,9 @@ struct KernelParams {
     uint32_t a_mn_major;      // 1: A is M-contiguous
     uint32_t b_mn_major;      // 1: B is N-contiguous
     uint32_t trans_out;       // 1: element (r, c) goes to D[c*ldc + r]
-    float* ws;                // split partials, [tile][split][cta][128][BN] fp32
-    int* counters;            // [tile][cta] split arrivals; zero on entry, left zero
+    uint32_t d_tma;           // 1: D rows are 16-byte aligned: store D tiles with TMA (tmD)
+    float* ws;                // split partials, [split tile][split][cta][128][BN] fp32
+    int* counters;            // [split tile][cta] split arrivals; zero on entry, left zero
     int* status;              // [0] status code, [1] site
     uint64_t timeout_ns;
 };
@@ -106,8 +108,12 @@ struct TileConfig {
     static constexpr int NUM_EPI_WARPS = 4;
     static constexpr int NUM_THREADS = 32 * (2 + NUM_EPI_WARPS);
     static constexpr int NUM_BARRIERS = 2 * STAGES + 2 + 2 + 1;
+    // epilogue staging for TMA stores: per epilogue warp two 32-row buffers
+    // of up to 128 bytes a row (32 fp32 columns)
+    static constexpr int STAGING_BUF = 32 * 128;
+    static constexpr int STAGING_BYTES = NUM_EPI_WARPS * 2 * STAGING_BUF;
     // after the barriers: TMEM address, abort flag, 2 wait flags, 2 split flags
-    static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + NUM_BARRIERS * 8 + 32;
+    static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + STAGING_BYTES + NUM_BARRIERS * 8 + 32;
     static_assert(CG == 1 || CG == 2, "CTA group");
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N");
     static_assert(BN % W == 0, "whole tcgen05.ld chunks");
@@ -136,17 +142,38 @@ __host__ __device__ constexpr int largest_divisor_upto(int n, int cap) {
     return best;
 }
 
-// Work item w: split (w % splits) of tile (w / splits); the splits of a
-// tile are consecutive items, so they run at the same time on neighbouring
-// units.  Each split covers k-blocks [kb0, kb1), never empty (splits <= k-blocks).
+// Work items: first the dp_tiles whole tiles, then the remaining tiles each
+// split into `splits` contiguous K ranges.  The splits of a tile are
+// consecutive items, so they run at the same time on neighbouring units;
+// a split covers k-blocks [kb0, kb1), never empty (splits <= k-blocks).
+// With dp_tiles = (whole waves of tiles) only the last, partial wave is
+// split, so its tiles spread over all units instead of leaving most idle.
 struct WorkItem {
-    int tile, split, kb0, kb1;
+    int tile;      // output tile
+    int stile;     // index among the split tiles (-1: a whole tile)
+    int split, nsplit, kb0, kb1;
 };
+
+__device__ __forceinline__ int num_work_items(const KernelParams& p) {
+    return p.dp_tiles + (p.num_tiles - p.dp_tiles) * p.splits;
+}
 
 __device__ __forceinline__ WorkItem work_item(const KernelParams& p, int w) {
     WorkItem x;
-    x.tile = w / p.splits;
-    x.split = w - x.tile * p.splits;
+    if (w < p.dp_tiles) {
+        x.tile = w;
+        x.stile = -1;
+        x.split = 0;
+        x.nsplit = 1;
+        x.kb0 = 0;
+        x.kb1 = p.num_k_blocks;
+        return x;
+    }
+    const int t = w - p.dp_tiles;
+    x.stile = t / p.splits;
+    x.tile = p.dp_tiles + x.stile;
+    x.split = t - x.stile * p.splits;
+    x.nsplit = p.splits;
     x.kb0 = static_cast<int>(static_cast<int64_t>(p.num_k_blocks) * x.split / p.splits);
     x.kb1 = static_cast<int>(static_cast<int64_t>(p.num_k_blocks) * (x.split + 1) / p.splits);
     return x;
@@ -425,12 +452,87 @@ __device__ __forceinline__ void prefetch_c_row(const KernelParams& p, int row, i
     if (b > a) prefetch_l2_bulk(reinterpret_cast<const void*>(a), static_cast<uint32_t>(b - a));
 }
 
+// One 32-row x 32-column segment of this warp through its staging buffer:
+// wait until the buffer's previous TMA store has read it, write the row of
+// this lane (swizzled as the tensor map expects: 128-byte rows for fp32,
+// 64-byte rows for 16-bit types), make it visible to the async proxy, and
+// let lane 0 issue the store.  Rows and columns outside D are clipped by TMA.
+template <int OUT>
+__device__ __forceinline__ void stage_row_and_store(const void* tmap, const uint32_t (&words)[OUT == kOutF32 ? 32 : 16],
+                                                    int col0, int row0, int lane, uint32_t stg, int& sbuf) {
+    const uint32_t dst = stg + static_cast<uint32_t>(sbuf) * 4096u;
+    if (lane == 0) bulk_wait_group_read<1>();
+    __syncwarp();
+    if constexpr (OUT == kOutF32) {
+        const uint32_t rowp = dst + static_cast<uint32_t>(lane) * 128u;
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch)
+            st_shared_v4(rowp + ((static_cast<uint32_t>(ch) ^ (lane & 7u)) << 4), words[4 * ch], words[4 * ch + 1],
+                         words[4 * ch + 2], words[4 * ch + 3]);
+    } else {
+        const uint32_t rowp = dst + static_cast<uint32_t>(lane) * 64u;
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch)
+            st_shared_v4(rowp + ((static_cast<uint32_t>(ch) ^ ((lane >> 1) & 3u)) << 4), words[4 * ch],
+                         words[4 * ch + 1], words[4 * ch + 2], words[4 * ch + 3]);
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+        tma_store_2d(tmap, dst, col0, row0);
+        bulk_commit_group();
+    }
+    sbuf ^= 1;
+}
+
+// Epilogue values of one segment -> D through the staging buffer.
+template <class Cfg>
+__device__ __forceinline__ void stage_and_store(const KernelParams& p, const void* tmap, float (&v)[32], int row,
+                                                int col0, int row0w, int lane, uint32_t stg, int& sbuf,
+                                                bool row_ok) {
+    constexpr int ESZ = Vec<Cfg::OUT>::ESZ;
+    float acc[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) acc[i] = v[i];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = p.alpha * acc[i];
+    if (p.beta != 0.0f && row_ok) {
+        const int n = min(32, p.N - col0);
+        float c[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) c[i] = 0.0f;
+        const int64_t off = static_cast<int64_t>(row) * p.ldc + col0;
+        row_segment_dispatch<Cfg::OUT, 32, false>(
+            const_cast<char*>(static_cast<const char*>(p.C)) + off * ESZ, c, n);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = fmaf(p.alpha, acc[i], p.beta * c[i]);
+    }
+    if constexpr (Cfg::OUT == kOutF32) {
+        uint32_t words[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) words[i] = __float_as_uint(v[i]);
+        stage_row_and_store<kOutF32>(tmap, words, col0, row0w, lane, stg, sbuf);
+    } else {
+        uint32_t words[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) words[i] = pack2<Cfg::OUT>(v[2 * i], v[2 * i + 1]);
+        stage_row_and_store<Cfg::OUT>(tmap, words, col0, row0w, lane, stg, sbuf);
+    }
+}
+
+// A split's fp32 partial segment -> the workspace through the staging buffer.
+__device__ __forceinline__ void stage_and_store_f32(const void* tmap, const uint32_t (&r)[32], int col0, int row0,
+                                                    int lane, uint32_t stg, int& sbuf) {
+    stage_row_and_store<kOutF32>(tmap, r, col0, row0, lane, stg, sbuf);
+}
+
 // ---------------------------------------------------------------------------
 // the kernel
 // ---------------------------------------------------------------------------
 template <class Cfg>
 __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
 gemm_sm103_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                  const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmW,
                   const KernelParams p) {
     constexpr int CG = Cfg::CG;
     constexpr int W = Cfg::W;
@@ -439,14 +541,15 @@ gemm_sm103_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     const uint32_t base = (raw + 1023u) & ~1023u;   // 128B-swizzle atoms need 1024-byte alignment
     uint8_t* base_ptr = smem_raw + (base - raw);
 
-    const uint32_t bar_base = base + Cfg::STAGES * Cfg::STAGE_BYTES;
+    const uint32_t staging_base = base + Cfg::STAGES * Cfg::STAGE_BYTES;   // 1024-byte aligned
+    const uint32_t bar_base = staging_base + Cfg::STAGING_BYTES;
     auto full_bar = [&](int s) { return bar_base + 8u * s; };
     auto empty_bar = [&](int s) { return bar_base + 8u * (Cfg::STAGES + s); };
     auto accf_bar = [&](int b) { return bar_base + 8u * (2 * Cfg::STAGES + b); };
     auto acce_bar = [&](int b) { return bar_base + 8u * (2 * Cfg::STAGES + 2 + b); };
     const uint32_t drain_bar = bar_base + 8u * (2 * Cfg::STAGES + 4);
-    uint32_t* tmem_slot =
-        reinterpret_cast<uint32_t*>(base_ptr + Cfg::STAGES * Cfg::STAGE_BYTES + 8 * Cfg::NUM_BARRIERS);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base_ptr + Cfg::STAGES * Cfg::STAGE_BYTES +
+                                                      Cfg::STAGING_BYTES + 8 * Cfg::NUM_BARRIERS);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     volatile int* epi_ok_flag = reinterpret_cast<volatile int*>(tmem_slot + 2);     // [2]
     volatile int* epi_last_flag = reinterpret_cast<volatile int*>(tmem_slot + 4);   // [2]
@@ -458,7 +561,7 @@ gemm_sm103_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     const int unit = CG == 1 ? static_cast<int>(blockIdx.x) : static_cast<int>(cluster_id_x());
     const int num_units = CG == 1 ? static_cast<int>(gridDim.x) : static_cast<int>(num_clusters_x());
     const bool leader = rank == 0;
-    const int num_work = p.num_tiles * p.splits;
+    const int num_work = num_work_items(p);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < Cfg::STAGES; ++s) {
@@ -476,6 +579,10 @@ gemm_sm103_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
+    }
+    if (warp == 2 && lane == 0) {
+        if (p.d_tma) tma_prefetch_desc(&tmD);
+        if (p.splits > 1) tma_prefetch_desc(&tmW);
     }
     if (warp == 1) {
         tmem_alloc<CG>(smem_addr(tmem_slot), Cfg::TMEM_COLS);
@@ -638,6 +745,8 @@ gemm_sm103_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         // ------------------------------------------------------------------
         const int quad = warp % 4;
         const int row_local = 32 * quad + lane;
+        const uint32_t stg = staging_base + static_cast<uint32_t>(warp - 2) * 2u * Cfg::STAGING_BUF;
+        int sbuf = 0;                     // staging buffer for the next TMA store of this warp
         int buf = 0;
         uint32_t acc_phase = 0;
         int iter = 0;
@@ -658,45 +767,83 @@ gemm_sm103_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             const int row = m0 + row_local;
             const bool row_ok = row < p.M;
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(32 * quad) << 16) + buf * Cfg::ACC_COLS;
-            if (p.splits == 1) {
+            if (x.nsplit == 1) {
+                bool staged = false;
+                if constexpr (W == 32) {
+                    if (p.d_tma) {
+                        // staged through shared memory, one TMA store per 32 x 32 segment
+                        staged = true;
+                        const int row0w = m0 + 32 * quad;
 #pragma unroll 1
-                for (int c = 0; c < Cfg::BN / W; ++c) {
-                    const int col0 = n0 + W * c;
-                    if (col0 >= p.N) break;   // warp-uniform
-                    __syncwarp();             // tcgen05.ld is .sync.aligned: converge the warp
-                    uint32_t r[W];
-                    tmem_ld_row<W>(t_row + W * c, r);
-                    tmem_ld_wait();
-                    if (!row_ok) continue;
-                    float acc[W];
+                        for (int c = 0; c < Cfg::BN / W; ++c) {
+                            const int col0 = n0 + W * c;
+                            if (col0 >= p.N) break;   // warp-uniform
+                            __syncwarp();
+                            uint32_t r[W];
+                            tmem_ld_row<W>(t_row + W * c, r);
+                            tmem_ld_wait();
+                            if (row0w >= p.M) continue;   // warp-uniform: no row of this warp exists
+                            float v[W];
 #pragma unroll
-                    for (int i = 0; i < W; ++i) acc[i] = acc_value<Cfg::ACC_F16>(r[i]);
-                    epilogue_chunk<Cfg>(p, acc, row, col0);
+                            for (int i = 0; i < W; ++i) v[i] = acc_value<Cfg::ACC_F16>(r[i]);
+                            stage_and_store<Cfg>(p, &tmD, v, row, col0, row0w, lane, stg, sbuf, row_ok);
+                        }
+                    }
+                }
+                if (!staged) {
+#pragma unroll 1
+                    for (int c = 0; c < Cfg::BN / W; ++c) {
+                        const int col0 = n0 + W * c;
+                        if (col0 >= p.N) break;   // warp-uniform
+                        __syncwarp();             // tcgen05.ld is .sync.aligned: converge the warp
+                        uint32_t r[W];
+                        tmem_ld_row<W>(t_row + W * c, r);
+                        tmem_ld_wait();
+                        if (!row_ok) continue;
+                        float acc[W];
+#pragma unroll
+                        for (int i = 0; i < W; ++i) acc[i] = acc_value<Cfg::ACC_F16>(r[i]);
+                        epilogue_chunk<Cfg>(p, acc, row, col0);
+                    }
                 }
             } else {
                 // 1. this split's fp32 partial -> workspace ([128][BN] per CTA)
                 const int64_t tile_elems = static_cast<int64_t>(Cfg::BM) * Cfg::BN;
                 auto slot = [&](int split) {
-                    return p.ws + ((static_cast<int64_t>(x.tile) * p.splits + split) * CG + rank) * tile_elems;
+                    return p.ws + ((static_cast<int64_t>(x.stile) * p.splits + split) * CG + rank) * tile_elems;
                 };
                 float* mine = slot(x.split) + static_cast<int64_t>(row_local) * Cfg::BN;
+                const int ws_row0 = static_cast<int>(
+                    ((static_cast<int64_t>(x.stile) * p.splits + x.split) * CG + rank) * Cfg::BM + 32 * quad);
 #pragma unroll 1
                 for (int c = 0; c < Cfg::BN / W; ++c) {
                     __syncwarp();
                     uint32_t r[W];
                     tmem_ld_row<W>(t_row + W * c, r);
                     tmem_ld_wait();
+                    if constexpr (W == 32) {
+                        stage_and_store_f32(&tmW, r, W * c, ws_row0, lane, stg, sbuf);
+                    } else {
 #pragma unroll
-                    for (int i = 0; i < W; i += 4)
-                        __stcg(reinterpret_cast<float4*>(mine + W * c + i),
-                               make_float4(__uint_as_float(r[i]), __uint_as_float(r[i + 1]),
-                                           __uint_as_float(r[i + 2]), __uint_as_float(r[i + 3])));
+                        for (int i = 0; i < W; i += 4)
+                            __stcg(reinterpret_cast<float4*>(mine + W * c + i),
+                                   make_float4(__uint_as_float(r[i]), __uint_as_float(r[i + 1]),
+                                               __uint_as_float(r[i + 2]), __uint_as_float(r[i + 3])));
+                    }
+                }
+                if constexpr (W == 32) {
+                    // the partial must be in global memory before the arrival is counted
+                    if (lane == 0) {
+                        bulk_wait_group<0>();
+                        fence_proxy_async_global();
+                    }
+                    __syncwarp();
                 }
                 // 2. count arrivals; the last split of the tile reduces
                 __threadfence();
                 named_bar_sync(1, 32 * Cfg::NUM_EPI_WARPS);
                 if (threadIdx.x == 64) {
-                    int* ctr = p.counters + static_cast<int64_t>(x.tile) * CG + rank;
+                    int* ctr = p.counters + static_cast<int64_t>(x.stile) * CG + rank;
                     const int old = atomicAdd(ctr, 1);
                     const int last = old == p.splits - 1;
                     if (last) atomicExch(ctr, 0);   // ready for the next launch
@@ -758,6 +905,9 @@ gemm_sm103_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 acc_phase ^= 1u;
             }
         }
+        // TMA stores still reading the staging buffers (or writing D) finish first
+        if (lane == 0) bulk_wait_group<0>();
+        __syncwarp();
     }
 
     tc_fence_before_sync();

@@ -151,3 +151,18 @@ def test_pinned_config_that_does_not_fit(plans):
         assert e.value.status == 2
     finally:
         plan.force_config("auto")
+
+
+@pytest.mark.parametrize("shape", [(4096, 4096, 1024), (2560, 2560, 2048)], ids=lambda s: "x".join(map(str, s)))
+def test_partial_wave_split(plans, shape):
+    """Whole waves of tiles unsplit, the tiles of the last partial wave split
+    along K: sampled entries bit-exact on the integer twin."""
+    from gpu_util import check_sampled
+    w = W(*shape)
+    plan = plans["f16"]
+    desc = plan.describe(w.M, w.N, w.K)
+    h = wl.make_inputs(w, integer=True)
+    D = run_gpu(plan, w, h)
+    torch.cuda.synchronize()
+    check_sampled(w, h, D, integer=True, n_random=4096)
+    return desc
