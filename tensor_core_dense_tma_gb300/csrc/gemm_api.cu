@@ -99,24 +99,38 @@ int default_units(const gemm_plan* plan, int kind) {
     return u > 0 ? u : plan->sm_count / kCfgCtas[kind];
 }
 
-// Columns of B one tile loads per K step: the tile width, or whole 64-column
-// boxes per CTA when B is N-contiguous (row-major B, or A of a swapped problem
-// stored column-major) and the per-CTA width is not a multiple of 64.
-int64_t loaded_cols(int kind, bool b_mn_major) {
-    const int64_t per_cta = kCfgTileN[kind] / kCfgCtas[kind];
-    if (!b_mn_major) return kCfgTileN[kind];
+// Columns of B one tile (or half-width item) loads per K step: the width,
+// or whole 64-column boxes per CTA when B is N-contiguous (row-major B) and
+// the per-CTA width is not a multiple of 64.
+int64_t loaded_cols(int kind, bool b_mn_major, bool half) {
+    const int64_t width = kCfgTileN[kind] / (half ? 2 : 1);
+    const int64_t per_cta = width / kCfgCtas[kind];
+    if (!b_mn_major) return width;
     return ((per_cta + 63) / 64) * 64 * kCfgCtas[kind];
 }
 
+// Time of one 64-deep K step of a tile (or half-width item) on its unit,
+// relative to a 256 x 256 tile on a CTA pair.  Per SM, the step is half
+// tensor-core work (accumulator rows x columns, 128 x 256 for the pair tile)
+// and half operand feed (A rows + B columns loaded, 128 + 128 for the pair
+// tile); the pair tile is close to balanced between the two.
+double step_cost(int kind, bool b_mn_major, bool half) {
+    const double width = static_cast<double>(kCfgTileN[kind]) / (half ? 2.0 : 1.0);
+    const double mma = 128.0 * width / (128.0 * 256.0);
+    const double feed = (128.0 + static_cast<double>(loaded_cols(kind, b_mn_major, half)) / kCfgCtas[kind]) / 256.0;
+    return 0.5 * mma + 0.5 * feed;
+}
+
 // Configuration, K-split count and orientation with the smallest modelled
-// time.  A tile costs (k-blocks + 4 fixed) x the B columns it loads per K
-// step (the operand feed, not the MMA width, sets the pace); one CTA per
-// 128 x 256 tile is charged 15 % more (it re-reads B for every 128 rows).
-// Whole waves of tiles run unsplit; when tiles are left over for a partial
-// last wave (or there are fewer tiles than units), those tiles are split
-// into `s` K ranges, each split costing its k-blocks + 4, plus the partial-sum
-// traffic (2 + s * BN / 64: every split writes its fp32 partial and the last
-// one reads them all back).
+// time: for each category of work item, waves (items over co-resident
+// units) times the item's cost in K steps (its k-blocks times step_cost, plus
+// 4 fixed).  Whole waves of tiles run whole; the tiles of a partial last
+// wave (or all tiles, when there are fewer than units) are either split into
+// `s` K ranges -- plus the partial-sum traffic, 2 + 2 * s * BN / 64 steps:
+// every split writes its fp32 partial and the last one reads them all back
+// (latency-bound, so charged double) -- or
+// run as two half-width items.  A divided tile is charged 2 extra steps, so
+// ties go to whole tiles.
 // `valid` is false when a pinned configuration does not fit the problem.
 Choice choose(const gemm_plan* plan, int64_t M, int64_t N, int64_t K, gemm_dtype_t acc, bool b_mn_major,
               bool* valid) {
@@ -124,7 +138,9 @@ Choice choose(const gemm_plan* plan, int64_t M, int64_t N, int64_t K, gemm_dtype
     *valid = true;
     const bool swap = M <= 64 && N > M;
     const int64_t Mk = swap ? N : M, Nk = swap ? M : N;
+    const bool bmn = swap ? false : b_mn_major;   // swapped: B is the small A^T, its layout does not matter
     const int64_t kb = (K + 63) / 64;
+    const bool pinned = plan->forced_kind >= 0 && plan->forced_splits > 0;
     int cands[3];
     int nc = 0;
     if (plan->forced_kind >= 0) {
@@ -143,6 +159,18 @@ Choice choose(const gemm_plan* plan, int64_t M, int64_t N, int64_t K, gemm_dtype
         cands[nc++] = kCfgSingle256;
     }
     double best_cost = -1.0;
+    auto consider = [&](double cost, int kind, int splits, int64_t dp, bool halves, int64_t tiles, int64_t units) {
+        if (best_cost < 0 || cost < best_cost) {
+            best_cost = cost;
+            best.kind = kind;
+            best.splits = splits;
+            best.dp_tiles = dp;
+            best.n_halves = halves;
+            best.swap = swap;
+            best.tiles = tiles;
+            best.units = static_cast<int>(units);
+        }
+    };
     for (int ci = 0; ci < nc; ++ci) {
         const int kind = cands[ci];
         const int64_t units = default_units(plan, kind);
@@ -151,45 +179,43 @@ Choice choose(const gemm_plan* plan, int64_t M, int64_t N, int64_t K, gemm_dtype
         const int64_t dp = tiles >= units ? (tiles / units) * units : 0;   // tiles of whole waves
         const int64_t rest = tiles - dp;                                      // the partial wave
         const int64_t tile_bytes = int64_t(kCfgCtas[kind]) * 128 * kCfgTileN[kind] * 4;
+        const double full_step = step_cost(kind, bmn, false);
+        const double full_item = static_cast<double>(kb) * full_step + 4.0;
+        // whole tiles only
+        if (!pinned || plan->forced_splits == 1)
+            consider(static_cast<double>((tiles + units - 1) / units) * full_item, kind, 1, tiles, false, tiles,
+                     units);
+        // split along K: the partial wave's tiles (or, pinned, every tile)
         int64_t smax = acc == GEMM_F16 ? 1 : kMaxSplits;       // fp16 accumulation is never split
         if (smax > kb) smax = kb;
-        if (rest == 0) smax = 1;
-        while (smax > 1 && (rest * smax * tile_bytes > static_cast<int64_t>(kWorkspaceBytes) ||
-                            rest * kCfgCtas[kind] > kNumCounters))
+        const int64_t dp_split = pinned ? 0 : dp;
+        const int64_t split_tiles = tiles - dp_split;
+        while (smax > 1 && (split_tiles * smax * tile_bytes > static_cast<int64_t>(kWorkspaceBytes) ||
+                            split_tiles * kCfgCtas[kind] > kNumCounters))
             --smax;
-        int64_t smin = 1;
-        if (plan->forced_kind >= 0 && plan->forced_splits > 0) {
-            if (plan->forced_splits > 1 && (plan->forced_splits > kb || acc == GEMM_F16 ||
-                                            tiles * plan->forced_splits * tile_bytes >
-                                                static_cast<int64_t>(kWorkspaceBytes) ||
-                                            tiles * kCfgCtas[kind] > kNumCounters)) {
+        int64_t smin = 2;
+        if (pinned) {
+            if (plan->forced_splits > 1 && plan->forced_splits > smax) {
                 *valid = false;
                 return best;
             }
             smin = smax = plan->forced_splits;
         }
-        const double width = static_cast<double>(loaded_cols(kind, swap ? false : b_mn_major)) *
-                             (kind == kCfgSingle256 ? 1.15 : 1.0);
-        for (int64_t s = smin; s <= smax; ++s) {
-            // a pinned split count splits every tile (dp = 0), as documented
-            const bool pinned = plan->forced_kind >= 0 && plan->forced_splits > 0;
-            const int64_t dp_s = s == 1 ? tiles : (pinned ? 0 : dp);
-            const int64_t split_tiles = tiles - dp_s;
-            const int64_t waves_dp = (dp_s + units - 1) / units;
-            const int64_t waves_split = (split_tiles * s + units - 1) / units;
-            const double reduce = s > 1 ? 2.0 + static_cast<double>(s) * kCfgTileN[kind] / 64.0 : 0.0;
-            const double cost = (static_cast<double>(waves_dp) * static_cast<double>(kb + 4) +
-                                 static_cast<double>(waves_split) *
-                                     (static_cast<double>((kb + s - 1) / s + 4) + reduce)) * width;
-            if (best_cost < 0 || cost < best_cost) {
-                best_cost = cost;
-                best.kind = kind;
-                best.splits = static_cast<int>(s);
-                best.dp_tiles = dp_s;
-                best.swap = swap;
-                best.tiles = tiles;
-                best.units = static_cast<int>(units);
+        if (split_tiles > 0) {
+            for (int64_t s = smin; s <= smax && s > 1; ++s) {
+                const double reduce = 2.0 + 2.0 * static_cast<double>(s) * kCfgTileN[kind] / 64.0;
+                const double item = static_cast<double>((kb + s - 1) / s) * full_step + 4.0 + reduce + 2.0;
+                const double cost = static_cast<double>(dp_split / units) * full_item +
+                                    static_cast<double>((split_tiles * s + units - 1) / units) * item;
+                consider(cost, kind, static_cast<int>(s), dp_split, false, tiles, units);
             }
+        }
+        // two half-width items per tile of the partial wave
+        if (kCfgHalves[kind] && rest > 0 && !pinned) {
+            const double item = static_cast<double>(kb) * step_cost(kind, bmn, true) + 4.0 + 2.0;
+            const double cost = static_cast<double>(dp / units) * full_item +
+                                static_cast<double>((2 * rest + units - 1) / units) * item;
+            consider(cost, kind, 1, dp, true, tiles, units);
         }
     }
     return best;
@@ -224,6 +250,7 @@ std::string config_name(const Choice& ch, gemm_dtype_t acc, gemm_dtype_t out) {
                     std::to_string(kCfgTileN[ch.kind]) + "_" + outs[out_slot(acc, out)];
     if (ch.swap) s += "_swapAB";
     if (ch.splits > 1) s += "_splitk" + std::to_string(ch.splits);
+    if (ch.n_halves) s += "_nhalves";
     return s;
 }
 
@@ -380,11 +407,13 @@ gemm_status_t gemm_plan_describe(gemm_plan_t plan, int64_t M, int64_t N, int64_t
     bool valid = true;
     const Choice ch = choose(plan, M, N, K, accum_dtype, layoutB == GEMM_ROW_MAJOR, &valid);
     if (!valid) return GEMM_ERR_UNSUPPORTED;
-    const int64_t work = ch.splits > 1 ? ch.dp_tiles + (ch.tiles - ch.dp_tiles) * ch.splits : ch.tiles;
+    const int64_t work = ch.n_halves      ? ch.dp_tiles + (ch.tiles - ch.dp_tiles) * 2
+                         : ch.splits > 1 ? ch.dp_tiles + (ch.tiles - ch.dp_tiles) * ch.splits
+                                         : ch.tiles;
     const int64_t units = work < ch.units ? work : ch.units;
-    std::snprintf(buf, static_cast<size_t>(len), "%s tiles=%lld split_tiles=%lld splits=%d ctas=%lld sms=%d",
+    std::snprintf(buf, static_cast<size_t>(len), "%s tiles=%lld divided_tiles=%lld splits=%d ctas=%lld sms=%d",
                   config_name(ch, accum_dtype, out_dtype).c_str(), static_cast<long long>(ch.tiles),
-                  static_cast<long long>(ch.splits > 1 ? ch.tiles - ch.dp_tiles : 0), ch.splits,
+                  static_cast<long long>((ch.splits > 1 || ch.n_halves) ? ch.tiles - ch.dp_tiles : 0), ch.splits,
                   static_cast<long long>(units * kCfgCtas[ch.kind]), plan->sm_count);
     return GEMM_OK;
 }
@@ -526,6 +555,7 @@ extern "C" gemm_status_t gemm_run_static_scratch(int device, gemm_dtype_t in_dty
     const int64_t kb = (K + 63) / 64;
     if (splits > kb || (accum_dtype == GEMM_F16 && splits > 1)) return GEMM_ERR_UNSUPPORTED;
     ch.splits = splits;
+    ch.n_halves = false;
     ch.dp_tiles = 0;   // every tile is split `splits` ways
     // the size limit: split partials and counters must fit the fixed array
     if (splits > 1) {

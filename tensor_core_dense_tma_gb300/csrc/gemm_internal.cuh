@@ -58,6 +58,9 @@ enum ConfigId : int {
 constexpr int kCfgTileM[kNumCfgKinds] = {128, 128, 128, 256, 256};
 constexpr int kCfgTileN[kNumCfgKinds] = {16, 64, 256, 256, 224};
 constexpr int kCfgCtas[kNumCfgKinds] = {1, 1, 1, 2, 2};
+// configurations whose tiles can run as two half-width items (BN/2 a
+// multiple of 32: whole epilogue chunks)
+constexpr bool kCfgHalves[kNumCfgKinds] = {false, true, true, true, false};
 
 inline int out_slot(gemm_dtype_t acc, gemm_dtype_t out) {
     if (acc == GEMM_F16) return 3;
@@ -98,7 +101,8 @@ struct Problem {
 struct Choice {
     int kind = kCfgPair256;
     int splits = 1;
-    int64_t dp_tiles = 0;      // whole tiles before the split ones (see KernelParams)
+    int64_t dp_tiles = 0;      // whole tiles before the divided ones (see KernelParams)
+    bool n_halves = false;     // divided tiles run as two half-width items (splits == 1)
     bool swap = false;
     int64_t tiles = 0;
     int units = 0;
@@ -212,9 +216,16 @@ gemm_status_t launch_tc(gemm_plan* plan, const Choice& ch, const Problem& pr, co
     const int64_t out_esz = out_dtype == GEMM_F32 ? 4 : 2;
     const bool d_tma = Cfg::W == 32 && !pr.swap && (reinterpret_cast<uintptr_t>(D) % 16) == 0 &&
                        (ldc * out_esz) % 16 == 0;
-    CUtensorMap tmD, tmW;
+    CUtensorMap tmBh, tmD, tmW;
+    std::memset(&tmBh, 0, sizeof(tmBh));
     std::memset(&tmD, 0, sizeof(tmD));
     std::memset(&tmW, 0, sizeof(tmW));
+    const bool n_halves = ch.n_halves && Cfg::HALVES_OK && ch.splits == 1;
+    if (n_halves && !b_mn) {
+        // K-major B of a half-width item: half as many rows per CTA
+        st = encode_map(plan, &tmBh, pr.B, pr.K, pr.N, pr.ldb, 64, Cfg::BN_CTA_HALF, in_dt);
+        if (st != GEMM_OK) return st;
+    }
     if (d_tma) {
         st = encode_map(plan, &tmD, D, pr.N, pr.M, ldc, 32, 32, out_dtype,
                         out_esz == 4 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
@@ -236,7 +247,8 @@ gemm_status_t launch_tc(gemm_plan* plan, const Choice& ch, const Problem& pr, co
     p.num_k_blocks = static_cast<int32_t>((pr.K + Cfg::BK - 1) / Cfg::BK);
     p.num_tiles = p.num_m_blocks * p.num_n_blocks;
     p.splits = ch.splits;
-    p.dp_tiles = static_cast<int32_t>(ch.splits > 1 ? ch.dp_tiles : p.num_tiles);
+    p.n_halves = n_halves ? 1 : 0;
+    p.dp_tiles = static_cast<int32_t>((ch.splits > 1 || n_halves) ? ch.dp_tiles : p.num_tiles);
     p.group_m = 8;
     p.ldc = ldc;
     p.C = C;
@@ -244,6 +256,7 @@ gemm_status_t launch_tc(gemm_plan* plan, const Choice& ch, const Problem& pr, co
     p.alpha = alpha;
     p.beta = beta;
     p.idesc = make_idesc(!Cfg::ACC_F16, plan->in_dtype == GEMM_BF16, a_mn, b_mn, Cfg::UMMA_M, Cfg::BN);
+    p.idesc_half = make_idesc(!Cfg::ACC_F16, plan->in_dtype == GEMM_BF16, a_mn, b_mn, Cfg::UMMA_M, Cfg::BN / 2);
     p.a_mn_major = a_mn;
     p.b_mn_major = b_mn;
     p.trans_out = pr.swap ? 1u : 0u;
@@ -256,10 +269,10 @@ gemm_status_t launch_tc(gemm_plan* plan, const Choice& ch, const Problem& pr, co
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[1];
     fill_launch_config<Cfg>(cfg, attr, stream);
-    const int64_t work = p.dp_tiles + static_cast<int64_t>(p.num_tiles - p.dp_tiles) * p.splits;
+    const int64_t work = p.dp_tiles + static_cast<int64_t>(p.num_tiles - p.dp_tiles) * (n_halves ? 2 : p.splits);
     const int units = work < ch.units ? static_cast<int>(work) : ch.units;
     cfg.gridDim = dim3(Cfg::CG * units, 1, 1);
-    if (cudaLaunchKernelEx(&cfg, tcdt::gemm_sm103_kernel<Cfg>, tmA, tmB, tmD, tmW, p) != cudaSuccess) {
+    if (cudaLaunchKernelEx(&cfg, tcdt::gemm_sm103_kernel<Cfg>, tmA, tmB, tmBh, tmD, tmW, p) != cudaSuccess) {
         cudaGetLastError();
         return GEMM_ERR_CUDA;
     }

@@ -63,13 +63,15 @@ struct KernelParams {
     int32_t M, N, K;          // of the product the kernel computes (swapped when trans_out)
     int32_t num_m_blocks, num_n_blocks, num_k_blocks, num_tiles;
     int32_t dp_tiles;         // tiles [0, dp_tiles) are whole work items ...
-    int32_t splits;           // ... the rest are split into this many K ranges
+    int32_t splits;           // ... the rest are split into this many K ranges, or
+    int32_t n_halves;         // (1) each run as two half-width items (columns [0, BN/2), [BN/2, BN))
     int32_t group_m;          // m-blocks per raster group
     int64_t ldc;
     const void* C;            // may alias D; unread when beta == 0
     void* D;
     float alpha, beta;
     uint32_t idesc;           // tcgen05 instruction descriptor
+    uint32_t idesc_half;      // the same with N = BN/2 (half-width items)
     uint32_t a_mn_major;      // 1: A is M-contiguous
     uint32_t b_mn_major;      // 1: B is N-contiguous
     uint32_t trans_out;       // 1: element (r, c) goes to D[c*ldc + r]
@@ -99,6 +101,10 @@ struct TileConfig {
     static constexpr int W = BN < 32 ? BN : 32;    // accumulator columns per tcgen05.ld
     static constexpr uint32_t MN_CHUNK_BYTES = 64 * BK * 2;    // 64 MN-elements x BK rows
     static constexpr int B_CHUNKS = (BN_CTA + 63) / 64;        // MN-major B: 64-column TMA boxes
+    static constexpr int BN_CTA_HALF = BN_CTA / 2;             // B columns per CTA of a half-width item
+    static constexpr int B_CHUNKS_HALF = (BN_CTA_HALF + 63) / 64;
+    // half-width items need whole 32-column epilogue chunks and whole 8-row atoms
+    static constexpr bool HALVES_OK = (BN / 2) % 32 == 0 && BN_CTA_HALF % 8 == 0;
     static constexpr int A_BYTES = BM * BK * 2;
     static constexpr int B_BYTES = B_CHUNKS * 64 * BK * 2;     // room for whole MN-major chunks
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
@@ -142,24 +148,27 @@ __host__ __device__ constexpr int largest_divisor_upto(int n, int cap) {
     return best;
 }
 
-// Work items: first the dp_tiles whole tiles, then the remaining tiles each
-// split into `splits` contiguous K ranges.  The splits of a tile are
-// consecutive items, so they run at the same time on neighbouring units;
-// a split covers k-blocks [kb0, kb1), never empty (splits <= k-blocks).
-// With dp_tiles = (whole waves of tiles) only the last, partial wave is
-// split, so its tiles spread over all units instead of leaving most idle.
+// Work items: first the dp_tiles whole tiles, then the remaining tiles, each
+// either split into `splits` contiguous K ranges or (n_halves) run as two
+// half-width items.  The pieces of a tile are consecutive items, so they run
+// at the same time on neighbouring units; a split covers k-blocks
+// [kb0, kb1), never empty (splits <= k-blocks).  With dp_tiles = (whole
+// waves of tiles) only the last, partial wave is divided, so its work
+// spreads over all units instead of leaving most of them idle.
 struct WorkItem {
     int tile;      // output tile
-    int stile;     // index among the split tiles (-1: a whole tile)
+    int stile;     // index among the divided tiles (-1: a whole tile)
     int split, nsplit, kb0, kb1;
+    int half;      // -1: full width; 0 / 1: column half of the tile
 };
 
 __device__ __forceinline__ int num_work_items(const KernelParams& p) {
-    return p.dp_tiles + (p.num_tiles - p.dp_tiles) * p.splits;
+    return p.dp_tiles + (p.num_tiles - p.dp_tiles) * (p.n_halves ? 2 : p.splits);
 }
 
 __device__ __forceinline__ WorkItem work_item(const KernelParams& p, int w) {
     WorkItem x;
+    x.half = -1;
     if (w < p.dp_tiles) {
         x.tile = w;
         x.stile = -1;
@@ -170,6 +179,16 @@ __device__ __forceinline__ WorkItem work_item(const KernelParams& p, int w) {
         return x;
     }
     const int t = w - p.dp_tiles;
+    if (p.n_halves) {
+        x.stile = t >> 1;
+        x.tile = p.dp_tiles + x.stile;
+        x.half = t & 1;
+        x.split = 0;
+        x.nsplit = 1;
+        x.kb0 = 0;
+        x.kb1 = p.num_k_blocks;
+        return x;
+    }
     x.stile = t / p.splits;
     x.tile = p.dp_tiles + x.stile;
     x.split = t - x.stile * p.splits;
@@ -532,8 +551,8 @@ __device__ __forceinline__ void stage_and_store_f32(const void* tmap, const uint
 template <class Cfg>
 __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
 gemm_sm103_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                  const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmW,
-                  const KernelParams p) {
+                  const __grid_constant__ CUtensorMap tmBh, const __grid_constant__ CUtensorMap tmD,
+                  const __grid_constant__ CUtensorMap tmW, const KernelParams p) {
     constexpr int CG = Cfg::CG;
     constexpr int W = Cfg::W;
     extern __shared__ uint8_t smem_raw[];
@@ -581,6 +600,7 @@ gemm_sm103_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         tma_prefetch_desc(&tmB);
     }
     if (warp == 2 && lane == 0) {
+        if (p.n_halves && !p.b_mn_major) tma_prefetch_desc(&tmBh);
         if (p.d_tma) tma_prefetch_desc(&tmD);
         if (p.splits > 1) tma_prefetch_desc(&tmW);
     }
@@ -604,15 +624,22 @@ gemm_sm103_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             uint32_t phase = 0;
             int64_t issued = 0;
             bool ok = true;
-            const uint32_t b_tx = p.b_mn_major ? static_cast<uint32_t>(Cfg::B_BYTES)
-                                               : static_cast<uint32_t>(Cfg::BN_CTA * Cfg::BK * 2);
-            const uint32_t stage_tx = CG * (Cfg::A_BYTES + b_tx);
+            const uint32_t b_tx_full = p.b_mn_major ? static_cast<uint32_t>(Cfg::B_BYTES)
+                                                    : static_cast<uint32_t>(Cfg::BN_CTA * Cfg::BK * 2);
+            const uint32_t b_tx_half = p.b_mn_major ? static_cast<uint32_t>(Cfg::B_CHUNKS_HALF * 64 * Cfg::BK * 2)
+                                                    : static_cast<uint32_t>(Cfg::BN_CTA_HALF * Cfg::BK * 2);
             for (int w = unit; ok && w < num_work; w += num_units) {
                 const WorkItem x = work_item(p, w);
                 int mb, nb;
                 tile_coords(p, x.tile, mb, nb);
+                const bool half = Cfg::HALVES_OK && x.half >= 0;
+                const uint32_t stage_tx = CG * (Cfg::A_BYTES + (half ? b_tx_half : b_tx_full));
+                const int b_chunks = half ? Cfg::B_CHUNKS_HALF : Cfg::B_CHUNKS;
+                const void* tmb = half && !p.b_mn_major ? static_cast<const void*>(&tmBh)
+                                                        : static_cast<const void*>(&tmB);
                 const int m0 = mb * Cfg::UMMA_M + Cfg::BM * static_cast<int>(rank);
-                const int n0 = nb * Cfg::BN + Cfg::BN_CTA * static_cast<int>(rank);
+                const int n0 = half ? nb * Cfg::BN + x.half * (Cfg::BN / 2) + Cfg::BN_CTA_HALF * static_cast<int>(rank)
+                                    : nb * Cfg::BN + Cfg::BN_CTA * static_cast<int>(rank);
                 for (int kb = x.kb0; kb < x.kb1; ++kb) {
                     if (!wait_phase(empty_bar(stage), phase ^ 1u, wctx, kSiteProducerEmpty)) {
                         ok = false;
@@ -632,11 +659,11 @@ gemm_sm103_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                             tma_load_2d(sa, &tmA, fb_local, k0, m0);
                         }
                         if (p.b_mn_major) {
-#pragma unroll
-                            for (int c = 0; c < Cfg::B_CHUNKS; ++c)
+#pragma unroll 1
+                            for (int c = 0; c < b_chunks; ++c)
                                 tma_load_2d(sb + c * Cfg::MN_CHUNK_BYTES, &tmB, fb_local, n0 + 64 * c, k0);
                         } else {
-                            tma_load_2d(sb, &tmB, fb_local, k0, n0);
+                            tma_load_2d(sb, tmb, fb_local, k0, n0);
                         }
                     } else {
                         const uint32_t fb = map_to_cta(fb_local, 0);   // the leader's barrier
@@ -648,11 +675,11 @@ gemm_sm103_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                             tma_load_2d_pair(sa, &tmA, fb, k0, m0);
                         }
                         if (p.b_mn_major) {
-#pragma unroll
-                            for (int c = 0; c < Cfg::B_CHUNKS; ++c)
+#pragma unroll 1
+                            for (int c = 0; c < b_chunks; ++c)
                                 tma_load_2d_pair(sb + c * Cfg::MN_CHUNK_BYTES, &tmB, fb, n0 + 64 * c, k0);
                         } else {
-                            tma_load_2d_pair(sb, &tmB, fb, k0, n0);
+                            tma_load_2d_pair(sb, tmb, fb, k0, n0);
                         }
                     }
                     ++issued;
@@ -705,6 +732,7 @@ gemm_sm103_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 }
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + buf * Cfg::ACC_COLS;
+                const uint32_t idesc = (Cfg::HALVES_OK && x.half >= 0) ? p.idesc_half : p.idesc;
                 for (int kb = x.kb0; kb < x.kb1; ++kb) {
                     if (!wait_phase(full_bar(stage), phase, wctx, kSiteMmaFull)) {
                         ok = false;
@@ -717,7 +745,7 @@ gemm_sm103_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                     for (int k = 0; k < Cfg::BK / Cfg::UMMA_K; ++k) {
                         const uint64_t adesc = smem_desc_sw128(sa + k * a_kstep, a_lbo, 1024u);
                         const uint64_t bdesc = smem_desc_sw128(sb + k * b_kstep, b_lbo, 1024u);
-                        umma_f16_ss<CG>(d_tmem, adesc, bdesc, p.idesc, (kb != x.kb0 || k != 0) ? 1u : 0u);
+                        umma_f16_ss<CG>(d_tmem, adesc, bdesc, idesc, (kb != x.kb0 || k != 0) ? 1u : 0u);
                     }
                     umma_commit<CG>(empty_bar(stage), kPair);   // stage reusable once these MMAs finish
                     if (++stage == Cfg::STAGES) {
@@ -755,10 +783,12 @@ gemm_sm103_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             int mb, nb;
             tile_coords(p, x.tile, mb, nb);
             const int m0 = mb * Cfg::UMMA_M + Cfg::BM * static_cast<int>(rank);
-            const int n0 = nb * Cfg::BN;
+            const bool half = Cfg::HALVES_OK && x.half >= 0;
+            const int n0 = nb * Cfg::BN + (half ? x.half * (Cfg::BN / 2) : 0);
+            const int nchunks = (half ? Cfg::BN / 2 : Cfg::BN) / W;
             // warm L2 with this thread's C row while the main loop runs
             if (p.beta != 0.0f && !p.trans_out && m0 + row_local < p.M)
-                prefetch_c_row<Cfg>(p, m0 + row_local, n0, Cfg::BN);
+                prefetch_c_row<Cfg>(p, m0 + row_local, n0, nchunks * W);
             if (threadIdx.x == 64)
                 epi_ok_flag[iter & 1] = wait_phase(accf_bar(buf), acc_phase, wctx, kSiteEpilogueAccFull) ? 1 : 0;
             named_bar_sync(1, 32 * Cfg::NUM_EPI_WARPS);
@@ -775,7 +805,7 @@ gemm_sm103_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                         staged = true;
                         const int row0w = m0 + 32 * quad;
 #pragma unroll 1
-                        for (int c = 0; c < Cfg::BN / W; ++c) {
+                        for (int c = 0; c < nchunks; ++c) {
                             const int col0 = n0 + W * c;
                             if (col0 >= p.N) break;   // warp-uniform
                             __syncwarp();
@@ -792,7 +822,7 @@ gemm_sm103_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 }
                 if (!staged) {
 #pragma unroll 1
-                    for (int c = 0; c < Cfg::BN / W; ++c) {
+                    for (int c = 0; c < nchunks; ++c) {
                         const int col0 = n0 + W * c;
                         if (col0 >= p.N) break;   // warp-uniform
                         __syncwarp();             // tcgen05.ld is .sync.aligned: converge the warp

@@ -153,16 +153,21 @@ def test_pinned_config_that_does_not_fit(plans):
         plan.force_config("auto")
 
 
-@pytest.mark.parametrize("shape", [(4096, 4096, 1024), (2560, 2560, 2048)], ids=lambda s: "x".join(map(str, s)))
-def test_partial_wave_split(plans, shape):
-    """Whole waves of tiles unsplit, the tiles of the last partial wave split
-    along K: sampled entries bit-exact on the integer twin."""
+@pytest.mark.parametrize("shape", [(4096, 4096, 1024), (2560, 2560, 2048), (3000, 3496, 1504)],
+                         ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("layouts", LAYOUTS, ids=lambda l: "".join(x[0] for x in l))
+@pytest.mark.parametrize("out", ["f32", "bf16"])
+def test_partial_wave_divided(plans, shape, layouts, out):
+    """Whole waves of tiles run whole; the tiles of the last, partial wave are
+    divided (split along K, or run as two half-width items, whichever the plan
+    picks): sampled entries bit-exact on the integer twin."""
     from gpu_util import check_sampled
-    w = W(*shape)
+    w = W(*shape, *layouts, out=out, alpha=0.5, beta=1.0)
     plan = plans["f16"]
-    desc = plan.describe(w.M, w.N, w.K)
+    desc = plan.describe(w.M, w.N, w.K, w.layoutA, w.layoutB, "f32", out)
+    if w.layoutB == "row":
+        assert "divided_tiles=0" not in desc, desc
     h = wl.make_inputs(w, integer=True)
     D = run_gpu(plan, w, h)
     torch.cuda.synchronize()
     check_sampled(w, h, D, integer=True, n_random=4096)
-    return desc
