@@ -380,6 +380,78 @@ __device__ __forceinline__ void row_segment_dispatch(char* base, float (&v)[W], 
     }
 }
 
+// A warp's 32 x 32 block of C (rows row0.., columns col0..), read row by row
+// with the lanes on consecutive columns (each load instruction of the warp
+// covers one contiguous row segment), then transposed through a 4 KB
+// shared-memory buffer so that lane r ends up with row row0 + r.  Words are
+// stored at (row, col ^ row): conflict-free in both directions.  Elements
+// outside C read as 0.
+template <int OUT>
+__device__ __forceinline__ void load_c_block(const KernelParams& p, int row0, int col0, int lane, uint32_t buf,
+                                             float (&c)[32]) {
+    const int col = col0 + lane;
+    const bool col_ok = col < p.N;
+    {
+        float t[32];
+#pragma unroll
+        for (int r = 0; r < 32; ++r) {
+            const int row = row0 + r;
+            t[r] = (col_ok && row < p.M) ? load_elem<OUT>(p.C, static_cast<int64_t>(row) * p.ldc + col) : 0.0f;
+        }
+#pragma unroll
+        for (int r = 0; r < 32; ++r)
+            st_shared_f32(buf + 4u * static_cast<uint32_t>(r * 32 + (lane ^ r)), t[r]);
+    }
+    __syncwarp();
+#pragma unroll
+    for (int j = 0; j < 32; ++j) c[j] = ld_shared_f32(buf + 4u * static_cast<uint32_t>(lane * 32 + (j ^ lane)));
+    __syncwarp();
+}
+
+// Asynchronous form for fp32 C: this lane copies column col0 + lane of the
+// 32 rows into the buffer (word (row, col ^ row)), zero outside C, and
+// commits the copies as one group; read the block with read_c_block after
+// waiting for the group.
+__device__ __forceinline__ void issue_c_block_f32(const KernelParams& p, int row0, int col0, int lane, uint32_t buf) {
+    const int col = col0 + lane;
+    const bool col_ok = col < p.N;
+    const float* C = static_cast<const float*>(p.C);
+#pragma unroll
+    for (int r = 0; r < 32; ++r) {
+        const int row = row0 + r;
+        const bool ok = col_ok && row < p.M;
+        const float* src = ok ? C + static_cast<int64_t>(row) * p.ldc + col : C;
+        cp_async_4(buf + 4u * static_cast<uint32_t>(r * 32 + (lane ^ r)), src, ok ? 4u : 0u);
+    }
+    cp_async_commit();
+}
+
+// Row row0 + lane of a block written by load/issue_c_block.
+__device__ __forceinline__ void read_c_block(int lane, uint32_t buf, float (&c)[32]) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) c[j] = ld_shared_f32(buf + 4u * static_cast<uint32_t>(lane * 32 + (j ^ lane)));
+}
+
+// The reverse: lane r holds row row0 + r of a 32 x 32 block of D; transpose
+// through the buffer and store row by row with the lanes on consecutive
+// columns.  Elements outside D are not written.
+template <int OUT>
+__device__ __forceinline__ void store_d_block(const KernelParams& p, int row0, int col0, int lane, uint32_t buf,
+                                              const float (&v)[32]) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) st_shared_f32(buf + 4u * static_cast<uint32_t>(lane * 32 + (j ^ lane)), v[j]);
+    __syncwarp();
+    const int col = col0 + lane;
+    const bool col_ok = col < p.N;
+#pragma unroll
+    for (int r = 0; r < 32; ++r) {
+        const float x = ld_shared_f32(buf + 4u * static_cast<uint32_t>(r * 32 + (lane ^ r)));
+        const int row = row0 + r;
+        if (col_ok && row < p.M) store_elem<OUT>(p.D, static_cast<int64_t>(row) * p.ldc + col, x);
+    }
+    __syncwarp();
+}
+
 // alpha * acc (+ beta * C) for W consecutive accumulator columns of one
 // accumulator row, written to D (row-major, or transposed with trans_out).
 template <class Cfg>
@@ -515,14 +587,17 @@ __device__ __forceinline__ void stage_and_store(const KernelParams& p, const voi
     for (int i = 0; i < 32; ++i) acc[i] = v[i];
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] = p.alpha * acc[i];
-    if (p.beta != 0.0f && row_ok) {
-        const int n = min(32, p.N - col0);
+    if (p.beta != 0.0f) {
+        // coalesced read of this warp's C block through the staging buffer the
+        // segment will use (once its previous TMA store has read it)
+        const uint32_t buf = stg + static_cast<uint32_t>(sbuf) * 4096u;
+        if (lane == 0) bulk_wait_group_read<1>();
+        __syncwarp();
         float c[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) c[i] = 0.0f;
-        const int64_t off = static_cast<int64_t>(row) * p.ldc + col0;
-        row_segment_dispatch<Cfg::OUT, 32, false>(
-            const_cast<char*>(static_cast<const char*>(p.C)) + off * ESZ, c, n);
+        load_c_block<Cfg::OUT>(p, row0w, col0, lane, buf, c);
+        (void)row_ok;
+        (void)ESZ;
+        (void)row;
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] = fmaf(p.alpha, acc[i], p.beta * c[i]);
     }
@@ -800,7 +875,7 @@ gemm_sm103_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             if (x.nsplit == 1) {
                 bool staged = false;
                 if constexpr (W == 32) {
-                    if (p.d_tma) {
+                    if (p.d_tma && (p.beta == 0.0f || Cfg::OUT != kOutF32)) {
                         // staged through shared memory, one TMA store per 32 x 32 segment
                         staged = true;
                         const int row0w = m0 + 32 * quad;
@@ -817,6 +892,53 @@ gemm_sm103_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
 #pragma unroll
                             for (int i = 0; i < W; ++i) v[i] = acc_value<Cfg::ACC_F16>(r[i]);
                             stage_and_store<Cfg>(p, &tmD, v, row, col0, row0w, lane, stg, sbuf, row_ok);
+                        }
+                    }
+                }
+                if constexpr (W == 32) {
+                    if (!staged && !p.trans_out) {
+                        // D rows not 16-byte aligned (or an fp32 C to add): coalesced
+                        // loads of C and stores of D, each block transposed through one
+                        // of this warp's two staging buffers; an fp32 C block is copied
+                        // asynchronously one chunk ahead
+                        staged = true;
+                        const int row0w = m0 + 32 * quad;
+#pragma unroll 1
+                        for (int c = 0; c < nchunks; ++c) {
+                            const int col0 = n0 + W * c;
+                            if (col0 >= p.N) break;   // warp-uniform
+                            __syncwarp();
+                            uint32_t r[W];
+                            tmem_ld_row<W>(t_row + W * c, r);
+                            tmem_ld_wait();
+                            if (row0w >= p.M) continue;   // warp-uniform
+                            float v[W];
+#pragma unroll
+                            for (int i = 0; i < W; ++i) v[i] = p.alpha * acc_value<Cfg::ACC_F16>(r[i]);
+                            const uint32_t cur = stg + static_cast<uint32_t>(c & 1) * 4096u;
+                            if (p.beta != 0.0f) {
+                                float cv[W];
+                                if constexpr (Cfg::OUT == kOutF32) {
+                                    // C of this chunk was copied during the previous one; start
+                                    // the next chunk's copy into the other buffer
+                                    if (c == 0) issue_c_block_f32(p, row0w, col0, lane, cur);
+                                    const bool next = c + 1 < nchunks && col0 + W < p.N;
+                                    if (next)
+                                        issue_c_block_f32(p, row0w, col0 + W, lane,
+                                                          stg + static_cast<uint32_t>((c + 1) & 1) * 4096u);
+                                    if (next) cp_async_wait<1>();
+                                    else cp_async_wait<0>();
+                                    __syncwarp();
+                                    read_c_block(lane, cur, cv);
+                                    __syncwarp();
+                                } else {
+                                    load_c_block<Cfg::OUT>(p, row0w, col0, lane, cur, cv);
+                                }
+#pragma unroll
+                                for (int i = 0; i < W; ++i)
+                                    v[i] = fmaf(p.alpha, acc_value<Cfg::ACC_F16>(r[i]), p.beta * cv[i]);
+                            }
+                            store_d_block<Cfg::OUT>(p, row0w, col0, lane, cur, v);
                         }
                     }
                 }
