@@ -55,8 +55,9 @@ def up_to_date(out: str = LIB_PATH) -> bool:
 
 def build(force: bool = False, extra_flags: list[str] | None = None, out: str = LIB_PATH,
           verbose: bool = False) -> str:
-    """Build the library if any source is newer than it; return its path."""
-    if not force and not extra_flags and up_to_date(out):
+    """Build the library (at `out`, with optional extra nvcc flags) if any
+    source is newer than it; return its path."""
+    if not force and up_to_date(out):
         return out
     os.makedirs(os.path.dirname(out), exist_ok=True)
     nvcc = nvcc_path()

@@ -383,6 +383,16 @@ gemm_status_t gemm_plan_force_config(gemm_plan_t plan, gemm_config_t config, int
     return GEMM_OK;
 }
 
+#ifdef TCDT_FAULT_INJECTION
+// Test builds only (not part of the product library or of include/gemm.h):
+// make the producer of every CTA skip its `index`-th TMA issue (-1: none).
+gemm_status_t gemm_test_inject_skip_load(gemm_plan_t plan, int64_t index) {
+    if (!plan) return GEMM_ERR_INVALID_ARG;
+    plan->fi_skip_load = index;
+    return GEMM_OK;
+}
+#endif
+
 uint64_t gemm_plan_launch_count(gemm_plan_t plan) { return plan ? plan->launches : 0; }
 
 int gemm_plan_sm_count(gemm_plan_t plan) { return plan ? plan->sm_count : 0; }

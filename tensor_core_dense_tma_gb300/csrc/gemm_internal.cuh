@@ -83,6 +83,9 @@ struct gemm_plan {
     int units[tcdt_host::kNumCfgKinds] = {};  // co-resident CTAs (single) or CTA pairs (pair)
     size_t ws_bytes = 0;          // capacity of d_ws
     int forced_kind = -1;         // gemm_plan_force_config
+#ifdef TCDT_FAULT_INJECTION
+    int64_t fi_skip_load = -1;    // test builds only
+#endif
     int forced_splits = 0;
 };
 
@@ -265,6 +268,9 @@ gemm_status_t launch_tc(gemm_plan* plan, const Choice& ch, const Problem& pr, co
     p.counters = plan->d_counters;
     p.status = plan->d_status;
     p.timeout_ns = plan->timeout_ns;
+#ifdef TCDT_FAULT_INJECTION
+    p.fi_skip_load = plan->fi_skip_load;
+#endif
 
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[1];

@@ -80,6 +80,9 @@ struct KernelParams {
     int* counters;            // [split tile][cta] split arrivals; zero on entry, left zero
     int* status;              // [0] status code, [1] site
     uint64_t timeout_ns;
+#ifdef TCDT_FAULT_INJECTION
+    int64_t fi_skip_load;     // test builds only: this producer issue (counted per CTA) loads nothing
+#endif
 };
 
 // One output tile is UMMA_M x BN (UMMA_M = 128 * CG).  With CG == 2 a
@@ -725,7 +728,14 @@ gemm_sm103_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                     const uint32_t fb_local = full_bar(stage);
                     const int k0 = kb * Cfg::BK;
                     if (leader) mbar_arrive_expect_tx(fb_local, stage_tx);
-                    if constexpr (CG == 1) {
+#ifdef TCDT_FAULT_INJECTION
+                    // the barrier expects bytes that never come: a wait downstream must run out
+                    const bool skip = issued == p.fi_skip_load;
+#else
+                    constexpr bool skip = false;
+#endif
+                    if (skip) {
+                    } else if constexpr (CG == 1) {
                         if (p.a_mn_major) {
 #pragma unroll
                             for (int c = 0; c < Cfg::BM / 64; ++c)
