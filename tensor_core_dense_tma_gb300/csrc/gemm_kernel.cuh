@@ -229,6 +229,13 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, const 
     }
 }
 
+// wait_phase by every lane of a warp; true only if it succeeded in all of
+// them, so the warp takes the same branch afterwards.
+template <bool kClusterScope = false>
+__device__ __forceinline__ bool warp_wait_phase(uint32_t bar, uint32_t parity, const WaitCtx& w, int site) {
+    return __all_sync(0xffffffffu, wait_phase<kClusterScope>(bar, parity, w, site));
+}
+
 // Bounded wait used only while winding down after an abort.
 __device__ __forceinline__ void wait_phase_drain(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
     const uint64_t t0 = globaltimer_ns();
@@ -695,9 +702,10 @@ gemm_sm103_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
 
     if (warp == 0) {
         // ------------------------------------------------------------------
-        // TMA producer (one thread per CTA)
+        // TMA producer: the whole warp runs the loop in step and one elected
+        // lane issues the copies of each stage
         // ------------------------------------------------------------------
-        if (lane == 0) {
+        {
             int stage = 0;
             uint32_t phase = 0;
             int64_t issued = 0;
@@ -719,7 +727,7 @@ gemm_sm103_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 const int n0 = half ? nb * Cfg::BN + x.half * (Cfg::BN / 2) + Cfg::BN_CTA_HALF * static_cast<int>(rank)
                                     : nb * Cfg::BN + Cfg::BN_CTA * static_cast<int>(rank);
                 for (int kb = x.kb0; kb < x.kb1; ++kb) {
-                    if (!wait_phase(empty_bar(stage), phase ^ 1u, wctx, kSiteProducerEmpty)) {
+                    if (!warp_wait_phase(empty_bar(stage), phase ^ 1u, wctx, kSiteProducerEmpty)) {
                         ok = false;
                         break;
                     }
@@ -727,46 +735,49 @@ gemm_sm103_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                     const uint32_t sb = sa + Cfg::A_BYTES;
                     const uint32_t fb_local = full_bar(stage);
                     const int k0 = kb * Cfg::BK;
-                    if (leader) mbar_arrive_expect_tx(fb_local, stage_tx);
 #ifdef TCDT_FAULT_INJECTION
                     // the barrier expects bytes that never come: a wait downstream must run out
                     const bool skip = issued == p.fi_skip_load;
 #else
                     constexpr bool skip = false;
 #endif
-                    if (skip) {
-                    } else if constexpr (CG == 1) {
-                        if (p.a_mn_major) {
+                    if (elect_one_sync()) {
+                        if (leader) mbar_arrive_expect_tx(fb_local, stage_tx);
+                        if (skip) {
+                        } else if constexpr (CG == 1) {
+                            if (p.a_mn_major) {
 #pragma unroll
-                            for (int c = 0; c < Cfg::BM / 64; ++c)
-                                tma_load_2d(sa + c * Cfg::MN_CHUNK_BYTES, &tmA, fb_local, m0 + 64 * c, k0);
-                        } else {
-                            tma_load_2d(sa, &tmA, fb_local, k0, m0);
-                        }
-                        if (p.b_mn_major) {
+                                for (int c = 0; c < Cfg::BM / 64; ++c)
+                                    tma_load_2d(sa + c * Cfg::MN_CHUNK_BYTES, &tmA, fb_local, m0 + 64 * c, k0);
+                            } else {
+                                tma_load_2d(sa, &tmA, fb_local, k0, m0);
+                            }
+                            if (p.b_mn_major) {
 #pragma unroll 1
-                            for (int c = 0; c < b_chunks; ++c)
-                                tma_load_2d(sb + c * Cfg::MN_CHUNK_BYTES, &tmB, fb_local, n0 + 64 * c, k0);
+                                for (int c = 0; c < b_chunks; ++c)
+                                    tma_load_2d(sb + c * Cfg::MN_CHUNK_BYTES, &tmB, fb_local, n0 + 64 * c, k0);
+                            } else {
+                                tma_load_2d(sb, tmb, fb_local, k0, n0);
+                            }
                         } else {
-                            tma_load_2d(sb, tmb, fb_local, k0, n0);
-                        }
-                    } else {
-                        const uint32_t fb = map_to_cta(fb_local, 0);   // the leader's barrier
-                        if (p.a_mn_major) {
+                            const uint32_t fb = map_to_cta(fb_local, 0);   // the leader's barrier
+                            if (p.a_mn_major) {
 #pragma unroll
-                            for (int c = 0; c < Cfg::BM / 64; ++c)
-                                tma_load_2d_pair(sa + c * Cfg::MN_CHUNK_BYTES, &tmA, fb, m0 + 64 * c, k0);
-                        } else {
-                            tma_load_2d_pair(sa, &tmA, fb, k0, m0);
-                        }
-                        if (p.b_mn_major) {
+                                for (int c = 0; c < Cfg::BM / 64; ++c)
+                                    tma_load_2d_pair(sa + c * Cfg::MN_CHUNK_BYTES, &tmA, fb, m0 + 64 * c, k0);
+                            } else {
+                                tma_load_2d_pair(sa, &tmA, fb, k0, m0);
+                            }
+                            if (p.b_mn_major) {
 #pragma unroll 1
-                            for (int c = 0; c < b_chunks; ++c)
-                                tma_load_2d_pair(sb + c * Cfg::MN_CHUNK_BYTES, &tmB, fb, n0 + 64 * c, k0);
-                        } else {
-                            tma_load_2d_pair(sb, tmb, fb, k0, n0);
+                                for (int c = 0; c < b_chunks; ++c)
+                                    tma_load_2d_pair(sb + c * Cfg::MN_CHUNK_BYTES, &tmB, fb, n0 + 64 * c, k0);
+                            } else {
+                                tma_load_2d_pair(sb, tmb, fb, k0, n0);
+                            }
                         }
                     }
+                    __syncwarp();
                     ++issued;
                     if (++stage == Cfg::STAGES) {
                         stage = 0;
@@ -789,9 +800,13 @@ gemm_sm103_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------------
-        // MMA issuer: one thread of the leader CTA
+        // MMA issuer: warp 1 of the leader CTA runs the loop in step and one
+        // elected lane issues each K block's MMAs and commits.  Kept
+        // warp-uniform, the loop issues a 256-wide tcgen05.mma every 128
+        // cycles (its execution time); issued from a one-lane branch, each
+        // one took about 1.6 times as long.
         // ------------------------------------------------------------------
-        if (lane == 0 && leader) {
+        if (leader) {
             int stage = 0;
             uint32_t phase = 0;
             int buf = 0;
@@ -809,8 +824,8 @@ gemm_sm103_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             for (int w = unit; ok && w < num_work; w += num_units) {
                 const WorkItem x = work_item(p, w);
                 bool got;
-                if constexpr (CG == 1) got = wait_phase(acce_bar(buf), acc_phase ^ 1u, wctx, kSiteMmaAccEmpty);
-                else got = wait_phase<true>(acce_bar(buf), acc_phase ^ 1u, wctx, kSiteMmaAccEmpty);
+                if constexpr (CG == 1) got = warp_wait_phase(acce_bar(buf), acc_phase ^ 1u, wctx, kSiteMmaAccEmpty);
+                else got = warp_wait_phase<true>(acce_bar(buf), acc_phase ^ 1u, wctx, kSiteMmaAccEmpty);
                 if (!got) {
                     ok = false;
                     break;
@@ -819,34 +834,46 @@ gemm_sm103_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 const uint32_t d_tmem = tmem_base + buf * Cfg::ACC_COLS;
                 const uint32_t idesc = (Cfg::HALVES_OK && x.half >= 0) ? p.idesc_half : p.idesc;
                 for (int kb = x.kb0; kb < x.kb1; ++kb) {
-                    if (!wait_phase(full_bar(stage), phase, wctx, kSiteMmaFull)) {
+                    if (!warp_wait_phase(full_bar(stage), phase, wctx, kSiteMmaFull)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after_sync();
                     const uint32_t sa = base + stage * Cfg::STAGE_BYTES;
                     const uint32_t sb = sa + Cfg::A_BYTES;
+                    if (elect_one_sync()) {
 #pragma unroll
-                    for (int k = 0; k < Cfg::BK / Cfg::UMMA_K; ++k) {
-                        const uint64_t adesc = smem_desc_sw128(sa + k * a_kstep, a_lbo, 1024u);
-                        const uint64_t bdesc = smem_desc_sw128(sb + k * b_kstep, b_lbo, 1024u);
-                        umma_f16_ss<CG>(d_tmem, adesc, bdesc, idesc, (kb != x.kb0 || k != 0) ? 1u : 0u);
+                        for (int k = 0; k < Cfg::BK / Cfg::UMMA_K; ++k) {
+                            const uint64_t adesc = smem_desc_sw128(sa + k * a_kstep, a_lbo, 1024u);
+                            const uint64_t bdesc = smem_desc_sw128(sb + k * b_kstep, b_lbo, 1024u);
+                            umma_f16_ss<CG>(d_tmem, adesc, bdesc, idesc, (kb != x.kb0 || k != 0) ? 1u : 0u);
+                        }
+                        // the stage is reusable once these MMAs finish; after the
+                        // item's last K block the accumulator is complete (the same
+                        // lane commits, so the commit covers its MMAs)
+                        umma_commit<CG>(empty_bar(stage), kPair);
+                        if (kb + 1 == x.kb1) umma_commit<CG>(accf_bar(buf), kPair);
                     }
-                    umma_commit<CG>(empty_bar(stage), kPair);   // stage reusable once these MMAs finish
+                    __syncwarp();
                     if (++stage == Cfg::STAGES) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
                 if (!ok) break;
-                umma_commit<CG>(accf_bar(buf), kPair);          // accumulator complete
+                if (x.kb1 == x.kb0) {
+                    // no K block (not produced by the scheduler): publish the empty accumulator
+                    if (elect_one_sync()) umma_commit<CG>(accf_bar(buf), kPair);
+                    __syncwarp();
+                }
                 if (++buf == 2) {
                     buf = 0;
                     acc_phase ^= 1u;
                 }
             }
             if (!ok) {
-                umma_commit<CG>(drain_bar, 1);                  // wait for every MMA issued so far
+                if (elect_one_sync()) umma_commit<CG>(drain_bar, 1);   // wait for every MMA issued so far
+                __syncwarp();
                 wait_phase_drain(drain_bar, 0, 100000000ull);
             }
         }

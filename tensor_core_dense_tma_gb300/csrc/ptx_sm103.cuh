@@ -55,6 +55,20 @@ __device__ __forceinline__ void cluster_sync_all() {
     asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// True in exactly one lane of the calling (converged) warp, the lowest
+// active one.  Code that issues tcgen05 or TMA instructions from one lane
+// keeps the rest of its loop warp-uniform and elects the issuing lane here.
+__device__ __forceinline__ bool elect_one_sync() {
+    uint32_t pred = 0;
+    asm volatile(
+        "{\n\t.reg .pred P;\n\t"
+        "elect.sync _|P, %1;\n\t"
+        "selp.u32 %0, 1, 0, P;\n\t}"
+        : "=r"(pred)
+        : "r"(0xffffffffu));
+    return pred != 0;
+}
+
 // ---------------------------------------------------------------------------
 // mbarrier
 // ---------------------------------------------------------------------------
