@@ -99,38 +99,36 @@ int default_units(const gemm_plan* plan, int kind) {
     return u > 0 ? u : plan->sm_count / kCfgCtas[kind];
 }
 
-// Columns of B one tile (or half-width item) loads per K step: the width,
-// or whole 64-column boxes per CTA when B is N-contiguous (row-major B) and
-// the per-CTA width is not a multiple of 64.
-int64_t loaded_cols(int kind, bool b_mn_major, bool half) {
-    const int64_t width = kCfgTileN[kind] / (half ? 2 : 1);
-    const int64_t per_cta = width / kCfgCtas[kind];
-    if (!b_mn_major) return width;
-    return ((per_cta + 63) / 64) * 64 * kCfgCtas[kind];
-}
-
 // Time of one 64-deep K step of a tile (or half-width item) on its unit,
-// relative to a 256 x 256 tile on a CTA pair.  Per SM, the step is half
-// tensor-core work (accumulator rows x columns, 128 x 256 for the pair tile)
-// and half operand feed (A rows + B columns loaded, 128 + 128 for the pair
-// tile); the pair tile is close to balanced between the two.
+// relative to a 256 x 256 tile on a CTA pair, as measured on GB300 at
+// 4096^3 (the main loop is bound by operand feed and, for N <= 128 MMAs, by
+// MMA issue, so the costs do not follow the tile areas):
+//   pair 256x256: 1.0; its half-width items: 0.757
+//   pair 256x224: 0.95 with row-major B (whole 64-column boxes per CTA),
+//                 0.85 with column-major B
+//   one CTA 128x256: 1.16; its half-width items: 0.88
+// (a least-squares fit over 9 shapes x 2 layouts x 6 choices, 4 % rms).
+// The transposed-product tiles (128 x 16, 128 x 64) only compete with each
+// other and with their own splits; they get the same per-step cost.
 double step_cost(int kind, bool b_mn_major, bool half) {
-    const double width = static_cast<double>(kCfgTileN[kind]) / (half ? 2.0 : 1.0);
-    const double mma = 128.0 * width / (128.0 * 256.0);
-    const double feed = (128.0 + static_cast<double>(loaded_cols(kind, b_mn_major, half)) / kCfgCtas[kind]) / 256.0;
-    return 0.5 * mma + 0.5 * feed;
+    switch (kind) {
+        case kCfgPair256: return half ? 0.757 : 1.0;
+        case kCfgPair224: return b_mn_major ? 0.95 : 0.85;
+        case kCfgSingle256: return half ? 0.88 : 1.16;
+        default: return 1.0;
+    }
 }
 
 // Configuration, K-split count and orientation with the smallest modelled
 // time: for each category of work item, waves (items over co-resident
 // units) times the item's cost in K steps (its k-blocks times step_cost, plus
-// 4 fixed).  Whole waves of tiles run whole; the tiles of a partial last
-// wave (or all tiles, when there are fewer than units) are either split into
-// `s` K ranges -- plus the partial-sum traffic, 2 + 2 * s * BN / 64 steps:
-// every split writes its fp32 partial and the last one reads them all back
-// (latency-bound, so charged double) -- or
-// run as two half-width items.  A divided tile is charged 2 extra steps, so
-// ties go to whole tiles.
+// 5 fixed; 3.4 for a half-width item).  Whole waves of tiles run whole; the
+// tiles of a partial last wave (or all tiles, when there are fewer than
+// units) are either split into `s` K ranges -- plus the reduction, 8 + 30 *
+// BN / 256 + 2 * s steps: every split writes its fp32 partial and the last
+// one to arrive reads them all back, a chain of latencies that costs about
+// 40 steps for a 256-wide tile on GB300 -- or run as two half-width items.
+// A divided tile is charged 2 extra steps, so ties go to whole tiles.
 // `valid` is false when a pinned configuration does not fit the problem.
 Choice choose(const gemm_plan* plan, int64_t M, int64_t N, int64_t K, gemm_dtype_t acc, bool b_mn_major,
               bool* valid) {
@@ -180,7 +178,7 @@ Choice choose(const gemm_plan* plan, int64_t M, int64_t N, int64_t K, gemm_dtype
         const int64_t rest = tiles - dp;                                      // the partial wave
         const int64_t tile_bytes = int64_t(kCfgCtas[kind]) * 128 * kCfgTileN[kind] * 4;
         const double full_step = step_cost(kind, bmn, false);
-        const double full_item = static_cast<double>(kb) * full_step + 4.0;
+        const double full_item = static_cast<double>(kb) * full_step + 5.0;
         // whole tiles only
         if (!pinned || plan->forced_splits == 1)
             consider(static_cast<double>((tiles + units - 1) / units) * full_item, kind, 1, tiles, false, tiles,
@@ -203,8 +201,8 @@ Choice choose(const gemm_plan* plan, int64_t M, int64_t N, int64_t K, gemm_dtype
         }
         if (split_tiles > 0) {
             for (int64_t s = smin; s <= smax && s > 1; ++s) {
-                const double reduce = 2.0 + 2.0 * static_cast<double>(s) * kCfgTileN[kind] / 64.0;
-                const double item = static_cast<double>((kb + s - 1) / s) * full_step + 4.0 + reduce + 2.0;
+                const double reduce = 8.0 + 30.0 * kCfgTileN[kind] / 256.0 + 2.0 * static_cast<double>(s);
+                const double item = static_cast<double>((kb + s - 1) / s) * full_step + 5.0 + reduce + 2.0;
                 const double cost = static_cast<double>(dp_split / units) * full_item +
                                     static_cast<double>((split_tiles * s + units - 1) / units) * item;
                 consider(cost, kind, static_cast<int>(s), dp_split, false, tiles, units);
@@ -212,7 +210,7 @@ Choice choose(const gemm_plan* plan, int64_t M, int64_t N, int64_t K, gemm_dtype
         }
         // two half-width items per tile of the partial wave
         if (kCfgHalves[kind] && rest > 0 && !pinned) {
-            const double item = static_cast<double>(kb) * step_cost(kind, bmn, true) + 4.0 + 2.0;
+            const double item = static_cast<double>(kb) * step_cost(kind, bmn, true) + 3.4 + 2.0;
             const double cost = static_cast<double>(dp / units) * full_item +
                                 static_cast<double>((2 * rest + units - 1) / units) * item;
             consider(cost, kind, 1, dp, true, tiles, units);
