@@ -401,12 +401,16 @@ __device__ __forceinline__ void load_c_block(const KernelParams& p, int row0, in
                                              float (&c)[32]) {
     const int col = col0 + lane;
     const bool col_ok = col < p.N;
+    const int nrows = col_ok ? p.M - row0 : 0;   // rows of the block inside C (for this lane)
     {
+        // one row pointer stepped by ldc: the block's 32 addresses cost an add each
+        const char* src = static_cast<const char*>(p.C) + (static_cast<int64_t>(row0) * p.ldc + col) * Vec<OUT>::ESZ;
+        const int64_t step = p.ldc * Vec<OUT>::ESZ;
         float t[32];
 #pragma unroll
         for (int r = 0; r < 32; ++r) {
-            const int row = row0 + r;
-            t[r] = (col_ok && row < p.M) ? load_elem<OUT>(p.C, static_cast<int64_t>(row) * p.ldc + col) : 0.0f;
+            t[r] = r < nrows ? load_elem<OUT>(src, 0) : 0.0f;
+            src += step;
         }
 #pragma unroll
         for (int r = 0; r < 32; ++r)
@@ -424,14 +428,14 @@ __device__ __forceinline__ void load_c_block(const KernelParams& p, int row0, in
 // waiting for the group.
 __device__ __forceinline__ void issue_c_block_f32(const KernelParams& p, int row0, int col0, int lane, uint32_t buf) {
     const int col = col0 + lane;
-    const bool col_ok = col < p.N;
+    const int nrows = col < p.N ? p.M - row0 : 0;
     const float* C = static_cast<const float*>(p.C);
+    const float* src = C + static_cast<int64_t>(row0) * p.ldc + col;
 #pragma unroll
     for (int r = 0; r < 32; ++r) {
-        const int row = row0 + r;
-        const bool ok = col_ok && row < p.M;
-        const float* src = ok ? C + static_cast<int64_t>(row) * p.ldc + col : C;
-        cp_async_4(buf + 4u * static_cast<uint32_t>(r * 32 + (lane ^ r)), src, ok ? 4u : 0u);
+        const bool ok = r < nrows;
+        cp_async_4(buf + 4u * static_cast<uint32_t>(r * 32 + (lane ^ r)), ok ? src : C, ok ? 4u : 0u);
+        src += p.ldc;
     }
     cp_async_commit();
 }
@@ -452,12 +456,14 @@ __device__ __forceinline__ void store_d_block(const KernelParams& p, int row0, i
     for (int j = 0; j < 32; ++j) st_shared_f32(buf + 4u * static_cast<uint32_t>(lane * 32 + (j ^ lane)), v[j]);
     __syncwarp();
     const int col = col0 + lane;
-    const bool col_ok = col < p.N;
+    const int nrows = col < p.N ? p.M - row0 : 0;
+    char* dst = static_cast<char*>(p.D) + (static_cast<int64_t>(row0) * p.ldc + col) * Vec<OUT>::ESZ;
+    const int64_t step = p.ldc * Vec<OUT>::ESZ;
 #pragma unroll
     for (int r = 0; r < 32; ++r) {
         const float x = ld_shared_f32(buf + 4u * static_cast<uint32_t>(r * 32 + (lane ^ r)));
-        const int row = row0 + r;
-        if (col_ok && row < p.M) store_elem<OUT>(p.D, static_cast<int64_t>(row) * p.ldc + col, x);
+        if (r < nrows) store_elem<OUT>(dst, 0, x);
+        dst += step;
     }
     __syncwarp();
 }
