@@ -164,6 +164,7 @@ Choice choose(const gemm_plan* plan, int64_t M, int64_t N, int64_t K, gemm_dtype
             best.splits = splits;
             best.dp_tiles = dp;
             best.n_halves = halves;
+            best.early = false;
             best.swap = swap;
             best.tiles = tiles;
             best.units = static_cast<int>(units);
@@ -208,6 +209,21 @@ Choice choose(const gemm_plan* plan, int64_t M, int64_t N, int64_t K, gemm_dtype
                 consider(cost, kind, static_cast<int>(s), dp_split, false, tiles, units);
             }
         }
+        // the partial wave's tiles split along K with early partials: at most
+        // one split per unit, the early splits first and the owners last, after
+        // at least one whole wave (so an owner never waits for its partials)
+        if (rest > 0 && dp >= units && !pinned && plan->d_flags && acc != GEMM_F16 && kCfgTileN[kind] >= 128) {
+            for (int64_t s = 2; s <= 4; ++s) {
+                if (rest * s > units || s > kb || rest * s * tile_bytes > static_cast<int64_t>(plan->ws_bytes) ||
+                    rest * s * kCfgCtas[kind] > kNumCounters)
+                    break;
+                const double item = static_cast<double>((kb + s - 1) / s) * full_step + 5.0 + 2.0 + 2.0;
+                const double cost = static_cast<double>(dp / units) * full_item + item;
+                const double before = best_cost;
+                consider(cost, kind, static_cast<int>(s), dp, false, tiles, units);
+                if (best_cost != before) best.early = true;
+            }
+        }
         // two half-width items per tile of the partial wave
         if (kCfgHalves[kind] && rest > 0 && !pinned) {
             const double item = static_cast<double>(kb) * step_cost(kind, bmn, true) + 3.4 + 2.0;
@@ -247,7 +263,7 @@ std::string config_name(const Choice& ch, gemm_dtype_t acc, gemm_dtype_t out) {
     std::string s = "tc" + std::to_string(kCfgCtas[ch.kind]) + "cta_" + std::to_string(kCfgTileM[ch.kind]) + "x" +
                     std::to_string(kCfgTileN[ch.kind]) + "_" + outs[out_slot(acc, out)];
     if (ch.swap) s += "_swapAB";
-    if (ch.splits > 1) s += "_splitk" + std::to_string(ch.splits);
+    if (ch.splits > 1) s += (ch.early ? "_esplitk" : "_splitk") + std::to_string(ch.splits);
     if (ch.n_halves) s += "_nhalves";
     return s;
 }
@@ -295,12 +311,15 @@ gemm_status_t gemm_plan_create(gemm_plan_t* out, int device, gemm_dtype_t in_dty
               (plan->ws_bytes = kWorkspaceBytes) > 0 &&
               cudaMalloc(&plan->d_counters, kNumCounters * sizeof(int)) == cudaSuccess &&
               cudaMemset(plan->d_counters, 0, kNumCounters * sizeof(int)) == cudaSuccess &&
+              cudaMalloc(&plan->d_flags, kNumCounters * sizeof(unsigned)) == cudaSuccess &&
+              cudaMemset(plan->d_flags, 0, kNumCounters * sizeof(unsigned)) == cudaSuccess &&
               prepare_all(plan) == GEMM_OK;
     if (!ok) {
         cudaGetLastError();
         if (plan->d_status) cudaFree(plan->d_status);
         if (plan->d_ws) cudaFree(plan->d_ws);
         if (plan->d_counters) cudaFree(plan->d_counters);
+        if (plan->d_flags) cudaFree(plan->d_flags);
         delete plan;
         return GEMM_ERR_CUDA;
     }
@@ -433,6 +452,7 @@ gemm_status_t gemm_plan_destroy(gemm_plan_t plan) {
         if (plan->d_status) cudaFree(plan->d_status);
         if (plan->d_ws) cudaFree(plan->d_ws);
         if (plan->d_counters) cudaFree(plan->d_counters);
+        if (plan->d_flags) cudaFree(plan->d_flags);
     }
     delete plan;
     return GEMM_OK;

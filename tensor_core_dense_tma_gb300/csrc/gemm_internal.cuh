@@ -76,6 +76,7 @@ struct gemm_plan {
     int* d_status = nullptr;      // [0] status, [1] site
     float* d_ws = nullptr;        // split-K partials
     int* d_counters = nullptr;    // split-K arrival counters (kept zero between launches)
+    unsigned* d_flags = nullptr;  // early-partial ready flags, kNumCounters (null: none)
     uint64_t timeout_ns = 2000000000ull;
     uint64_t launches = 0;
     tcdt_host::EncodeTiledFn encode = nullptr;
@@ -106,6 +107,7 @@ struct Choice {
     int splits = 1;
     int64_t dp_tiles = 0;      // whole tiles before the divided ones (see KernelParams)
     bool n_halves = false;     // divided tiles run as two half-width items (splits == 1)
+    bool early = false;        // divided tiles split with early partials (splits > 1)
     bool swap = false;
     int64_t tiles = 0;
     int units = 0;
@@ -266,6 +268,12 @@ gemm_status_t launch_tc(gemm_plan* plan, const Choice& ch, const Problem& pr, co
     p.d_tma = d_tma ? 1u : 0u;
     p.ws = plan->d_ws;
     p.counters = plan->d_counters;
+    p.early = (ch.early && ch.splits > 1 && plan->d_flags && Cfg::W == 32) ? 1 : 0;
+    {
+        const uint32_t e = static_cast<uint32_t>(plan->launches + 1);
+        p.epoch = e == 0u ? 1u : e;
+    }
+    p.flags = plan->d_flags;
     p.status = plan->d_status;
     p.timeout_ns = plan->timeout_ns;
 #ifdef TCDT_FAULT_INJECTION

@@ -57,6 +57,8 @@ enum WaitSite : int {
     kSiteMmaAccEmpty = 2,
     kSiteMmaFull = 3,
     kSiteEpilogueAccFull = 4,
+    kSitePartialReady = 5,
+    kSiteMmaAccInit = 6,
 };
 
 struct KernelParams {
@@ -78,6 +80,9 @@ struct KernelParams {
     uint32_t d_tma;           // 1: D rows are 16-byte aligned: store D tiles with TMA (tmD)
     float* ws;                // split partials, [split tile][split][cta][128][BN] fp32
     int* counters;            // [split tile][cta] split arrivals; zero on entry, left zero
+    int32_t early;            // 1: divided tiles use early partials (see unit_item)
+    uint32_t epoch;           // this launch's nonzero tag for partial-ready flags
+    unsigned* flags;          // [split tile][split][cta] partial-ready flags (earlier launches' tags)
     int* status;              // [0] status code, [1] site
     uint64_t timeout_ns;
 #ifdef TCDT_FAULT_INJECTION
@@ -116,7 +121,7 @@ struct TileConfig {
                                    : 2 * ACC_COLS <= 128 ? 128 : 2 * ACC_COLS <= 256 ? 256 : 512;
     static constexpr int NUM_EPI_WARPS = 4;
     static constexpr int NUM_THREADS = 32 * (2 + NUM_EPI_WARPS);
-    static constexpr int NUM_BARRIERS = 2 * STAGES + 2 + 2 + 1;
+    static constexpr int NUM_BARRIERS = 2 * STAGES + 2 + 2 + 1 + 1 + NUM_EPI_WARPS;
     // epilogue staging for TMA stores: per epilogue warp two 32-row buffers
     // of up to 128 bytes a row (32 fp32 columns)
     static constexpr int STAGING_BUF = 32 * 128;
@@ -158,11 +163,19 @@ __host__ __device__ constexpr int largest_divisor_upto(int n, int cap) {
 // [kb0, kb1), never empty (splits <= k-blocks).  With dp_tiles = (whole
 // waves of tiles) only the last, partial wave is divided, so its work
 // spreads over all units instead of leaving most of them idle.
+enum ItemRole : int {
+    kRoleWhole = 0,    // a whole tile (also a half-width item)
+    kRoleSplit = 1,    // one K range of a split tile; the last split to arrive reduces
+    kRoleEarly = 2,    // an early-partial split: writes its fp32 partial and a ready flag
+    kRoleOwner = 3,    // the owner split: its accumulator starts as the sum of the partials
+};
+
 struct WorkItem {
     int tile;      // output tile
     int stile;     // index among the divided tiles (-1: a whole tile)
     int split, nsplit, kb0, kb1;
     int half;      // -1: full width; 0 / 1: column half of the tile
+    int role;
 };
 
 __device__ __forceinline__ int num_work_items(const KernelParams& p) {
@@ -172,6 +185,7 @@ __device__ __forceinline__ int num_work_items(const KernelParams& p) {
 __device__ __forceinline__ WorkItem work_item(const KernelParams& p, int w) {
     WorkItem x;
     x.half = -1;
+    x.role = kRoleWhole;
     if (w < p.dp_tiles) {
         x.tile = w;
         x.stile = -1;
@@ -198,6 +212,41 @@ __device__ __forceinline__ WorkItem work_item(const KernelParams& p, int w) {
     x.nsplit = p.splits;
     x.kb0 = static_cast<int>(static_cast<int64_t>(p.num_k_blocks) * x.split / p.splits);
     x.kb1 = static_cast<int>(static_cast<int64_t>(p.num_k_blocks) * (x.split + 1) / p.splits);
+    x.role = kRoleSplit;
+    return x;
+}
+
+// The work items of one unit, in order.  Normally unit u takes items
+// u, u + units, u + 2 units, ...  With early partials the whole tiles form
+// whole waves (dp_tiles = waves x units) and split tile j's S splits go to
+// units j*S .. j*S + S - 1: split s >= 1 (an early split) is its unit's first
+// item and leaves its fp32 partial in the workspace; split 0 (the owner) is
+// its unit's last item, whose accumulator starts from the partials, written
+// a whole-tile time or more earlier, so nothing waits on them in practice.
+__device__ __forceinline__ int unit_items(const KernelParams& p, int unit, int units) {
+    if (!p.early) {
+        const int n = num_work_items(p);
+        return unit < n ? (n - unit + units - 1) / units : 0;
+    }
+    const int whole = p.dp_tiles / units;
+    return whole + (unit < (p.num_tiles - p.dp_tiles) * p.splits ? 1 : 0);
+}
+
+__device__ __forceinline__ WorkItem unit_item(const KernelParams& p, int unit, int units, int i) {
+    if (!p.early) return work_item(p, unit + i * units);
+    const int whole = p.dp_tiles / units;
+    const bool split = unit < (p.num_tiles - p.dp_tiles) * p.splits;
+    const int s = split ? unit % p.splits : 0;
+    int k = i;                          // index among the unit's whole tiles
+    if (split && s != 0) {
+        if (i == 0) k = -1;             // the early split comes first
+        else k = i - 1;
+    } else if (split && i == whole) {
+        k = -1;                         // the owner split comes last
+    }
+    if (k >= 0) return work_item(p, unit + k * units);
+    WorkItem x = work_item(p, p.dp_tiles + unit);   // split (unit / S, unit % S) of the divided tiles
+    x.role = s == 0 ? kRoleOwner : kRoleEarly;
     return x;
 }
 
@@ -234,6 +283,23 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, const 
 template <bool kClusterScope = false>
 __device__ __forceinline__ bool warp_wait_phase(uint32_t bar, uint32_t parity, const WaitCtx& w, int site) {
     return __all_sync(0xffffffffu, wait_phase<kClusterScope>(bar, parity, w, site));
+}
+
+// Bounded wait until another unit has published this launch's tag.
+__device__ __forceinline__ bool wait_flag(const unsigned* flag, unsigned epoch, const WaitCtx& w, int site) {
+    if (ld_acquire_gpu(flag) == epoch) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+#pragma unroll 1
+        for (int i = 0; i < 64; ++i)
+            if (ld_acquire_gpu(flag) == epoch) return true;
+        if (*w.abort_flag) return false;
+        if (globaltimer_ns() - t0 > w.timeout_ns) {
+            *w.abort_flag = 1;
+            if (atomicCAS(w.status, 0, kStatusTimeout) == 0) atomicExch(w.status + 1, site);
+            return false;
+        }
+    }
 }
 
 // Bounded wait used only while winding down after an abort.
@@ -658,6 +724,8 @@ gemm_sm103_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     auto accf_bar = [&](int b) { return bar_base + 8u * (2 * Cfg::STAGES + b); };
     auto acce_bar = [&](int b) { return bar_base + 8u * (2 * Cfg::STAGES + 2 + b); };
     const uint32_t drain_bar = bar_base + 8u * (2 * Cfg::STAGES + 4);
+    const uint32_t accinit_bar = bar_base + 8u * (2 * Cfg::STAGES + 5);   // owner accumulator seeded
+    auto seed_bar = [&](int w) { return bar_base + 8u * (2 * Cfg::STAGES + 6 + w); };   // per epilogue warp
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base_ptr + Cfg::STAGES * Cfg::STAGE_BYTES +
                                                       Cfg::STAGING_BYTES + 8 * Cfg::NUM_BARRIERS);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -671,7 +739,7 @@ gemm_sm103_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     const int unit = CG == 1 ? static_cast<int>(blockIdx.x) : static_cast<int>(cluster_id_x());
     const int num_units = CG == 1 ? static_cast<int>(gridDim.x) : static_cast<int>(num_clusters_x());
     const bool leader = rank == 0;
-    const int num_work = num_work_items(p);
+    const int num_items = unit_items(p, unit, num_units);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < Cfg::STAGES; ++s) {
@@ -683,6 +751,8 @@ gemm_sm103_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             mbar_init(acce_bar(b), Cfg::NUM_EPI_WARPS * CG);
         }
         mbar_init(drain_bar, 1);
+        mbar_init(accinit_bar, Cfg::NUM_EPI_WARPS * CG);
+        for (int w = 0; w < Cfg::NUM_EPI_WARPS; ++w) mbar_init(seed_bar(w), 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -720,8 +790,8 @@ gemm_sm103_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                                                     : static_cast<uint32_t>(Cfg::BN_CTA * Cfg::BK * 2);
             const uint32_t b_tx_half = p.b_mn_major ? static_cast<uint32_t>(Cfg::B_CHUNKS_HALF * 64 * Cfg::BK * 2)
                                                     : static_cast<uint32_t>(Cfg::BN_CTA_HALF * Cfg::BK * 2);
-            for (int w = unit; ok && w < num_work; w += num_units) {
-                const WorkItem x = work_item(p, w);
+            for (int it = 0; ok && it < num_items; ++it) {
+                const WorkItem x = unit_item(p, unit, num_units, it);
                 int mb, nb;
                 tile_coords(p, x.tile, mb, nb);
                 const bool half = Cfg::HALVES_OK && x.half >= 0;
@@ -827,17 +897,26 @@ gemm_sm103_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             const uint32_t b_lbo = p.b_mn_major ? Cfg::MN_CHUNK_BYTES : 16u;
             const uint32_t a_kstep = p.a_mn_major ? 16u * 128u : 32u;
             const uint32_t b_kstep = p.b_mn_major ? 16u * 128u : 32u;
-            for (int w = unit; ok && w < num_work; w += num_units) {
-                const WorkItem x = work_item(p, w);
+            uint32_t init_phase = 0;
+            for (int it = 0; ok && it < num_items; ++it) {
+                const WorkItem x = unit_item(p, unit, num_units, it);
                 bool got;
                 if constexpr (CG == 1) got = warp_wait_phase(acce_bar(buf), acc_phase ^ 1u, wctx, kSiteMmaAccEmpty);
                 else got = warp_wait_phase<true>(acce_bar(buf), acc_phase ^ 1u, wctx, kSiteMmaAccEmpty);
+                if (got && x.role == kRoleOwner) {
+                    // the epilogue warps of both CTAs seed this accumulator with the
+                    // early splits' partials
+                    if constexpr (CG == 1) got = warp_wait_phase(accinit_bar, init_phase, wctx, kSiteMmaAccInit);
+                    else got = warp_wait_phase<true>(accinit_bar, init_phase, wctx, kSiteMmaAccInit);
+                    init_phase ^= 1u;
+                }
                 if (!got) {
                     ok = false;
                     break;
                 }
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + buf * Cfg::ACC_COLS;
+                const bool seeded = x.role == kRoleOwner;   // accumulate from the first MMA on
                 const uint32_t idesc = (Cfg::HALVES_OK && x.half >= 0) ? p.idesc_half : p.idesc;
                 for (int kb = x.kb0; kb < x.kb1; ++kb) {
                     if (!warp_wait_phase(full_bar(stage), phase, wctx, kSiteMmaFull)) {
@@ -852,7 +931,7 @@ gemm_sm103_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                         for (int k = 0; k < Cfg::BK / Cfg::UMMA_K; ++k) {
                             const uint64_t adesc = smem_desc_sw128(sa + k * a_kstep, a_lbo, 1024u);
                             const uint64_t bdesc = smem_desc_sw128(sb + k * b_kstep, b_lbo, 1024u);
-                            umma_f16_ss<CG>(d_tmem, adesc, bdesc, idesc, (kb != x.kb0 || k != 0) ? 1u : 0u);
+                            umma_f16_ss<CG>(d_tmem, adesc, bdesc, idesc, (seeded || kb != x.kb0 || k != 0) ? 1u : 0u);
                         }
                         // the stage is reusable once these MMAs finish; after the
                         // item's last K block the accumulator is complete (the same
@@ -893,11 +972,12 @@ gemm_sm103_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         const int row_local = 32 * quad + lane;
         const uint32_t stg = staging_base + static_cast<uint32_t>(warp - 2) * 2u * Cfg::STAGING_BUF;
         int sbuf = 0;                     // staging buffer for the next TMA store of this warp
+        uint32_t seed_phase = 0;          // phase of this warp's seed barrier
         int buf = 0;
         uint32_t acc_phase = 0;
         int iter = 0;
-        for (int w = unit; w < num_work; w += num_units, ++iter) {
-            const WorkItem x = work_item(p, w);
+        for (; iter < num_items; ++iter) {
+            const WorkItem x = unit_item(p, unit, num_units, iter);
             int mb, nb;
             tile_coords(p, x.tile, mb, nb);
             const int m0 = mb * Cfg::UMMA_M + Cfg::BM * static_cast<int>(rank);
@@ -907,6 +987,89 @@ gemm_sm103_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             // warm L2 with this thread's C row while the main loop runs
             if (p.beta != 0.0f && !p.trans_out && m0 + row_local < p.M)
                 prefetch_c_row<Cfg>(p, m0 + row_local, n0, nchunks * W);
+            if constexpr (W == 32) {
+                if (p.early && iter + 1 < num_items) {
+                    const WorkItem y = unit_item(p, unit, num_units, iter + 1);
+                    if (y.role == kRoleOwner) {
+                        // While this item's MMAs run, seed the next item's accumulator
+                        // (the other TMEM buffer, drained by the previous iteration)
+                        // with the sum of the early splits' partials, in split order.
+                        const int S = y.nsplit;
+                        if (threadIdx.x == 64) {
+                            const unsigned* f = p.flags + static_cast<int64_t>(y.stile) * S * CG + rank;
+                            bool got = true;
+                            for (int j = 1; j < S && got; ++j)
+                                got = wait_flag(f + static_cast<int64_t>(j) * CG, p.epoch, wctx, kSitePartialReady);
+                            epi_last_flag[iter & 1] = got ? 1 : 0;
+                        }
+                        named_bar_sync(1, 32 * Cfg::NUM_EPI_WARPS);
+                        if (!epi_last_flag[iter & 1]) break;
+                        // Each warp brings its 32 rows of the partials in by TMA, two
+                        // 32 x 32 fp32 boxes at a time, through its two staging buffers
+                        // (128-byte swizzle, as the stores use them).  Plain loads of the
+                        // partials here slowed the concurrent main loop by half.
+                        const uint32_t sbar = seed_bar(warp - 2);
+                        const uint32_t t_next =
+                            tmem_base + (static_cast<uint32_t>(32 * quad) << 16) + (buf ^ 1) * Cfg::ACC_COLS;
+                        constexpr int NCH = Cfg::BN / W;
+                        bool seeded_ok = true;
+                        if (lane == 0) fence_proxy_async_global();
+#pragma unroll 1
+                        for (int c = 0; c < NCH && seeded_ok; c += 2) {
+                            const int nc = c + 1 < NCH ? 2 : 1;
+                            float sum[2][W];
+#pragma unroll 1
+                            for (int j = 1; j < S && seeded_ok; ++j) {
+                                const int prow = static_cast<int>(
+                                    ((static_cast<int64_t>(y.stile) * S + j) * CG + rank) * Cfg::BM + 32 * quad);
+                                if (lane == 0) {
+                                    bulk_wait_group_read<0>();   // earlier stores have read the staging buffers
+                                    mbar_arrive_expect_tx(sbar, static_cast<uint32_t>(nc) * 4096u);
+                                    for (int h = 0; h < nc; ++h)
+                                        tma_load_2d(stg + static_cast<uint32_t>(h) * 4096u, &tmW, sbar, W * (c + h), prow);
+                                }
+                                __syncwarp();
+                                seeded_ok = warp_wait_phase(sbar, seed_phase, wctx, kSitePartialReady);
+                                seed_phase ^= 1u;
+                                if (!seeded_ok) break;
+#pragma unroll
+                                for (int h = 0; h < 2; ++h) {
+                                    if (h < nc) {
+                                        const uint32_t rowp = stg + static_cast<uint32_t>(h) * 4096u + lane * 128u;
+#pragma unroll
+                                        for (int ch = 0; ch < 8; ++ch) {
+                                            const float4 q = ld_shared_v4f(rowp + ((static_cast<uint32_t>(ch) ^ (lane & 7u)) << 4));
+                                            const float v4[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+                                            for (int e = 0; e < 4; ++e)
+                                                sum[h][4 * ch + e] = j == 1 ? v4[e] : sum[h][4 * ch + e] + v4[e];
+                                        }
+                                    }
+                                }
+                                __syncwarp();   // the buffers are read before the next loads land
+                            }
+                            if (!seeded_ok) break;
+#pragma unroll
+                            for (int h = 0; h < 2; ++h) {
+                                if (h < nc) {
+                                    uint32_t r[W];
+#pragma unroll
+                                    for (int i = 0; i < W; ++i) r[i] = __float_as_uint(sum[h][i]);
+                                    tmem_st_32x32b_x32(t_next + W * (c + h), r);
+                                }
+                            }
+                        }
+                        if (!seeded_ok) break;
+                        tmem_st_wait();
+                        tc_fence_before_sync();
+                        __syncwarp();
+                        if (lane == 0) {
+                            if constexpr (CG == 1) mbar_arrive(accinit_bar);
+                            else mbar_arrive_cluster(map_to_cta(accinit_bar, 0));   // the leader's barrier
+                        }
+                    }
+                }
+            }
             if (threadIdx.x == 64)
                 epi_ok_flag[iter & 1] = wait_phase(accf_bar(buf), acc_phase, wctx, kSiteEpilogueAccFull) ? 1 : 0;
             named_bar_sync(1, 32 * Cfg::NUM_EPI_WARPS);
@@ -915,7 +1078,30 @@ gemm_sm103_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             const int row = m0 + row_local;
             const bool row_ok = row < p.M;
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(32 * quad) << 16) + buf * Cfg::ACC_COLS;
-            if (x.nsplit == 1) {
+            if (x.role == kRoleEarly) {
+                // an early split: its fp32 partial -> workspace, then the ready flag
+                if constexpr (W == 32) {
+                    const int ws_row0 = static_cast<int>(
+                        ((static_cast<int64_t>(x.stile) * x.nsplit + x.split) * CG + rank) * Cfg::BM + 32 * quad);
+#pragma unroll 1
+                    for (int c = 0; c < Cfg::BN / W; ++c) {
+                        __syncwarp();
+                        uint32_t r[W];
+                        tmem_ld_row<W>(t_row + W * c, r);
+                        tmem_ld_wait();
+                        stage_and_store_f32(&tmW, r, W * c, ws_row0, lane, stg, sbuf);
+                    }
+                    if (lane == 0) {
+                        bulk_wait_group<0>();
+                        fence_proxy_async_global();
+                    }
+                    __syncwarp();
+                    __threadfence();
+                    named_bar_sync(1, 32 * Cfg::NUM_EPI_WARPS);
+                    if (threadIdx.x == 64)
+                        st_release_gpu(p.flags + (static_cast<int64_t>(x.stile) * x.nsplit + x.split) * CG + rank, p.epoch);
+                }
+            } else if (x.nsplit == 1 || x.role == kRoleOwner) {
                 bool staged = false;
                 if constexpr (W == 32) {
                     if (p.d_tma && (p.beta == 0.0f || Cfg::OUT != kOutF32)) {

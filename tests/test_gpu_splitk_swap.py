@@ -171,3 +171,45 @@ def test_partial_wave_divided(plans, shape, layouts, out):
     D = run_gpu(plan, w, h)
     torch.cuda.synchronize()
     check_sampled(w, h, D, integer=True, n_random=4096)
+
+
+# Shapes whose partial last wave is split along K with early partials: the
+# non-owner splits run first in their units and leave fp32 partials, the owner
+# split runs last and starts its accumulator from them.  Ragged edges,
+# alpha/beta with C, 16-bit and fp32 outputs, row- and column-major operands.
+EARLY_SHAPES = [(2300, 2290, 800), (4096, 4096, 1024), (2560, 2560, 2048), (3000, 3496, 1504)]
+
+
+@pytest.mark.parametrize("shape", EARLY_SHAPES, ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("out", ["f32", "bf16"])
+def test_early_split_integer_twin(plans, shape, out):
+    from gpu_util import check_sampled
+    w = W(*shape, "row", "row", out=out, alpha=0.5, beta=1.0)
+    plan = plans["f16"]
+    desc = plan.describe(w.M, w.N, w.K, w.layoutA, w.layoutB, "f32", out)
+    assert "esplitk" in desc, desc
+    lda, ldb = padded(w)
+    h = wl.make_inputs(w, integer=True, lda=lda, ldb=ldb)
+    D = run_gpu(plan, w, h)
+    torch.cuda.synchronize()
+    if w.M * w.N * w.K <= 5e9:
+        check_full(w, h, D, integer=True)
+    else:
+        check_sampled(w, h, D, integer=True, n_random=8192)
+
+
+def test_early_split_random_repeats_bitwise(plans):
+    """Random data through early partials: within tolerance of the oracle and
+    bit-identical from call to call (partials are summed in split order)."""
+    w = W(2300, 2290, 800, "col", "row", out="f32", alpha=0.5, beta=1.0)
+    plan = plans["f16"]
+    assert "esplitk" in plan.describe(w.M, w.N, w.K, w.layoutA, w.layoutB, "f32", "f32")
+    lda, ldb = padded(w)
+    h = wl.make_inputs(w, lda=lda, ldb=ldb)
+    D0 = run_gpu(plan, w, h)
+    torch.cuda.synchronize()
+    check_full(w, h, D0, integer=False)
+    for _ in range(5):
+        D1 = run_gpu(plan, w, h)
+        torch.cuda.synchronize()
+        assert torch.equal(D0, D1)
