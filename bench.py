@@ -175,9 +175,33 @@ def cpu_baseline(w, h, target_s: float = 12.0):
                 w.out_dtype, w.alpha, w.beta, nthreads=cores)
     dt = time.perf_counter() - t0
     flops = 2.0 * rows * w.N * w.K
+    # the same triple loop on one thread, on a slice that takes about a fifth of the time
+    r1 = max(1, min(w.M, int(rows / cores * 0.2)))
+    t1 = time.perf_counter()
+    oracle.gemm(w.in_dtype, A, B, C, r1, w.N, w.K, h.lda, h.ldb, h.ldc, w.layoutA, w.layoutB,
+                w.out_dtype, w.alpha, w.beta, nthreads=1)
+    d1 = time.perf_counter() - t1
+    f1 = 2.0 * r1 * w.N * w.K
     return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
             "sample": f"first {rows} rows of D ({rows}x{w.N}x{w.K}, {flops:.3g} flop) in {dt:.2f} s "
-                      f"on {cores} threads"}
+                      f"on {cores} threads",
+            "single_thread": {"value": f1 / d1 / 1e12, "unit": "TFLOP/s",
+                              "sample": f"first {r1} rows of D ({f1:.3g} flop) in {d1:.2f} s on 1 thread"}}
+
+
+def kernel_sources_hash() -> str:
+    """Hash of the sources the GEMM kernels are compiled from (the kernel, its
+    PTX wrappers, the launch code and the per-configuration units)."""
+    import glob
+    import hashlib
+    csrc = os.path.join(ROOT, "tensor_core_dense_tma_gb300", "csrc")
+    files = [os.path.join(csrc, n) for n in ("gemm_kernel.cuh", "ptx_sm103.cuh", "gemm_internal.cuh")]
+    files += sorted(glob.glob(os.path.join(csrc, "gemm_cfg_*.cu")))
+    hsh = hashlib.sha256()
+    for fn in files:
+        with open(fn, "rb") as f:
+            hsh.update(f.read())
+    return hsh.hexdigest()[:16]
 
 
 def traffic_from_profiles(kernel_tag: str):
@@ -189,13 +213,7 @@ def traffic_from_profiles(kernel_tag: str):
             kv = dict(line.strip().split("=", 1) for line in f if "=" in line and not line.startswith("#"))
     except OSError:
         return None
-    from tensor_core_dense_tma_gb300 import build as tcbuild
-    import hashlib
-    hsh = hashlib.sha256()
-    for fn in tcbuild._inputs():
-        with open(fn, "rb") as f:
-            hsh.update(f.read())
-    if kv.get("sources_sha256") != hsh.hexdigest()[:16]:
+    if kv.get("sources_sha256") != kernel_sources_hash():
         return None
     val = kv.get(f"{kernel_tag}.bytes_per_launch")
     return float(val) if val else None
@@ -379,6 +397,16 @@ def main():
                                if peak_src == "measured" else "fallback 1.9 PFLOP/s bf16 burst",
                 "kernel": kernel_tag,
                 "algorithmic": f"2*M*N*K = {w.flops:.4g} flop per launch"}
+    try:
+        # tensor-core rate probe (no memory traffic): cycles per 256x256x16 MMA and the peak
+        # it implies at the clock measured meanwhile; outside the timed region
+        probe = tc.gemm_measure_mma_rate(dev.index if dev.index is not None else 0, w.in_dtype,
+                                         w.accum_dtype, 256)
+        roofline["mma_probe"] = {k: probe[k] for k in ("cycles_per_mma", "flop_per_clk_per_sm", "sm_mhz",
+                                                       "peak_tflops_at_clock")}
+        roofline["mma_probe"]["peak_tflops_at_2070_mhz"] = probe["sms"] * probe["flop_per_clk_per_sm"] * 2070e6 / 1e12
+    except Exception as e:   # the probe is context; never fail the bench on it
+        roofline["mma_probe"] = {"error": str(e)[:120]}
     cpu = None
     if not args.no_cpu_baseline and world == 1:
         cpu = cpu_baseline(w, h)

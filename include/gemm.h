@@ -192,6 +192,20 @@ gemm_status_t gemm_run_static_scratch(int device, gemm_dtype_t in_dtype, const v
                                       gemm_dtype_t out_dtype, float alpha, float beta, int splits,
                                       void *stream);
 
+/* Tensor-core rate probe (no memory traffic): the median number of SM
+ * cycles one tcgen05.mma kind::f16 with M = 256 (a CTA pair), N = `n`
+ * columns (16..256, a multiple of 16) and K = 16 takes when issued as the
+ * GEMM kernel issues it (one elected lane, four MMAs and one commit per
+ * stage, a six-deep ring of stage barriers), on every SM pair of `device`,
+ * and the SM clock measured meanwhile (cycles per nanosecond x 1000).  Each
+ * SM of the pair does 2 * 128 * n * 16 flop per MMA, so the tensor peak at
+ * that clock is sm_count * 2 * 128 * n * 16 / cycles_per_mma * sm_mhz * 1e6.
+ * in_dtype GEMM_F16 or GEMM_BF16; accum_dtype GEMM_F32, or GEMM_F16 with
+ * fp16 input.  Launches its own kernels and synchronises the device; takes
+ * a few milliseconds.  Returns GEMM_ERR_TIMEOUT if a wait inside ran out. */
+gemm_status_t gemm_measure_mma_rate(int device, gemm_dtype_t in_dtype, gemm_dtype_t accum_dtype, int n,
+                                    double *cycles_per_mma, double *sm_mhz);
+
 /* Free the plan and its device memory.  NULL is accepted (no-op).  The
  * caller must have synchronised any stream still running its launches. */
 gemm_status_t gemm_plan_destroy(gemm_plan_t plan);

@@ -80,6 +80,9 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.gemm_run_static_scratch.restype = i32
     lib.gemm_status_string.argtypes = [i32]
     lib.gemm_status_string.restype = ctypes.c_char_p
+    lib.gemm_measure_mma_rate.argtypes = [i32, i32, i32, i32, ctypes.POINTER(ctypes.c_double),
+                                          ctypes.POINTER(ctypes.c_double)]
+    lib.gemm_measure_mma_rate.restype = i32
     return lib
 
 
@@ -187,6 +190,24 @@ def gemm_run_static_scratch(device, in_dtype, A, B, C, D, M, N, K, lda, ldb, ldc
 
 def gemm_status_string(status: int) -> str:
     return load().gemm_status_string(status).decode()
+
+
+def gemm_measure_mma_rate(device: int = 0, in_dtype: str = "f16", accum_dtype: str = "f32",
+                          n: int = 256) -> dict:
+    """Tensor-core rate probe (see gemm.h): cycles per 256 x n x 16 MMA on a
+    CTA pair, the SM clock meanwhile, the flop per SM per cycle and the peak
+    at that clock over all SMs."""
+    cyc, mhz = ctypes.c_double(), ctypes.c_double()
+    st = load().gemm_measure_mma_rate(device, DTYPE[in_dtype], DTYPE[accum_dtype], n, ctypes.byref(cyc),
+                                      ctypes.byref(mhz))
+    if st != 0:
+        raise GemmError(st, "gemm_measure_mma_rate")
+    import torch
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    flop_clk = 2.0 * 128 * n * 16 / cyc.value
+    return {"cycles_per_mma": cyc.value, "sm_mhz": mhz.value, "flop_per_clk_per_sm": flop_clk,
+            "peak_tflops_at_clock": sms * flop_clk * mhz.value * 1e6 / 1e12, "sms": sms, "n": n,
+            "in_dtype": in_dtype, "accum_dtype": accum_dtype}
 
 
 # torch-facing convenience -----------------------------------------------------

@@ -93,3 +93,41 @@ def test_full_size_sampled(plans, name, integer):
     check_sampled(w, h, D, integer, n_random=n)
     del D
     torch.cuda.empty_cache()
+
+
+# Full-size workloads small enough for the oracle to compute every element in
+# seconds on the host cores: all elements, random data and the integer twin.
+FULL_ORACLE = ["pr1", "ragged", "bf16_1024", "bf16_2048", "skinny"]
+
+
+@pytest.mark.parametrize("name", FULL_ORACLE)
+@pytest.mark.parametrize("integer", [False, True], ids=["random", "twin"])
+def test_full_size_every_element(plans, name, integer):
+    w = wl.WORKLOADS[name]
+    h = wl.make_inputs(w, integer=integer)
+    D = run_gpu(plans[w.in_dtype], w, h)
+    torch.cuda.synchronize()
+    check_full(w, h, D, integer)
+    del D
+    torch.cuda.empty_cache()
+
+
+def test_sq4096_every_element_twin(plans):
+    """The bench's workload (4096^3, fp16 -> fp32) in the launch configuration
+    the bench times: all 16.8 M elements equal the oracle bit for bit on the
+    integer twin (every partial sum is an exact fp32 integer)."""
+    w = wl.WORKLOADS["sq4096"]
+    h = wl.make_inputs(w, integer=True)
+    D = run_gpu(plans[w.in_dtype], w, h)
+    torch.cuda.synchronize()
+    check_full(w, h, D, integer=True)
+
+
+def test_sq4096h_k256_every_element_twin(plans):
+    """fp16 accumulation at M = N = 4096 with K = 256 (partial sums stay exact
+    in fp16): every element bit for bit."""
+    w = wl.WORKLOADS["sq4096h"].with_shape(4096, 4096, 256)
+    h = wl.make_inputs(w, integer=True)
+    D = run_gpu(plans[w.in_dtype], w, h)
+    torch.cuda.synchronize()
+    check_full(w, h, D, integer=True)
