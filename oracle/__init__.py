@@ -65,6 +65,12 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.oracle_gemm_entries.argtypes = [i32, p, p, p, p, p, i64, p, p, i64, i64, i64, i64, i64,
                                         i64, i32, i32, i32, f64, f64, i32]
     lib.oracle_gemm_entries.restype = i32
+    lib.oracle_gemm_ep.argtypes = [i32, p, p, p, p, i64, p, p, i64, i64, i64, i64, i64, i64,
+                                   i32, i32, i32, f64, f64, p, p, p, i32, i32]
+    lib.oracle_gemm_ep.restype = i32
+    lib.oracle_gemm_entries_ep.argtypes = [i32, p, p, p, p, p, i64, p, p, i64, i64, i64, i64, i64,
+                                           i64, i32, i32, i32, f64, f64, p, p, p, i32, i32]
+    lib.oracle_gemm_entries_ep.restype = i32
     lib.oracle_round.argtypes = [p, i64, i32, p]
     lib.oracle_round.restype = i32
     lib.oracle_decode.argtypes = [p, i64, i32, p]
@@ -109,24 +115,42 @@ def _out_np_dtype(out_dtype: str):
     return np.float32 if out_dtype == "f32" else np.uint16
 
 
+ACT = {"none": 0, "relu": 1, "gelu": 2}
+
+
+def _vec(v: np.ndarray | None, n: int, what: str) -> np.ndarray | None:
+    if v is None:
+        return None
+    v = np.ascontiguousarray(v)
+    if v.dtype != np.float32 or v.shape != (n,):
+        raise TypeError(f"{what} must be a float32 vector of length {n}")
+    return v
+
+
 def gemm(in_dtype: str, A: np.ndarray, B: np.ndarray, C: np.ndarray | None,
          M: int, N: int, K: int, lda: int, ldb: int, ldc: int,
          layoutA: str = "row", layoutB: str = "row", out_dtype: str = "f32",
          alpha: float = 1.0, beta: float = 0.0, nthreads: int = 1,
-         want_exact: bool = False, lib: ctypes.CDLL | None = None):
+         want_exact: bool = False, lib: ctypes.CDLL | None = None,
+         bias: np.ndarray | None = None, row_scale: np.ndarray | None = None,
+         col_scale: np.ndarray | None = None, act: str = "none"):
     """Full M x N product.  Returns ``D`` (M x N, dense, out_dtype storage:
     float32 or uint16 bits) and, with ``want_exact``, also the unrounded
-    binary64 values ``V`` and the error scale ``S``."""
+    binary64 values ``V`` and the error scale ``S``.  The optional fused
+    epilogue (float32 vectors bias[N], row_scale[M], col_scale[N] and
+    act in none/relu/gelu) is applied as oracle.c defines it."""
     lib = lib or load_library()
     A = _in_bits(A)
     B = _in_bits(B)
     Cc = _c_array(C, out_dtype)
+    bv, rv, cv = _vec(bias, N, "bias"), _vec(row_scale, M, "row_scale"), _vec(col_scale, N, "col_scale")
     D = np.zeros((M, N), dtype=_out_np_dtype(out_dtype))
     V = np.zeros((M, N), dtype=np.float64) if want_exact else None
     S = np.zeros((M, N), dtype=np.float64) if want_exact else None
-    rc = lib.oracle_gemm(_DT[in_dtype], _ptr(A), _ptr(B), _ptr(Cc), _ptr(D), N, _ptr(V), _ptr(S),
-                         M, N, K, lda, ldb, ldc, _LAYOUT[layoutA], _LAYOUT[layoutB],
-                         _DT[out_dtype], float(alpha), float(beta), int(nthreads))
+    rc = lib.oracle_gemm_ep(_DT[in_dtype], _ptr(A), _ptr(B), _ptr(Cc), _ptr(D), N, _ptr(V), _ptr(S),
+                            M, N, K, lda, ldb, ldc, _LAYOUT[layoutA], _LAYOUT[layoutB],
+                            _DT[out_dtype], float(alpha), float(beta), _ptr(bv), _ptr(rv), _ptr(cv),
+                            ACT[act], int(nthreads))
     if rc != 0:
         raise ValueError("oracle_gemm rejected its arguments")
     return (D, V, S) if want_exact else D
@@ -137,7 +161,9 @@ def gemm_entries(in_dtype: str, A: np.ndarray, B: np.ndarray, C: np.ndarray | No
                  M: int, N: int, K: int, lda: int, ldb: int, ldc: int,
                  layoutA: str = "row", layoutB: str = "row", out_dtype: str = "f32",
                  alpha: float = 1.0, beta: float = 0.0, nthreads: int = 1,
-                 lib: ctypes.CDLL | None = None):
+                 lib: ctypes.CDLL | None = None,
+                 bias: np.ndarray | None = None, row_scale: np.ndarray | None = None,
+                 col_scale: np.ndarray | None = None, act: str = "none"):
     """Only the entries (rows[e], cols[e]).  Returns (D_e, V_e, S_e): the
     rounded values (out_dtype storage), the unrounded binary64 values and
     the error scale."""
@@ -145,15 +171,17 @@ def gemm_entries(in_dtype: str, A: np.ndarray, B: np.ndarray, C: np.ndarray | No
     A = _in_bits(A)
     B = _in_bits(B)
     Cc = _c_array(C, out_dtype)
+    bv, rv, cv = _vec(bias, N, "bias"), _vec(row_scale, M, "row_scale"), _vec(col_scale, N, "col_scale")
     ii = np.ascontiguousarray(rows, dtype=np.int64)
     jj = np.ascontiguousarray(cols, dtype=np.int64)
     n = ii.size
     V = np.zeros(n, dtype=np.float64)
     S = np.zeros(n, dtype=np.float64)
-    rc = lib.oracle_gemm_entries(_DT[in_dtype], _ptr(A), _ptr(B), _ptr(Cc), _ptr(ii), _ptr(jj), n,
-                                 _ptr(V), _ptr(S), M, N, K, lda, ldb, ldc,
-                                 _LAYOUT[layoutA], _LAYOUT[layoutB], _DT[out_dtype],
-                                 float(alpha), float(beta), int(nthreads))
+    rc = lib.oracle_gemm_entries_ep(_DT[in_dtype], _ptr(A), _ptr(B), _ptr(Cc), _ptr(ii), _ptr(jj), n,
+                                    _ptr(V), _ptr(S), M, N, K, lda, ldb, ldc,
+                                    _LAYOUT[layoutA], _LAYOUT[layoutB], _DT[out_dtype],
+                                    float(alpha), float(beta), _ptr(bv), _ptr(rv), _ptr(cv), ACT[act],
+                                    int(nthreads))
     if rc != 0:
         raise ValueError("oracle_gemm_entries rejected its arguments")
     return round_to(V, out_dtype, lib=lib), V, S

@@ -39,6 +39,19 @@
  *
  * Threads only split the set of output rows (or sampled entries); the
  * arithmetic of each element is the single-accumulator loop above.
+ *
+ * Fused epilogue (the *_ep entry points).  The pages list epilogue fusion
+ * -- bias, activation and scale applied before the write-back -- among the
+ * standard GEMM optimisations ("矩阵乘法优化可视化学习文档", section 6, the
+ * "Epilogue fusion" row, and section 8, the store step of the Triton
+ * kernel) without fixing a formula.  The reading taken here:
+ *     U[i,j] = alpha * r[i] * c[j] * sum_k A[i,k] B[k,j] + beta * C[i,j] + bias[j]
+ *     D[i,j] = act(U[i,j])
+ * with r (per-row scale), c (per-column scale) and bias given as float32
+ * vectors (1, 1 and 0 when absent), act = identity, ReLU(u) = max(u, 0) or
+ * GELU(u) = u * Phi(u) = u/2 * (1 + erf(u / sqrt 2)) (the exact form, erf
+ * from the C library in binary64).  S becomes the error scale of U:
+ * |alpha r c| * sum |A B| + |beta C| + |bias|.
  */
 #include <math.h>
 #include <pthread.h>
@@ -139,7 +152,14 @@ typedef struct {
     int layoutA, layoutB;       /* OR_ROW / OR_COL */
     int out_dtype;              /* OR_F16 / OR_BF16 / OR_F32 */
     double alpha, beta;
+    /* fused epilogue (all optional) */
+    const float *bias;          /* N, added per column */
+    const float *row_scale;     /* M, multiplies row i of alpha * A * B */
+    const float *col_scale;     /* N, multiplies column j of alpha * A * B */
+    int act;                    /* OR_ACT_* */
 } gemm_args;
+
+enum { OR_ACT_NONE = 0, OR_ACT_RELU = 1, OR_ACT_GELU = 2 };
 
 static double decode_in(int dt, uint16_t h)
 {
@@ -181,11 +201,25 @@ static void element(const gemm_args *g, int64_t i, int64_t j, double *v_out, dou
     }
     double v = g->alpha * acc;
     double s = fabs(g->alpha) * sabs;
+    if (g->row_scale || g->col_scale) {
+        double sc = (g->row_scale ? (double)g->row_scale[i] : 1.0) *
+                    (g->col_scale ? (double)g->col_scale[j] : 1.0);
+        v *= sc;
+        s *= fabs(sc);
+    }
     if (g->beta != 0.0) {
         double c = c_at(g, i, j);
         v += g->beta * c;
         s += fabs(g->beta * c);
     }
+    if (g->bias) {
+        v += (double)g->bias[j];
+        s += fabs((double)g->bias[j]);
+    }
+    if (g->act == OR_ACT_RELU)
+        v = v > 0.0 ? v : 0.0;
+    else if (g->act == OR_ACT_GELU)
+        v = 0.5 * v * (1.0 + erf(v / sqrt(2.0)));
     *v_out = v;
     *s_out = s;
 }
@@ -253,6 +287,8 @@ static int check(const gemm_args *g)
         return 1;
     if (g->beta != 0.0 && !g->C && g->M > 0 && g->N > 0)
         return 1;
+    if (g->act != OR_ACT_NONE && g->act != OR_ACT_RELU && g->act != OR_ACT_GELU)
+        return 1;
     return 0;
 }
 
@@ -267,16 +303,17 @@ static int clamp_threads(int nthreads, int64_t units)
     return nthreads;
 }
 
-/* Full product.  D (ldd), V and S may each be NULL.  Rows [0, M) are split
- * over `nthreads` threads.  Returns 0 on success. */
-int oracle_gemm(int in_dtype, const uint16_t *A, const uint16_t *B, const void *C,
-                void *D, int64_t ldd, double *V, double *S,
-                int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
-                int layoutA, int layoutB, int out_dtype, double alpha, double beta,
-                int nthreads)
+/* Full product with the fused epilogue.  D (ldd), V and S may each be NULL.
+ * Rows [0, M) are split over `nthreads` threads.  Returns 0 on success. */
+int oracle_gemm_ep(int in_dtype, const uint16_t *A, const uint16_t *B, const void *C,
+                   void *D, int64_t ldd, double *V, double *S,
+                   int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
+                   int layoutA, int layoutB, int out_dtype, double alpha, double beta,
+                   const float *bias, const float *row_scale, const float *col_scale, int act,
+                   int nthreads)
 {
     gemm_args g = {in_dtype, A, B, C, M, N, K, lda, ldb, ldc, layoutA, layoutB,
-                   out_dtype, alpha, beta};
+                   out_dtype, alpha, beta, bias, row_scale, col_scale, act};
     if (check(&g))
         return 1;
     int nt = clamp_threads(nthreads, M);
@@ -300,16 +337,28 @@ int oracle_gemm(int in_dtype, const uint16_t *A, const uint16_t *B, const void *
     return 0;
 }
 
-/* Selected entries (ii[e], jj[e]) only: unrounded V and the error scale S. */
-int oracle_gemm_entries(int in_dtype, const uint16_t *A, const uint16_t *B, const void *C,
-                        const int64_t *ii, const int64_t *jj, int64_t n_entries,
-                        double *V, double *S,
-                        int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
-                        int layoutA, int layoutB, int out_dtype, double alpha, double beta,
-                        int nthreads)
+/* Full product, plain epilogue (D = alpha A B + beta C). */
+int oracle_gemm(int in_dtype, const uint16_t *A, const uint16_t *B, const void *C,
+                void *D, int64_t ldd, double *V, double *S,
+                int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
+                int layoutA, int layoutB, int out_dtype, double alpha, double beta,
+                int nthreads)
+{
+    return oracle_gemm_ep(in_dtype, A, B, C, D, ldd, V, S, M, N, K, lda, ldb, ldc, layoutA, layoutB,
+                          out_dtype, alpha, beta, NULL, NULL, NULL, OR_ACT_NONE, nthreads);
+}
+
+/* Selected entries (ii[e], jj[e]) only, with the fused epilogue: V and S. */
+int oracle_gemm_entries_ep(int in_dtype, const uint16_t *A, const uint16_t *B, const void *C,
+                           const int64_t *ii, const int64_t *jj, int64_t n_entries,
+                           double *V, double *S,
+                           int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
+                           int layoutA, int layoutB, int out_dtype, double alpha, double beta,
+                           const float *bias, const float *row_scale, const float *col_scale, int act,
+                           int nthreads)
 {
     gemm_args g = {in_dtype, A, B, C, M, N, K, lda, ldb, ldc, layoutA, layoutB,
-                   out_dtype, alpha, beta};
+                   out_dtype, alpha, beta, bias, row_scale, col_scale, act};
     if (check(&g))
         return 1;
     for (int64_t e = 0; e < n_entries; ++e)
@@ -334,6 +383,19 @@ int oracle_gemm_entries(int in_dtype, const uint16_t *A, const uint16_t *B, cons
     for (int t = 1; t < nt; ++t)
         pthread_join(th[t], NULL);
     return 0;
+}
+
+/* Selected entries, plain epilogue. */
+int oracle_gemm_entries(int in_dtype, const uint16_t *A, const uint16_t *B, const void *C,
+                        const int64_t *ii, const int64_t *jj, int64_t n_entries,
+                        double *V, double *S,
+                        int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
+                        int layoutA, int layoutB, int out_dtype, double alpha, double beta,
+                        int nthreads)
+{
+    return oracle_gemm_entries_ep(in_dtype, A, B, C, ii, jj, n_entries, V, S, M, N, K, lda, ldb, ldc,
+                                  layoutA, layoutB, out_dtype, alpha, beta, NULL, NULL, NULL, OR_ACT_NONE,
+                                  nthreads);
 }
 
 /* Round n binary64 values once, RNE, to out_dtype (for sampled entries). */

@@ -369,4 +369,83 @@ def pin_entries_match_full(lib):
     assert np.array_equal(De, D[ii, jj])
 
 
+# --------------------------------------------------------------------------
+# Fused-epilogue pins (bias[N], row_scale[M], col_scale[N], ReLU / GELU)
+# --------------------------------------------------------------------------
+
+def _ep_identity(lib, Bvals, act="none", bias=None, row_scale=None, col_scale=None, C=None, beta=0.0):
+    """A = I (K x K), so U = rs[i] cs[j] B[i,j] + beta C[i,j] + bias[j] with no
+    rounding before the epilogue; returns V (after the activation) and S."""
+    K, N = Bvals.shape
+    A = _f16_bits(np.eye(K))
+    B = _f16_bits(Bvals)
+    Cb = None if C is None else np.ascontiguousarray(C, dtype=np.float32)
+    f32 = lambda v: None if v is None else np.ascontiguousarray(v, dtype=np.float32)
+    D, V, S = oracle.gemm("f16", A, B, Cb, K, N, K, K, N, N, "row", "row", "f32", 1.0, beta,
+                          want_exact=True, lib=lib, bias=f32(bias), row_scale=f32(row_scale),
+                          col_scale=f32(col_scale), act=act)
+    return V, S
+
+
+def pin_gelu_against_normal_cdf(lib):
+    """GELU(x) = x * Phi(x): checked against scipy's normal CDF (an
+    independent routine) on fp16-exact points, and GELU(0) = 0 exactly."""
+    from scipy.stats import norm
+    x = np.array([[0.0, 1.0, -1.0, 2.0, -2.0, 0.5, -0.5, 3.0],
+                  [8.0, -8.0, 0.125, -0.125, 1.5, -1.5, 4.0, -4.0]])
+    V, _ = _ep_identity(lib, x, act="gelu")
+    assert V[0, 0] == 0.0
+    assert np.allclose(V, x * norm.cdf(x), rtol=1e-13, atol=1e-15)
+    assert abs(V[0, 1] - 0.8413447460685429) < 1e-15          # Phi(1)
+
+
+def pin_gelu_odd_part_is_identity(lib):
+    """GELU(u) - GELU(-u) = u Phi(u) + u Phi(-u) = u for every u."""
+    rng = np.random.default_rng(21)
+    x = np.round(rng.uniform(-6, 6, (4, 16)) * 64) / 64
+    Vp, _ = _ep_identity(lib, x, act="gelu")
+    Vn, _ = _ep_identity(lib, -x, act="gelu")
+    assert np.allclose(Vp - Vn, x, rtol=0, atol=1e-14)
+
+
+def pin_relu(lib):
+    """ReLU keeps positives, zeroes negatives; ReLU(u) - ReLU(-u) = u."""
+    x = np.array([[3.0, -3.0, 0.0, 0.25], [-0.25, 7.0, -7.0, 1.0]])
+    V, _ = _ep_identity(lib, x, act="relu")
+    assert np.array_equal(V, np.where(x > 0, x, 0.0))
+    Vn, _ = _ep_identity(lib, -x, act="relu")
+    assert np.array_equal(V - Vn, x)
+
+
+def pin_bias_is_per_column(lib):
+    """With B = 0 the result is the bias of each column, in every row."""
+    bias = np.array([1.5, -2.0, 0.25, 3.0, -0.5], dtype=np.float32)
+    V, S = _ep_identity(lib, np.zeros((3, 5)), bias=bias)
+    assert np.array_equal(V, np.tile(bias.astype(np.float64), (3, 1)))
+    assert np.array_equal(S, np.tile(np.abs(bias.astype(np.float64)), (3, 1)))
+
+
+def pin_scales_row_and_column(lib):
+    """Row i of alpha*A*B is multiplied by row_scale[i] and column j by
+    col_scale[j]; beta*C and the bias are not scaled (non-square, so a
+    swapped row/column index shows)."""
+    rng = np.random.default_rng(22)
+    x = rng.integers(-3, 4, (3, 5)).astype(np.float64)
+    C = rng.integers(-3, 4, (3, 5)).astype(np.float32)
+    rs = np.array([2.0, 0.5, -4.0], dtype=np.float32)
+    cs = np.array([1.0, 8.0, 0.25, -2.0, 0.5], dtype=np.float32)
+    bias = np.array([1.0, -1.0, 2.0, 0.0, 0.5], dtype=np.float32)
+    V, S = _ep_identity(lib, x, bias=bias, row_scale=rs, col_scale=cs, C=C, beta=1.0)
+    want = rs[:, None].astype(np.float64) * cs[None, :] * x + C + bias[None, :]
+    assert np.array_equal(V, want)
+    assert np.array_equal(S, np.abs(rs[:, None].astype(np.float64) * cs[None, :] * x) + np.abs(C) + np.abs(bias))
+
+
+def pin_activation_after_bias(lib):
+    """The activation sees the biased value: ReLU(-1 + 2) = 1, ReLU(1 - 2) = 0."""
+    x = np.array([[-1.0, 1.0]])
+    V, _ = _ep_identity(lib, x, act="relu", bias=np.array([2.0, -2.0], dtype=np.float32))
+    assert np.array_equal(V, np.array([[1.0, 0.0]]))
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -34,6 +34,14 @@ MUTANTS = {
     "scale_without_abs": ("sabs += fabs(p);", "sabs += p;"),
     "scale_without_alpha": ("double s = fabs(g->alpha) * sabs;", "double s = sabs;"),
     "beta_read_when_zero": ("if (g->beta != 0.0) {", "if (g->C) {"),
+    "bias_per_row": ("v += (double)g->bias[j];", "v += (double)g->bias[i % g->N];"),
+    "bias_dropped": ("v += (double)g->bias[j];", "v += 0.0;"),
+    "col_scale_by_row": ("(g->col_scale ? (double)g->col_scale[j] : 1.0)", "(g->col_scale ? (double)g->col_scale[i % g->N] : 1.0)"),
+    "scale_squared": ("v *= sc;", "v *= sc * sc;"),
+    "gelu_tanh_approximation": ("v = 0.5 * v * (1.0 + erf(v / sqrt(2.0)));",
+                                "v = 0.5 * v * (1.0 + tanh(0.7978845608028654 * (v + 0.044715 * v * v * v)));"),
+    "relu_as_abs": ("v = v > 0.0 ? v : 0.0;", "v = fabs(v);"),
+    "activation_ignored": ("if (g->act == OR_ACT_RELU)", "if (0)"),
 }
 
 
