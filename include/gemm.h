@@ -92,6 +92,37 @@ gemm_status_t gemm_run(gemm_plan_t plan, const void *A, const void *B, const voi
                        gemm_dtype_t accum_dtype, gemm_dtype_t out_dtype,
                        float alpha, float beta, void *stream);
 
+/* Fused epilogue ("矩阵乘法优化可视化学习文档", section 6, the "Epilogue
+ * fusion" row: bias, activation and scale applied in the GEMM before the
+ * write-back; section 8, the store step).  With it, gemm_run_ep computes
+ *
+ *     U[i,j] = alpha * row_scale[i] * col_scale[j] * sum_k A[i,k] B[k,j]
+ *              + beta * C[i,j] + bias[j]
+ *     D[i,j] = act(U[i,j])
+ *
+ * in fp32 before the single RNE cast to the output type.  Each vector is a
+ * DEVICE array of fp32 owned by the caller (read only during the call's
+ * kernels), or NULL: row_scale has M entries (NULL: 1), col_scale and bias
+ * N entries (NULL: 1 and 0).  act: GEMM_ACT_NONE (identity), GEMM_ACT_RELU
+ * (max(u, 0)) or GEMM_ACT_GELU (u * Phi(u) = u/2 * (1 + erf(u / sqrt 2)),
+ * the exact form, erff in fp32).  With K == 0, D = act(beta * C + bias). */
+typedef enum { GEMM_ACT_NONE = 0, GEMM_ACT_RELU = 1, GEMM_ACT_GELU = 2 } gemm_activation_t;
+
+typedef struct {
+    const float *bias;         /* [N] added to column j, or NULL */
+    const float *row_scale;    /* [M] multiplies row i of alpha*A*B, or NULL */
+    const float *col_scale;    /* [N] multiplies column j of alpha*A*B, or NULL */
+    gemm_activation_t act;
+} gemm_epilogue_t;
+
+/* gemm_run with a fused epilogue; ep == NULL is exactly gemm_run.  An act
+ * value outside the enum returns GEMM_ERR_INVALID_ARG. */
+gemm_status_t gemm_run_ep(gemm_plan_t plan, const void *A, const void *B, const void *C, void *D,
+                          int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
+                          gemm_layout_t layoutA, gemm_layout_t layoutB,
+                          gemm_dtype_t accum_dtype, gemm_dtype_t out_dtype,
+                          float alpha, float beta, const gemm_epilogue_t *ep, void *stream);
+
 /* The host-side argument checks of gemm_run, without a plan or a device:
  * returns the status gemm_run would return before launching anything. */
 gemm_status_t gemm_validate(gemm_dtype_t in_dtype, const void *A, const void *B, const void *C,

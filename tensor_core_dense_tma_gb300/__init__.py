@@ -51,12 +51,24 @@ class GemmError(RuntimeError):
         super().__init__(f"{what}: {STATUS.get(status, status)}" if what else STATUS.get(status, str(status)))
 
 
+ACT = {"none": 0, "relu": 1, "gelu": 2}
+
+
+class Epilogue(ctypes.Structure):
+    """gemm_epilogue_t: device pointers (or None) and the activation code."""
+    _fields_ = [("bias", ctypes.c_void_p), ("row_scale", ctypes.c_void_p), ("col_scale", ctypes.c_void_p),
+                ("act", ctypes.c_int)]
+
+
 def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     p, i64, i32, u64, f32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_uint64, ctypes.c_float
     lib.gemm_plan_create.argtypes = [ctypes.POINTER(p), i32, i32]
     lib.gemm_plan_create.restype = i32
     lib.gemm_run.argtypes = [p, p, p, p, p, i64, i64, i64, i64, i64, i64, i32, i32, i32, i32, f32, f32, p]
     lib.gemm_run.restype = i32
+    lib.gemm_run_ep.argtypes = [p, p, p, p, p, i64, i64, i64, i64, i64, i64, i32, i32, i32, i32, f32, f32,
+                                ctypes.POINTER(Epilogue), p]
+    lib.gemm_run_ep.restype = i32
     lib.gemm_validate.argtypes = [i32, p, p, p, p, i64, i64, i64, i64, i64, i64, i32, i32, i32, i32, f32]
     lib.gemm_validate.restype = i32
     lib.gemm_plan_device_status.argtypes = [p, i32]
@@ -125,6 +137,13 @@ def gemm_run(plan, A, B, C, D, M, N, K, lda, ldb, ldc, layoutA, layoutB, accum_d
              alpha, beta, stream) -> int:
     return load().gemm_run(plan, A, B, C, D, M, N, K, lda, ldb, ldc, LAYOUT[layoutA], LAYOUT[layoutB],
                            DTYPE[accum_dtype], DTYPE[out_dtype], alpha, beta, stream)
+
+
+def gemm_run_ep(plan, A, B, C, D, M, N, K, lda, ldb, ldc, layoutA, layoutB, accum_dtype, out_dtype,
+                alpha, beta, ep: Epilogue | None, stream) -> int:
+    return load().gemm_run_ep(plan, A, B, C, D, M, N, K, lda, ldb, ldc, LAYOUT[layoutA], LAYOUT[layoutB],
+                              DTYPE[accum_dtype], DTYPE[out_dtype], alpha, beta,
+                              ctypes.byref(ep) if ep is not None else None, stream)
 
 
 def gemm_validate(in_dtype, A, B, C, D, M, N, K, lda, ldb, ldc, layoutA, layoutB, accum_dtype,
@@ -288,17 +307,25 @@ class Plan:
         return gemm_plan_describe(self.handle, M, N, K, layoutA, layoutB, accum_dtype, out_dtype)
 
     def run_raw(self, A_ptr, B_ptr, C_ptr, D_ptr, M, N, K, lda, ldb, ldc, layoutA, layoutB,
-                accum_dtype, out_dtype, alpha=1.0, beta=0.0, stream=None) -> None:
-        """gemm_run on raw device addresses; raises GemmError on a bad status."""
-        st = gemm_run(self.handle, A_ptr, B_ptr, C_ptr, D_ptr, M, N, K, lda, ldb, ldc, layoutA, layoutB,
-                      accum_dtype, out_dtype, float(alpha), float(beta), stream)
+                accum_dtype, out_dtype, alpha=1.0, beta=0.0, stream=None, ep: "Epilogue | None" = None) -> None:
+        """gemm_run (gemm_run_ep with an epilogue) on raw device addresses;
+        raises GemmError on a bad status."""
+        if ep is None:
+            st = gemm_run(self.handle, A_ptr, B_ptr, C_ptr, D_ptr, M, N, K, lda, ldb, ldc, layoutA, layoutB,
+                          accum_dtype, out_dtype, float(alpha), float(beta), stream)
+        else:
+            st = gemm_run_ep(self.handle, A_ptr, B_ptr, C_ptr, D_ptr, M, N, K, lda, ldb, ldc, layoutA, layoutB,
+                             accum_dtype, out_dtype, float(alpha), float(beta), ep, stream)
         if st != 0:
             raise GemmError(st, "gemm_run")
 
     def gemm(self, A, B, C=None, D=None, *, alpha: float = 1.0, beta: float = 0.0,
-             accum_dtype: str = "f32", out_dtype: str | None = None, stream=None):
-        """D = alpha*A@B + beta*C on device tensors; returns D (allocated if
-        not given).  Layouts and leading dimensions come from the strides."""
+             accum_dtype: str = "f32", out_dtype: str | None = None, stream=None,
+             bias=None, row_scale=None, col_scale=None, act: str = "none"):
+        """D = act(alpha * rs[i] * cs[j] * (A@B) + beta*C + bias[j]) on device
+        tensors (the epilogue terms are optional fp32 device vectors; see
+        gemm_epilogue_t); returns D (allocated if not given).  Layouts and
+        leading dimensions come from the strides."""
         import torch
         M, K = A.shape
         K2, N = B.shape
@@ -322,8 +349,18 @@ class Plan:
                 raise ValueError("C must have the output type")
         if stream is None:
             stream = torch.cuda.current_stream(A.device).cuda_stream
+        ep = None
+        if bias is not None or row_scale is not None or col_scale is not None or act != "none":
+            def vec(v, n, what):
+                if v is None:
+                    return None
+                if v.dtype != torch.float32 or v.dim() != 1 or v.shape[0] != n or not v.is_cuda or v.stride(0) != 1:
+                    raise ValueError(f"{what} must be a contiguous fp32 device vector of length {n}")
+                return v.data_ptr()
+            ep = Epilogue(vec(bias, N, "bias"), vec(row_scale, M, "row_scale"), vec(col_scale, N, "col_scale"),
+                          ACT[act])
         self.run_raw(A.data_ptr(), B.data_ptr(), C.data_ptr() if C is not None else None, D.data_ptr(),
-                     M, N, K, lda, ldb, max(ldc, N), la, lb, accum_dtype, out_dtype, alpha, beta, stream)
+                     M, N, K, lda, ldb, max(ldc, N), la, lb, accum_dtype, out_dtype, alpha, beta, stream, ep=ep)
         return D
 
     def gemm_host(self, A, B, C=None, D=None, *, alpha: float = 1.0, beta: float = 0.0,

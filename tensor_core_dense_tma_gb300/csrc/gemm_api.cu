@@ -88,10 +88,19 @@ struct DeviceGuard {
 
 // The problem the kernel computes (see Problem).
 Problem make_problem(bool swap, const void* A, const void* B, int64_t M, int64_t N, int64_t K, int64_t lda,
-                     int64_t ldb, gemm_layout_t la, gemm_layout_t lb) {
+                     int64_t ldb, gemm_layout_t la, gemm_layout_t lb, const gemm_epilogue_t* ep = nullptr) {
     auto flip = [](gemm_layout_t l) { return l == GEMM_ROW_MAJOR ? GEMM_COL_MAJOR : GEMM_ROW_MAJOR; };
-    if (!swap) return Problem{false, A, B, M, N, K, lda, ldb, la, lb};
-    return Problem{true, B, A, N, M, K, ldb, lda, flip(lb), flip(la)};
+    Problem pr = !swap ? Problem{false, A, B, M, N, K, lda, ldb, la, lb}
+                       : Problem{true, B, A, N, M, K, ldb, lda, flip(lb), flip(la)};
+    if (ep) {
+        // D^T = B^T A^T: the kernel's rows are D's columns
+        pr.act = static_cast<uint32_t>(ep->act);
+        pr.rs_row = swap ? ep->col_scale : ep->row_scale;
+        pr.cs_col = swap ? ep->row_scale : ep->col_scale;
+        pr.bias_row = swap ? ep->bias : nullptr;
+        pr.bias_col = swap ? nullptr : ep->bias;
+    }
+    return pr;
 }
 
 int default_units(const gemm_plan* plan, int kind) {
@@ -245,14 +254,19 @@ gemm_status_t prepare_all(gemm_plan* plan) {
 }
 
 gemm_status_t launch_scale(gemm_plan* plan, const void* C, void* D, int64_t M, int64_t N, int64_t ldc,
-                           gemm_dtype_t out, float beta, cudaStream_t stream) {
+                           gemm_dtype_t out, float beta, cudaStream_t stream, const gemm_epilogue_t* ep = nullptr) {
     const int64_t total = M * N;
     int64_t blocks = (total + 255) / 256;
     if (blocks > 4LL * plan->sm_count) blocks = 4LL * plan->sm_count;
     const int32_t m = static_cast<int32_t>(M), n = static_cast<int32_t>(N);
-    if (out == GEMM_F32) tcdt::scale_c_kernel<tcdt::kOutF32><<<blocks, 256, 0, stream>>>(m, n, C, D, ldc, beta);
-    else if (out == GEMM_F16) tcdt::scale_c_kernel<tcdt::kOutF16><<<blocks, 256, 0, stream>>>(m, n, C, D, ldc, beta);
-    else tcdt::scale_c_kernel<tcdt::kOutBF16><<<blocks, 256, 0, stream>>>(m, n, C, D, ldc, beta);
+    const float* bias = ep ? ep->bias : nullptr;
+    const uint32_t act = ep ? static_cast<uint32_t>(ep->act) : 0u;
+    if (out == GEMM_F32)
+        tcdt::scale_c_kernel<tcdt::kOutF32><<<blocks, 256, 0, stream>>>(m, n, C, D, ldc, beta, bias, act);
+    else if (out == GEMM_F16)
+        tcdt::scale_c_kernel<tcdt::kOutF16><<<blocks, 256, 0, stream>>>(m, n, C, D, ldc, beta, bias, act);
+    else
+        tcdt::scale_c_kernel<tcdt::kOutBF16><<<blocks, 256, 0, stream>>>(m, n, C, D, ldc, beta, bias, act);
     if (cudaGetLastError() != cudaSuccess) return GEMM_ERR_CUDA;
     ++plan->launches;
     return GEMM_OK;
@@ -339,20 +353,39 @@ gemm_status_t gemm_run(gemm_plan_t plan, const void* A, const void* B, const voi
                        int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc, gemm_layout_t layoutA,
                        gemm_layout_t layoutB, gemm_dtype_t accum_dtype, gemm_dtype_t out_dtype, float alpha,
                        float beta, void* stream) {
+    return gemm_run_ep(plan, A, B, C, D, M, N, K, lda, ldb, ldc, layoutA, layoutB, accum_dtype, out_dtype,
+                       alpha, beta, nullptr, stream);
+}
+
+gemm_status_t gemm_run_ep(gemm_plan_t plan, const void* A, const void* B, const void* C, void* D, int64_t M,
+                          int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc, gemm_layout_t layoutA,
+                          gemm_layout_t layoutB, gemm_dtype_t accum_dtype, gemm_dtype_t out_dtype, float alpha,
+                          float beta, const gemm_epilogue_t* ep, void* stream) {
     if (!plan) return GEMM_ERR_INVALID_ARG;
     gemm_status_t st = validate(plan->in_dtype, A, B, C, D, M, N, K, lda, ldb, ldc, layoutA, layoutB,
                                 accum_dtype, out_dtype, beta, true);
     if (st != GEMM_OK) return st;
+    if (ep && (static_cast<int>(ep->act) < 0 || static_cast<int>(ep->act) > 2)) return GEMM_ERR_INVALID_ARG;
+    if (ep && !ep->bias && !ep->row_scale && !ep->col_scale && ep->act == GEMM_ACT_NONE) ep = nullptr;
     if (M == 0 || N == 0) return GEMM_OK;
     DeviceGuard guard(plan->device);
     if (!guard.ok) return GEMM_ERR_CUDA;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (K == 0) return launch_scale(plan, C, D, M, N, ldc, out_dtype, beta, s);
+    if (K == 0) return launch_scale(plan, C, D, M, N, ldc, out_dtype, beta, s, ep);
     bool valid = true;
     const Choice ch = choose(plan, M, N, K, accum_dtype, layoutB == GEMM_ROW_MAJOR, &valid);
     if (!valid) return GEMM_ERR_UNSUPPORTED;
-    const Problem pr = make_problem(ch.swap, A, B, M, N, K, lda, ldb, layoutA, layoutB);
+    const Problem pr = make_problem(ch.swap, A, B, M, N, K, lda, ldb, layoutA, layoutB, ep);
     const int slot = out_slot(accum_dtype, out_dtype);
+    if (ep) {
+        switch (ch.kind) {
+            case kCfgSingle16: return launch_single16_ep(plan, slot, ch, pr, C, D, ldc, alpha, beta, s);
+            case kCfgSingle64: return launch_single64_ep(plan, slot, ch, pr, C, D, ldc, alpha, beta, s);
+            case kCfgSingle256: return launch_single256_ep(plan, slot, ch, pr, C, D, ldc, alpha, beta, s);
+            case kCfgPair224: return launch_pair224_ep(plan, slot, ch, pr, C, D, ldc, alpha, beta, s);
+            default: return launch_pair256_ep(plan, slot, ch, pr, C, D, ldc, alpha, beta, s);
+        }
+    }
     switch (ch.kind) {
         case kCfgSingle16: return launch_single16(plan, slot, ch, pr, C, D, ldc, alpha, beta, s);
         case kCfgSingle64: return launch_single64(plan, slot, ch, pr, C, D, ldc, alpha, beta, s);

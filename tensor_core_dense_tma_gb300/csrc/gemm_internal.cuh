@@ -80,7 +80,7 @@ struct gemm_plan {
     uint64_t timeout_ns = 2000000000ull;
     uint64_t launches = 0;
     tcdt_host::EncodeTiledFn encode = nullptr;
-    bool attr_set[tcdt_host::kNumCfgKinds][4] = {};
+    bool attr_set[tcdt_host::kNumCfgKinds][8] = {};   // [kind][output slot + 4 * fused epilogue]
     int units[tcdt_host::kNumCfgKinds] = {};  // co-resident CTAs (single) or CTA pairs (pair)
     size_t ws_bytes = 0;          // capacity of d_ws
     int forced_kind = -1;         // gemm_plan_force_config
@@ -100,6 +100,10 @@ struct Problem {
     const void *A, *B;
     int64_t M, N, K, lda, ldb;
     gemm_layout_t la, lb;
+    // fused epilogue in the coordinates of the product the kernel computes
+    // (rows and columns swapped with the operands when `swap`)
+    uint32_t act = 0;
+    const float *rs_row = nullptr, *cs_col = nullptr, *bias_row = nullptr, *bias_col = nullptr;
 };
 
 struct Choice {
@@ -113,11 +117,16 @@ struct Choice {
     int units = 0;
 };
 
-// Per-configuration entry points (one translation unit each).
+// Per-configuration entry points: the kernels without the fused epilogue in
+// one translation unit, those with it (the _ep entry points) in another, so
+// that all compile in parallel and the plain kernels' code is not affected.
 #define TCDT_DECLARE_KIND(name)                                                                          \
     gemm_status_t prepare_##name(gemm_plan* plan, int slot);                                             \
     gemm_status_t launch_##name(gemm_plan* plan, int slot, const Choice& ch, const Problem& pr,          \
-                                const void* C, void* D, int64_t ldc, float alpha, float beta, cudaStream_t s);
+                                const void* C, void* D, int64_t ldc, float alpha, float beta, cudaStream_t s); \
+    gemm_status_t launch_##name##_ep(gemm_plan* plan, int slot, const Choice& ch, const Problem& pr,     \
+                                     const void* C, void* D, int64_t ldc, float alpha, float beta,       \
+                                     cudaStream_t s);
 TCDT_DECLARE_KIND(single16)
 TCDT_DECLARE_KIND(single64)
 TCDT_DECLARE_KIND(single256)
@@ -174,10 +183,10 @@ void fill_launch_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr, cuda
 }
 
 // Shared-memory opt-in and co-residency of one kernel instantiation.
-template <class Cfg>
+template <class Cfg, bool EP = false>
 gemm_status_t prepare(gemm_plan* plan, int kind, int slot) {
-    if (plan->attr_set[kind][slot]) return GEMM_OK;
-    auto kern = tcdt::gemm_sm103_kernel<Cfg>;
+    if (plan->attr_set[kind][slot + (EP ? 4 : 0)]) return GEMM_OK;
+    auto kern = tcdt::gemm_sm103_kernel<Cfg, EP>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES) != cudaSuccess) {
         cudaGetLastError();
         return GEMM_ERR_CUDA;
@@ -198,11 +207,11 @@ gemm_status_t prepare(gemm_plan* plan, int kind, int slot) {
     cudaGetLastError();
     if (units <= 0) units = plan->sm_count / Cfg::CG;
     if (plan->units[kind] == 0 || units < plan->units[kind]) plan->units[kind] = units;
-    plan->attr_set[kind][slot] = true;
+    plan->attr_set[kind][slot + (EP ? 4 : 0)] = true;
     return GEMM_OK;
 }
 
-template <class Cfg>
+template <class Cfg, bool EP = false>
 gemm_status_t launch_tc(gemm_plan* plan, const Choice& ch, const Problem& pr, const void* C, void* D,
                         int64_t ldc, float alpha, float beta, gemm_dtype_t out_dtype, cudaStream_t stream) {
     const bool a_mn = pr.la == GEMM_COL_MAJOR;   // column-major A is M-contiguous
@@ -266,6 +275,12 @@ gemm_status_t launch_tc(gemm_plan* plan, const Choice& ch, const Problem& pr, co
     p.b_mn_major = b_mn;
     p.trans_out = pr.swap ? 1u : 0u;
     p.d_tma = d_tma ? 1u : 0u;
+    p.act = pr.act;
+    p.rs_row = pr.rs_row;
+    p.cs_col = pr.cs_col;
+    p.bias_row = pr.bias_row;
+    p.bias_col = pr.bias_col;
+    p.ep = (pr.act || pr.rs_row || pr.cs_col || pr.bias_row || pr.bias_col) ? 1u : 0u;
     p.ws = plan->d_ws;
     p.counters = plan->d_counters;
     p.early = (ch.early && ch.splits > 1 && plan->d_flags && Cfg::W == 32) ? 1 : 0;
@@ -286,7 +301,7 @@ gemm_status_t launch_tc(gemm_plan* plan, const Choice& ch, const Problem& pr, co
     const int64_t work = p.dp_tiles + static_cast<int64_t>(p.num_tiles - p.dp_tiles) * (n_halves ? 2 : p.splits);
     const int units = work < ch.units ? static_cast<int>(work) : ch.units;
     cfg.gridDim = dim3(Cfg::CG * units, 1, 1);
-    if (cudaLaunchKernelEx(&cfg, tcdt::gemm_sm103_kernel<Cfg>, tmA, tmB, tmBh, tmD, tmW, p) != cudaSuccess) {
+    if (cudaLaunchKernelEx(&cfg, tcdt::gemm_sm103_kernel<Cfg, EP>, tmA, tmB, tmBh, tmD, tmW, p) != cudaSuccess) {
         cudaGetLastError();
         return GEMM_ERR_CUDA;
     }
@@ -294,26 +309,26 @@ gemm_status_t launch_tc(gemm_plan* plan, const Choice& ch, const Problem& pr, co
     return GEMM_OK;
 }
 
-template <template <bool, int> class CfgT>
+template <template <bool, int> class CfgT, bool EP = false>
 gemm_status_t prepare_kind(gemm_plan* plan, int kind, int slot) {
     switch (slot) {
-        case 0: return prepare<CfgT<false, tcdt::kOutF32>>(plan, kind, slot);
-        case 1: return prepare<CfgT<false, tcdt::kOutF16>>(plan, kind, slot);
-        case 2: return prepare<CfgT<false, tcdt::kOutBF16>>(plan, kind, slot);
-        default: return prepare<CfgT<true, tcdt::kOutF16>>(plan, kind, slot);
+        case 0: return prepare<CfgT<false, tcdt::kOutF32>, EP>(plan, kind, slot);
+        case 1: return prepare<CfgT<false, tcdt::kOutF16>, EP>(plan, kind, slot);
+        case 2: return prepare<CfgT<false, tcdt::kOutBF16>, EP>(plan, kind, slot);
+        default: return prepare<CfgT<true, tcdt::kOutF16>, EP>(plan, kind, slot);
     }
 }
 
-template <template <bool, int> class CfgT>
+template <template <bool, int> class CfgT, bool EP = false>
 gemm_status_t launch_kind(gemm_plan* plan, int slot, const Choice& ch, const Problem& pr, const void* C, void* D,
                           int64_t ldc, float alpha, float beta, cudaStream_t s) {
-    gemm_status_t st = prepare_kind<CfgT>(plan, ch.kind, slot);
+    gemm_status_t st = prepare_kind<CfgT, EP>(plan, ch.kind, slot);
     if (st != GEMM_OK) return st;
     switch (slot) {
-        case 0: return launch_tc<CfgT<false, tcdt::kOutF32>>(plan, ch, pr, C, D, ldc, alpha, beta, GEMM_F32, s);
-        case 1: return launch_tc<CfgT<false, tcdt::kOutF16>>(plan, ch, pr, C, D, ldc, alpha, beta, GEMM_F16, s);
-        case 2: return launch_tc<CfgT<false, tcdt::kOutBF16>>(plan, ch, pr, C, D, ldc, alpha, beta, GEMM_BF16, s);
-        default: return launch_tc<CfgT<true, tcdt::kOutF16>>(plan, ch, pr, C, D, ldc, alpha, beta, GEMM_F16, s);
+        case 0: return launch_tc<CfgT<false, tcdt::kOutF32>, EP>(plan, ch, pr, C, D, ldc, alpha, beta, GEMM_F32, s);
+        case 1: return launch_tc<CfgT<false, tcdt::kOutF16>, EP>(plan, ch, pr, C, D, ldc, alpha, beta, GEMM_F16, s);
+        case 2: return launch_tc<CfgT<false, tcdt::kOutBF16>, EP>(plan, ch, pr, C, D, ldc, alpha, beta, GEMM_BF16, s);
+        default: return launch_tc<CfgT<true, tcdt::kOutF16>, EP>(plan, ch, pr, C, D, ldc, alpha, beta, GEMM_F16, s);
     }
 }
 
@@ -323,6 +338,13 @@ gemm_status_t launch_kind(gemm_plan* plan, int slot, const Choice& ch, const Pro
                                 const void* C, void* D, int64_t ldc, float alpha, float beta,            \
                                 cudaStream_t s) {                                                         \
         return launch_kind<CfgT>(plan, slot, ch, pr, C, D, ldc, alpha, beta, s);                        \
+    }
+
+#define TCDT_DEFINE_KIND_EP(name, CfgT)                                                                  \
+    gemm_status_t launch_##name##_ep(gemm_plan* plan, int slot, const Choice& ch, const Problem& pr,     \
+                                     const void* C, void* D, int64_t ldc, float alpha, float beta,       \
+                                     cudaStream_t s) {                                                    \
+        return launch_kind<CfgT, true>(plan, slot, ch, pr, C, D, ldc, alpha, beta, s);                  \
     }
 
 }  // namespace tcdt_host

@@ -78,6 +78,14 @@ struct KernelParams {
     uint32_t b_mn_major;      // 1: B is N-contiguous
     uint32_t trans_out;       // 1: element (r, c) goes to D[c*ldc + r]
     uint32_t d_tma;           // 1: D rows are 16-byte aligned: store D tiles with TMA (tmD)
+    // fused epilogue, in the coordinates of the product the kernel computes
+    // (the host swaps rows and columns for trans_out); all optional
+    uint32_t ep;              // 1: any of the following is set
+    uint32_t act;             // 0 none, 1 ReLU, 2 GELU
+    const float* rs_row;      // [M] scale of row r of the product
+    const float* cs_col;      // [N] scale of column c
+    const float* bias_row;    // [M] added to row r
+    const float* bias_col;    // [N] added to column c
     float* ws;                // split partials, [split tile][split][cta][128][BN] fp32
     int* counters;            // [split tile][cta] split arrivals; zero on entry, left zero
     int32_t early;            // 1: divided tiles use early partials (see unit_item)
@@ -367,6 +375,47 @@ struct Vec {
     static constexpr int ESZ = OUT == kOutF32 ? 4 : 2;
 };
 
+// Fused epilogue ("矩阵乘法优化可视化学习文档", section 6, epilogue fusion:
+// bias, activation and scale applied before the write-back):
+//     x = alpha * (s_row[r] * s_col[c] * acc) + beta * C + bias
+//     D = act(x),  act = identity, ReLU(x) = max(x, 0), GELU(x) = x * Phi(x)
+// ep_scale multiplies the accumulator values of one row segment by the
+// scales (before the alpha/beta step); ep_finish adds the bias and applies
+// the activation (after it).  Vectors are read only inside the product.
+constexpr float kInvSqrt2 = 0.70710678118654752f;
+
+__device__ __forceinline__ float ep_act(uint32_t act, float x) {
+    if (act == 1u) return fmaxf(x, 0.0f);
+    if (act == 2u) return 0.5f * x * (1.0f + erff(x * kInvSqrt2));
+    return x;
+}
+
+template <int W>
+__device__ __forceinline__ void ep_scale(const KernelParams& p, float (&a)[W], int row, int col0) {
+    const float rs = (p.rs_row && row < p.M) ? __ldg(p.rs_row + row) : 1.0f;
+#pragma unroll
+    for (int i = 0; i < W; ++i) {
+        const int col = col0 + i;
+        const float s = (p.cs_col && col < p.N) ? rs * __ldg(p.cs_col + col) : rs;
+        a[i] *= s;
+    }
+}
+
+template <int W>
+__device__ __forceinline__ void ep_finish(const KernelParams& p, float (&v)[W], int row, int col0) {
+    // a missing bias adds nothing (not +0, which would turn a -0 result into +0)
+    const bool has_br = p.bias_row && row < p.M;
+    const float br = has_br ? __ldg(p.bias_row + row) : 0.0f;
+#pragma unroll
+    for (int i = 0; i < W; ++i) {
+        const int col = col0 + i;
+        float x = v[i];
+        if (has_br) x += br;
+        if (p.bias_col && col < p.N) x += __ldg(p.bias_col + col);
+        v[i] = ep_act(p.act, x);
+    }
+}
+
 // 16 bytes of C (one aligned group) into c[i0 .. i0+VEC).
 template <int OUT, int W>
 __device__ __forceinline__ void load_group(const char* ptr, float (&c)[W], int i0) {
@@ -536,78 +585,165 @@ __device__ __forceinline__ void store_d_block(const KernelParams& p, int row0, i
 
 // alpha * acc (+ beta * C) for W consecutive accumulator columns of one
 // accumulator row, written to D (row-major, or transposed with trans_out).
-template <class Cfg>
+template <class Cfg, bool EP>
 __device__ __forceinline__ void epilogue_chunk(const KernelParams& p, const float (&acc)[Cfg::W], int row,
                                                int col0) {
-    constexpr int W = Cfg::W;
-    constexpr int ESZ = Vec<Cfg::OUT>::ESZ;
-    const int n = min(W, p.N - col0);
-    float v[W];
-#pragma unroll
-    for (int i = 0; i < W; ++i) v[i] = p.alpha * acc[i];
-    if (p.trans_out) {
-        // element (row, col0+i) -> D[(col0+i)*ldc + row]; lanes hold consecutive rows
-#pragma unroll
-        for (int i = 0; i < W; ++i)
-            if (i < n) {
-                const int64_t off = static_cast<int64_t>(col0 + i) * p.ldc + row;
-                float x = v[i];
-                if (p.beta != 0.0f) x = fmaf(p.alpha, acc[i], p.beta * load_elem<Cfg::OUT>(p.C, off));
-                store_elem<Cfg::OUT>(p.D, off, x);
+    if constexpr (!EP) {
+        constexpr int W = Cfg::W;
+        constexpr int ESZ = Vec<Cfg::OUT>::ESZ;
+        const int n = min(W, p.N - col0);
+        float v[W];
+    #pragma unroll
+        for (int i = 0; i < W; ++i) v[i] = p.alpha * acc[i];
+        if (p.trans_out) {
+            // element (row, col0+i) -> D[(col0+i)*ldc + row]; lanes hold consecutive rows
+    #pragma unroll
+            for (int i = 0; i < W; ++i)
+                if (i < n) {
+                    const int64_t off = static_cast<int64_t>(col0 + i) * p.ldc + row;
+                    float x = v[i];
+                    if (p.beta != 0.0f) x = fmaf(p.alpha, acc[i], p.beta * load_elem<Cfg::OUT>(p.C, off));
+                    store_elem<Cfg::OUT>(p.D, off, x);
+                }
+            return;
+        }
+        const int64_t off = static_cast<int64_t>(row) * p.ldc + col0;
+        if (p.beta != 0.0f) {
+            float c[W];
+    #pragma unroll
+            for (int i = 0; i < W; ++i) c[i] = 0.0f;
+            row_segment_dispatch<Cfg::OUT, W, false>(
+                const_cast<char*>(static_cast<const char*>(p.C)) + off * ESZ, c, n);
+    #pragma unroll
+            for (int i = 0; i < W; ++i) v[i] = fmaf(p.alpha, acc[i], p.beta * c[i]);
+        }
+        row_segment_dispatch<Cfg::OUT, W, true>(static_cast<char*>(p.D) + off * ESZ, v, n);
+    
+    } else {
+        constexpr int W = Cfg::W;
+        constexpr int ESZ = Vec<Cfg::OUT>::ESZ;
+        const int n = min(W, p.N - col0);
+        float a[W];
+    #pragma unroll
+        for (int i = 0; i < W; ++i) a[i] = acc[i];
+        if (p.ep) ep_scale<W>(p, a, row, col0);
+        float v[W];
+    #pragma unroll
+        for (int i = 0; i < W; ++i) v[i] = p.alpha * a[i];
+        if (p.trans_out) {
+            // element (row, col0+i) -> D[(col0+i)*ldc + row]; lanes hold consecutive rows
+            if (p.beta != 0.0f) {
+    #pragma unroll
+                for (int i = 0; i < W; ++i)
+                    if (i < n)
+                        v[i] = fmaf(p.alpha, a[i],
+                                    p.beta * load_elem<Cfg::OUT>(p.C, static_cast<int64_t>(col0 + i) * p.ldc + row));
             }
-        return;
+            if (p.ep) ep_finish<W>(p, v, row, col0);
+    #pragma unroll
+            for (int i = 0; i < W; ++i)
+                if (i < n) store_elem<Cfg::OUT>(p.D, static_cast<int64_t>(col0 + i) * p.ldc + row, v[i]);
+            return;
+        }
+        const int64_t off = static_cast<int64_t>(row) * p.ldc + col0;
+        if (p.beta != 0.0f) {
+            float c[W];
+    #pragma unroll
+            for (int i = 0; i < W; ++i) c[i] = 0.0f;
+            row_segment_dispatch<Cfg::OUT, W, false>(
+                const_cast<char*>(static_cast<const char*>(p.C)) + off * ESZ, c, n);
+    #pragma unroll
+            for (int i = 0; i < W; ++i) v[i] = fmaf(p.alpha, a[i], p.beta * c[i]);
+        }
+        if (p.ep) ep_finish<W>(p, v, row, col0);
+        row_segment_dispatch<Cfg::OUT, W, true>(static_cast<char*>(p.D) + off * ESZ, v, n);
+    
     }
-    const int64_t off = static_cast<int64_t>(row) * p.ldc + col0;
-    if (p.beta != 0.0f) {
-        float c[W];
-#pragma unroll
-        for (int i = 0; i < W; ++i) c[i] = 0.0f;
-        row_segment_dispatch<Cfg::OUT, W, false>(
-            const_cast<char*>(static_cast<const char*>(p.C)) + off * ESZ, c, n);
-#pragma unroll
-        for (int i = 0; i < W; ++i) v[i] = fmaf(p.alpha, acc[i], p.beta * c[i]);
-    }
-    row_segment_dispatch<Cfg::OUT, W, true>(static_cast<char*>(p.D) + off * ESZ, v, n);
 }
 
 // alpha * acc (+ beta * C) for 4 consecutive columns of one row (used by the
 // split-K reduction, whose threads own consecutive column quads of a row).
-template <class Cfg>
+template <class Cfg, bool EP>
 __device__ __forceinline__ void epilogue_quad(const KernelParams& p, const float4& a, int row, int col) {
-    constexpr int ESZ = Vec<Cfg::OUT>::ESZ;
-    const float acc[4] = {a.x, a.y, a.z, a.w};
-    const int n = min(4, p.N - col);
-    float v[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) v[i] = p.alpha * acc[i];
-    if (p.trans_out) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-            if (i < n) {
-                const int64_t off = static_cast<int64_t>(col + i) * p.ldc + row;
-                float x = v[i];
-                if (p.beta != 0.0f) x = fmaf(p.alpha, acc[i], p.beta * load_elem<Cfg::OUT>(p.C, off));
-                store_elem<Cfg::OUT>(p.D, off, x);
-            }
-        return;
-    }
-    const int64_t off = static_cast<int64_t>(row) * p.ldc + col;
-    if (p.beta != 0.0f) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-            if (i < n) v[i] = fmaf(p.alpha, acc[i], p.beta * load_elem<Cfg::OUT>(p.C, off + i));
-    }
-    char* dp = static_cast<char*>(p.D) + off * ESZ;
-    if (n == 4 && (reinterpret_cast<uintptr_t>(dp) & (4 * ESZ - 1)) == 0) {
-        if constexpr (Cfg::OUT == kOutF32) {
-            *reinterpret_cast<float4*>(dp) = make_float4(v[0], v[1], v[2], v[3]);
-        } else {
-            *reinterpret_cast<uint2*>(dp) = make_uint2(pack2<Cfg::OUT>(v[0], v[1]), pack2<Cfg::OUT>(v[2], v[3]));
+    if constexpr (!EP) {
+        constexpr int ESZ = Vec<Cfg::OUT>::ESZ;
+        const float acc[4] = {a.x, a.y, a.z, a.w};
+        const int n = min(4, p.N - col);
+        float v[4];
+    #pragma unroll
+        for (int i = 0; i < 4; ++i) v[i] = p.alpha * acc[i];
+        if (p.trans_out) {
+    #pragma unroll
+            for (int i = 0; i < 4; ++i)
+                if (i < n) {
+                    const int64_t off = static_cast<int64_t>(col + i) * p.ldc + row;
+                    float x = v[i];
+                    if (p.beta != 0.0f) x = fmaf(p.alpha, acc[i], p.beta * load_elem<Cfg::OUT>(p.C, off));
+                    store_elem<Cfg::OUT>(p.D, off, x);
+                }
+            return;
         }
+        const int64_t off = static_cast<int64_t>(row) * p.ldc + col;
+        if (p.beta != 0.0f) {
+    #pragma unroll
+            for (int i = 0; i < 4; ++i)
+                if (i < n) v[i] = fmaf(p.alpha, acc[i], p.beta * load_elem<Cfg::OUT>(p.C, off + i));
+        }
+        char* dp = static_cast<char*>(p.D) + off * ESZ;
+        if (n == 4 && (reinterpret_cast<uintptr_t>(dp) & (4 * ESZ - 1)) == 0) {
+            if constexpr (Cfg::OUT == kOutF32) {
+                *reinterpret_cast<float4*>(dp) = make_float4(v[0], v[1], v[2], v[3]);
+            } else {
+                *reinterpret_cast<uint2*>(dp) = make_uint2(pack2<Cfg::OUT>(v[0], v[1]), pack2<Cfg::OUT>(v[2], v[3]));
+            }
+        } else {
+    #pragma unroll
+            for (int i = 0; i < 4; ++i)
+                if (i < n) store_elem<Cfg::OUT>(p.D, off + i, v[i]);
+        }
+    
     } else {
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-            if (i < n) store_elem<Cfg::OUT>(p.D, off + i, v[i]);
+        constexpr int ESZ = Vec<Cfg::OUT>::ESZ;
+        float acc[4] = {a.x, a.y, a.z, a.w};
+        if (p.ep) ep_scale<4>(p, acc, row, col);
+        const int n = min(4, p.N - col);
+        float v[4];
+    #pragma unroll
+        for (int i = 0; i < 4; ++i) v[i] = p.alpha * acc[i];
+        if (p.trans_out) {
+            if (p.beta != 0.0f) {
+    #pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    if (i < n)
+                        v[i] = fmaf(p.alpha, acc[i],
+                                    p.beta * load_elem<Cfg::OUT>(p.C, static_cast<int64_t>(col + i) * p.ldc + row));
+            }
+            if (p.ep) ep_finish<4>(p, v, row, col);
+    #pragma unroll
+            for (int i = 0; i < 4; ++i)
+                if (i < n) store_elem<Cfg::OUT>(p.D, static_cast<int64_t>(col + i) * p.ldc + row, v[i]);
+            return;
+        }
+        const int64_t off = static_cast<int64_t>(row) * p.ldc + col;
+        if (p.beta != 0.0f) {
+    #pragma unroll
+            for (int i = 0; i < 4; ++i)
+                if (i < n) v[i] = fmaf(p.alpha, acc[i], p.beta * load_elem<Cfg::OUT>(p.C, off + i));
+        }
+        if (p.ep) ep_finish<4>(p, v, row, col);
+        char* dp = static_cast<char*>(p.D) + off * ESZ;
+        if (n == 4 && (reinterpret_cast<uintptr_t>(dp) & (4 * ESZ - 1)) == 0) {
+            if constexpr (Cfg::OUT == kOutF32) {
+                *reinterpret_cast<float4*>(dp) = make_float4(v[0], v[1], v[2], v[3]);
+            } else {
+                *reinterpret_cast<uint2*>(dp) = make_uint2(pack2<Cfg::OUT>(v[0], v[1]), pack2<Cfg::OUT>(v[2], v[3]));
+            }
+        } else {
+    #pragma unroll
+            for (int i = 0; i < 4; ++i)
+                if (i < n) store_elem<Cfg::OUT>(p.D, off + i, v[i]);
+        }
+    
     }
 }
 
@@ -659,7 +795,7 @@ __device__ __forceinline__ void stage_row_and_store(const void* tmap, const uint
 }
 
 // Epilogue values of one segment -> D through the staging buffer.
-template <class Cfg>
+template <class Cfg, bool EP>
 __device__ __forceinline__ void stage_and_store(const KernelParams& p, const void* tmap, float (&v)[32], int row,
                                                 int col0, int row0w, int lane, uint32_t stg, int& sbuf,
                                                 bool row_ok) {
@@ -667,6 +803,9 @@ __device__ __forceinline__ void stage_and_store(const KernelParams& p, const voi
     float acc[32];
 #pragma unroll
     for (int i = 0; i < 32; ++i) acc[i] = v[i];
+    if constexpr (EP) {
+        if (p.ep) ep_scale<32>(p, acc, row, col0);
+    }
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] = p.alpha * acc[i];
     if (p.beta != 0.0f) {
@@ -682,6 +821,9 @@ __device__ __forceinline__ void stage_and_store(const KernelParams& p, const voi
         (void)row;
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] = fmaf(p.alpha, acc[i], p.beta * c[i]);
+    }
+    if constexpr (EP) {
+        if (p.ep) ep_finish<32>(p, v, row, col0);
     }
     if constexpr (Cfg::OUT == kOutF32) {
         uint32_t words[32];
@@ -705,7 +847,7 @@ __device__ __forceinline__ void stage_and_store_f32(const void* tmap, const uint
 // ---------------------------------------------------------------------------
 // the kernel
 // ---------------------------------------------------------------------------
-template <class Cfg>
+template <class Cfg, bool EP = false>
 __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
 gemm_sm103_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                   const __grid_constant__ CUtensorMap tmBh, const __grid_constant__ CUtensorMap tmD,
@@ -1134,7 +1276,7 @@ gemm_sm103_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                             float v[W];
 #pragma unroll
                             for (int i = 0; i < W; ++i) v[i] = acc_value<Cfg::ACC_F16>(r[i]);
-                            stage_and_store<Cfg>(p, &tmD, v, row, col0, row0w, lane, stg, sbuf, row_ok);
+                            stage_and_store<Cfg, EP>(p, &tmD, v, row, col0, row0w, lane, stg, sbuf, row_ok);
                         }
                     }
                 }
@@ -1155,9 +1297,15 @@ gemm_sm103_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                             tmem_ld_row<W>(t_row + W * c, r);
                             tmem_ld_wait();
                             if (row0w >= p.M) continue;   // warp-uniform
+                            float a[W];
+#pragma unroll
+                            for (int i = 0; i < W; ++i) a[i] = acc_value<Cfg::ACC_F16>(r[i]);
+                            if constexpr (EP) {
+                                if (p.ep) ep_scale<W>(p, a, row, col0);
+                            }
                             float v[W];
 #pragma unroll
-                            for (int i = 0; i < W; ++i) v[i] = p.alpha * acc_value<Cfg::ACC_F16>(r[i]);
+                            for (int i = 0; i < W; ++i) v[i] = p.alpha * a[i];
                             const uint32_t cur = stg + static_cast<uint32_t>(c & 1) * 4096u;
                             if (p.beta != 0.0f) {
                                 float cv[W];
@@ -1178,8 +1326,10 @@ gemm_sm103_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                                     load_c_block<Cfg::OUT>(p, row0w, col0, lane, cur, cv);
                                 }
 #pragma unroll
-                                for (int i = 0; i < W; ++i)
-                                    v[i] = fmaf(p.alpha, acc_value<Cfg::ACC_F16>(r[i]), p.beta * cv[i]);
+                                for (int i = 0; i < W; ++i) v[i] = fmaf(p.alpha, a[i], p.beta * cv[i]);
+                            }
+                            if constexpr (EP) {
+                                if (p.ep) ep_finish<W>(p, v, row, col0);
                             }
                             store_d_block<Cfg::OUT>(p, row0w, col0, lane, cur, v);
                         }
@@ -1198,7 +1348,7 @@ gemm_sm103_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                         float acc[W];
 #pragma unroll
                         for (int i = 0; i < W; ++i) acc[i] = acc_value<Cfg::ACC_F16>(r[i]);
-                        epilogue_chunk<Cfg>(p, acc, row, col0);
+                        epilogue_chunk<Cfg, EP>(p, acc, row, col0);
                     }
                 }
             } else {
@@ -1284,7 +1434,7 @@ gemm_sm103_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                             const int r = q / QUADS_PER_ROW;
                             const int col = (q - r * QUADS_PER_ROW) * 4;
                             const int grow = m0 + r, gcol = n0 + col;
-                            if (grow < p.M && gcol < p.N) epilogue_quad<Cfg>(p, acc[j], grow, gcol);
+                            if (grow < p.M && gcol < p.N) epilogue_quad<Cfg, EP>(p, acc[j], grow, gcol);
                         }
                     }
                 }
@@ -1315,16 +1465,18 @@ gemm_sm103_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     }
 }
 
-// D = beta * C (or 0) when K == 0: no product to accumulate.
+// D = act(beta * C + bias) (or act(bias), or 0) when K == 0: no product to accumulate.
 template <int OUT>
-__global__ void scale_c_kernel(int32_t M, int32_t N, const void* C, void* D, int64_t ldc, float beta) {
+__global__ void scale_c_kernel(int32_t M, int32_t N, const void* C, void* D, int64_t ldc, float beta,
+                               const float* bias, uint32_t act) {
     const int64_t total = static_cast<int64_t>(M) * N;
     for (int64_t e = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; e < total;
          e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
         const int64_t i = e / N, j = e % N;
         const int64_t off = i * ldc + j;
-        const float v = beta != 0.0f ? beta * load_elem<OUT>(C, off) : 0.0f;
-        store_elem<OUT>(D, off, v);
+        float v = beta != 0.0f ? beta * load_elem<OUT>(C, off) : 0.0f;
+        if (bias) v += bias[j];
+        store_elem<OUT>(D, off, ep_act(act, v));
     }
 }
 
