@@ -60,6 +60,8 @@ def parse():
     ap.add_argument("--layoutB", choices=["row", "col"])
     ap.add_argument("--accum", choices=["f32", "f16"])
     ap.add_argument("--out", choices=["f32", "f16", "bf16"])
+    ap.add_argument("--epilogue", choices=["none", "bias", "bias_relu", "bias_gelu", "scale_bias_gelu"],
+                    default="none", help="fused epilogue timed with the GEMM (random fp32 vectors)")
     return ap.parse_args()
 
 
@@ -305,10 +307,21 @@ def main():
     C_l = None if C is None else C[:, :w.N]
     D_l = D[:, :w.N]
     stream = torch.cuda.current_stream(dev)
+    ep = {}
+    if args.epilogue != "none":
+        g = torch.Generator(device="cpu").manual_seed(4242)
+        if "bias" in args.epilogue:
+            ep["bias"] = torch.randn(w.N, generator=g).to(dev)
+        if "scale" in args.epilogue:
+            ep["row_scale"] = (0.5 + torch.rand(w.M, generator=g)).to(dev)
+            ep["col_scale"] = (0.5 + torch.rand(w.N, generator=g)).to(dev)
+        for a in ("relu", "gelu"):
+            if a in args.epilogue:
+                ep["act"] = a
 
     def step():
         plan.gemm(A_l, B_l, C_l, D_l, alpha=w.alpha, beta=w.beta, accum_dtype=w.accum_dtype,
-                  out_dtype=w.out_dtype, stream=stream.cuda_stream)
+                  out_dtype=w.out_dtype, stream=stream.cuda_stream, **ep)
 
     for i in range(args.warmup):
         flush_l2(i)
@@ -427,6 +440,7 @@ def main():
             "pct_of_nominal_dense_fp16": 100.0 * value / world / NOMINAL_DENSE_FP16_TFLOPS,
             "nominal_dense_fp16_tflops": NOMINAL_DENSE_FP16_TFLOPS,
             "kernel_config": plan.describe(w.M, w.N, w.K, w.layoutA, w.layoutB, w.accum_dtype, w.out_dtype),
+            "epilogue": args.epilogue,
             "wall_s_timed_loop": wall,
             "step_ms_min": min(per_step), "step_ms_median": statistics.median(per_step),
         },

@@ -105,7 +105,9 @@ gemm_status_t gemm_run(gemm_plan_t plan, const void *A, const void *B, const voi
  * kernels), or NULL: row_scale has M entries (NULL: 1), col_scale and bias
  * N entries (NULL: 1 and 0).  act: GEMM_ACT_NONE (identity), GEMM_ACT_RELU
  * (max(u, 0)) or GEMM_ACT_GELU (u * Phi(u) = u/2 * (1 + erf(u / sqrt 2)),
- * the exact form, erff in fp32).  With K == 0, D = act(beta * C + bias). */
+ * the exact form; erfc is evaluated in fp32 by Abramowitz & Stegun 7.1.26,
+ * so GELU is within about 1e-7 |u| + 1 ulp of the exact value).  With K == 0,
+ * D = act(beta * C + bias). */
 typedef enum { GEMM_ACT_NONE = 0, GEMM_ACT_RELU = 1, GEMM_ACT_GELU = 2 } gemm_activation_t;
 
 typedef struct {

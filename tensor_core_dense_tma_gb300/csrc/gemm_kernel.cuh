@@ -383,15 +383,54 @@ struct Vec {
 // scales (before the alpha/beta step); ep_finish adds the bias and applies
 // the activation (after it).  Vectors are read only inside the product.
 constexpr float kInvSqrt2 = 0.70710678118654752f;
+// A missing bias adds -0, the identity of fp32 addition (+0 would turn a -0
+// result into +0), so the sums need no test per element.
+constexpr float kNoBias = -0.0f;
 
-__device__ __forceinline__ float ep_act(uint32_t act, float x) {
-    if (act == 1u) return fmaxf(x, 0.0f);
-    if (act == 2u) return 0.5f * x * (1.0f + erff(x * kInvSqrt2));
-    return x;
+// GELU(x) = x * Phi(x) = 0.5 x (1 + erf(x / sqrt 2)), with erfc evaluated by
+// the rational-exponential approximation of Abramowitz & Stegun, Handbook of
+// Mathematical Functions, formula 7.1.26 (Hastings): for z >= 0,
+//     erfc(z) ~ t (a1 + t (a2 + t (a3 + t (a4 + t a5)))) exp(-z^2),  t = 1 / (1 + p z),
+// absolute error at most 1.5e-7.  With q = erfc(|x| / sqrt 2):
+//     x >= 0: GELU = x (1 - q / 2),   x < 0: GELU = x q / 2,
+// so the negative side is formed without the cancellation of 1 + erf.  The
+// reciprocal and exp2 are the hardware approximations (a few ulp); about 14
+// instructions an element where the library erff took about 30, and the
+// epilogue warps share their issue slots with the producer and MMA warps.
+constexpr float kAsP = 0.3275911f * kInvSqrt2;   // p, with z = |x| / sqrt 2 folded in
+constexpr float kAsA1 = 0.254829592f, kAsA2 = -0.284496736f, kAsA3 = 1.421413741f, kAsA4 = -1.453152027f,
+                kAsA5 = 1.061405429f;
+constexpr float kMinusHalfLog2e = -0.72134752044448170f;   // -z^2 = -x^2 / 2, in base 2
+
+__device__ __forceinline__ float ep_gelu(float x) {
+    float t, e;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(t) : "f"(fmaf(fabsf(x), kAsP, 1.0f)));
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(x * x * kMinusHalfLog2e));
+    const float poly = t * fmaf(t, fmaf(t, fmaf(t, fmaf(t, kAsA5, kAsA4), kAsA3), kAsA2), kAsA1);
+    const float q = poly * e;
+    return x * (x >= 0.0f ? fmaf(-0.5f, q, 1.0f) : 0.5f * q);
 }
 
+// The activation over a whole segment: the test on `act` stays outside the
+// element loops, so each activation is one straight run of code (a test per
+// element interleaved the three bodies and the epilogue warps then missed in
+// the instruction cache they share with the producer and MMA warps).
+template <int W>
+__device__ __forceinline__ void ep_act_w(uint32_t act, float (&v)[W]) {
+    if (act == 1u) {
+#pragma unroll
+        for (int i = 0; i < W; ++i) v[i] = fmaxf(v[i], 0.0f);
+    } else if (act == 2u) {
+#pragma unroll
+        for (int i = 0; i < W; ++i) v[i] = ep_gelu(v[i]);
+    }
+}
+
+// Per-thread form (each thread reads its own columns), for the split-K
+// reduction whose threads own different column quads.
 template <int W>
 __device__ __forceinline__ void ep_scale(const KernelParams& p, float (&a)[W], int row, int col0) {
+    if (!p.rs_row && !p.cs_col) return;
     const float rs = (p.rs_row && row < p.M) ? __ldg(p.rs_row + row) : 1.0f;
 #pragma unroll
     for (int i = 0; i < W; ++i) {
@@ -403,17 +442,66 @@ __device__ __forceinline__ void ep_scale(const KernelParams& p, float (&a)[W], i
 
 template <int W>
 __device__ __forceinline__ void ep_finish(const KernelParams& p, float (&v)[W], int row, int col0) {
-    // a missing bias adds nothing (not +0, which would turn a -0 result into +0)
-    const bool has_br = p.bias_row && row < p.M;
-    const float br = has_br ? __ldg(p.bias_row + row) : 0.0f;
+    const float br = (p.bias_row && row < p.M) ? __ldg(p.bias_row + row) : kNoBias;
+    if (p.bias_col) {
 #pragma unroll
-    for (int i = 0; i < W; ++i) {
-        const int col = col0 + i;
-        float x = v[i];
-        if (has_br) x += br;
-        if (p.bias_col && col < p.N) x += __ldg(p.bias_col + col);
-        v[i] = ep_act(p.act, x);
+        for (int i = 0; i < W; ++i) {
+            const int col = col0 + i;
+            v[i] = (v[i] + br) + (col < p.N ? __ldg(p.bias_col + col) : kNoBias);
+        }
+    } else if (p.bias_row) {
+#pragma unroll
+        for (int i = 0; i < W; ++i) v[i] += br;
     }
+    ep_act_w<W>(p.act, v);
+}
+
+// Warp form, for the paths where the 32 lanes of a warp hold 32 rows of the
+// same W columns: lane i reads column col0 + i of each column vector (one
+// coalesced load) and the values reach the other lanes by shuffles; each
+// lane reads the row vectors for its own row.  All 32 lanes must take part.
+// (Reading the 32 column values in every lane, as the per-thread form does,
+// cost ~30 us per tile: the shared-memory carve-out leaves almost no L1, so
+// each of the 32 loads went to L2 in turn.)
+struct EpLane {
+    float cs_l, bc_l;   // column scale / bias of column col0 + lane (1 / -0 where absent)
+    float rs, br;       // this lane's row scale (1) and row bias (-0)
+};
+
+template <int W>
+__device__ __forceinline__ EpLane ep_lane(const KernelParams& p, int row, int col0, int lane) {
+    EpLane e;
+    const int col = col0 + lane;
+    const bool cin = lane < W && col < p.N;
+    e.cs_l = (p.cs_col && cin) ? __ldg(p.cs_col + col) : 1.0f;
+    e.bc_l = (p.bias_col && cin) ? __ldg(p.bias_col + col) : kNoBias;
+    const bool rin = row < p.M;
+    e.rs = (p.rs_row && rin) ? __ldg(p.rs_row + row) : 1.0f;
+    e.br = (p.bias_row && rin) ? __ldg(p.bias_row + row) : kNoBias;
+    return e;
+}
+
+template <int W>
+__device__ __forceinline__ void ep_scale_w(const KernelParams& p, const EpLane& e, float (&a)[W]) {
+    if (p.cs_col) {
+#pragma unroll
+        for (int i = 0; i < W; ++i) a[i] *= e.rs * __shfl_sync(0xffffffffu, e.cs_l, i);
+    } else if (p.rs_row) {
+#pragma unroll
+        for (int i = 0; i < W; ++i) a[i] *= e.rs;
+    }
+}
+
+template <int W>
+__device__ __forceinline__ void ep_finish_w(const KernelParams& p, const EpLane& e, float (&v)[W]) {
+    if (p.bias_col) {
+#pragma unroll
+        for (int i = 0; i < W; ++i) v[i] = (v[i] + e.br) + __shfl_sync(0xffffffffu, e.bc_l, i);
+    } else if (p.bias_row) {
+#pragma unroll
+        for (int i = 0; i < W; ++i) v[i] += e.br;
+    }
+    ep_act_w<W>(p.act, v);
 }
 
 // 16 bytes of C (one aligned group) into c[i0 .. i0+VEC).
@@ -587,7 +675,7 @@ __device__ __forceinline__ void store_d_block(const KernelParams& p, int row0, i
 // accumulator row, written to D (row-major, or transposed with trans_out).
 template <class Cfg, bool EP>
 __device__ __forceinline__ void epilogue_chunk(const KernelParams& p, const float (&acc)[Cfg::W], int row,
-                                               int col0) {
+                                               int col0, bool row_ok = true, int lane = 0) {
     if constexpr (!EP) {
         constexpr int W = Cfg::W;
         constexpr int ESZ = Vec<Cfg::OUT>::ESZ;
@@ -620,13 +708,17 @@ __device__ __forceinline__ void epilogue_chunk(const KernelParams& p, const floa
         row_segment_dispatch<Cfg::OUT, W, true>(static_cast<char*>(p.D) + off * ESZ, v, n);
     
     } else {
+        // every lane of the warp calls this (the vectors are shared by shuffles);
+        // lanes whose row lies outside the product touch no memory
         constexpr int W = Cfg::W;
         constexpr int ESZ = Vec<Cfg::OUT>::ESZ;
-        const int n = min(W, p.N - col0);
+        EpLane ec{};
+        if (p.ep) ec = ep_lane<W>(p, row, col0, lane);
+        const int n = row_ok ? min(W, p.N - col0) : 0;
         float a[W];
     #pragma unroll
         for (int i = 0; i < W; ++i) a[i] = acc[i];
-        if (p.ep) ep_scale<W>(p, a, row, col0);
+        if (p.ep) ep_scale_w<W>(p, ec, a);
         float v[W];
     #pragma unroll
         for (int i = 0; i < W; ++i) v[i] = p.alpha * a[i];
@@ -639,7 +731,7 @@ __device__ __forceinline__ void epilogue_chunk(const KernelParams& p, const floa
                         v[i] = fmaf(p.alpha, a[i],
                                     p.beta * load_elem<Cfg::OUT>(p.C, static_cast<int64_t>(col0 + i) * p.ldc + row));
             }
-            if (p.ep) ep_finish<W>(p, v, row, col0);
+            if (p.ep) ep_finish_w<W>(p, ec, v);
     #pragma unroll
             for (int i = 0; i < W; ++i)
                 if (i < n) store_elem<Cfg::OUT>(p.D, static_cast<int64_t>(col0 + i) * p.ldc + row, v[i]);
@@ -650,13 +742,14 @@ __device__ __forceinline__ void epilogue_chunk(const KernelParams& p, const floa
             float c[W];
     #pragma unroll
             for (int i = 0; i < W; ++i) c[i] = 0.0f;
-            row_segment_dispatch<Cfg::OUT, W, false>(
-                const_cast<char*>(static_cast<const char*>(p.C)) + off * ESZ, c, n);
+            if (row_ok)
+                row_segment_dispatch<Cfg::OUT, W, false>(
+                    const_cast<char*>(static_cast<const char*>(p.C)) + off * ESZ, c, n);
     #pragma unroll
             for (int i = 0; i < W; ++i) v[i] = fmaf(p.alpha, a[i], p.beta * c[i]);
         }
-        if (p.ep) ep_finish<W>(p, v, row, col0);
-        row_segment_dispatch<Cfg::OUT, W, true>(static_cast<char*>(p.D) + off * ESZ, v, n);
+        if (p.ep) ep_finish_w<W>(p, ec, v);
+        if (row_ok) row_segment_dispatch<Cfg::OUT, W, true>(static_cast<char*>(p.D) + off * ESZ, v, n);
     
     }
 }
@@ -803,8 +896,12 @@ __device__ __forceinline__ void stage_and_store(const KernelParams& p, const voi
     float acc[32];
 #pragma unroll
     for (int i = 0; i < 32; ++i) acc[i] = v[i];
+    EpLane ec{};
     if constexpr (EP) {
-        if (p.ep) ep_scale<32>(p, acc, row, col0);
+        if (p.ep) {
+            ec = ep_lane<32>(p, row, col0, lane);
+            ep_scale_w<32>(p, ec, acc);
+        }
     }
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] = p.alpha * acc[i];
@@ -823,7 +920,7 @@ __device__ __forceinline__ void stage_and_store(const KernelParams& p, const voi
         for (int i = 0; i < 32; ++i) v[i] = fmaf(p.alpha, acc[i], p.beta * c[i]);
     }
     if constexpr (EP) {
-        if (p.ep) ep_finish<32>(p, v, row, col0);
+        if (p.ep) ep_finish_w<32>(p, ec, v);
     }
     if constexpr (Cfg::OUT == kOutF32) {
         uint32_t words[32];
@@ -1300,8 +1397,12 @@ gemm_sm103_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                             float a[W];
 #pragma unroll
                             for (int i = 0; i < W; ++i) a[i] = acc_value<Cfg::ACC_F16>(r[i]);
+                            EpLane ec{};
                             if constexpr (EP) {
-                                if (p.ep) ep_scale<W>(p, a, row, col0);
+                                if (p.ep) {
+                                    ec = ep_lane<W>(p, row, col0, lane);
+                                    ep_scale_w<W>(p, ec, a);
+                                }
                             }
                             float v[W];
 #pragma unroll
@@ -1329,7 +1430,7 @@ gemm_sm103_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                                 for (int i = 0; i < W; ++i) v[i] = fmaf(p.alpha, a[i], p.beta * cv[i]);
                             }
                             if constexpr (EP) {
-                                if (p.ep) ep_finish<W>(p, v, row, col0);
+                                if (p.ep) ep_finish_w<W>(p, ec, v);
                             }
                             store_d_block<Cfg::OUT>(p, row0w, col0, lane, cur, v);
                         }
@@ -1344,11 +1445,13 @@ gemm_sm103_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                         uint32_t r[W];
                         tmem_ld_row<W>(t_row + W * c, r);
                         tmem_ld_wait();
-                        if (!row_ok) continue;
+                        if constexpr (!EP) {
+                            if (!row_ok) continue;
+                        }
                         float acc[W];
 #pragma unroll
                         for (int i = 0; i < W; ++i) acc[i] = acc_value<Cfg::ACC_F16>(r[i]);
-                        epilogue_chunk<Cfg, EP>(p, acc, row, col0);
+                        epilogue_chunk<Cfg, EP>(p, acc, row, col0, row_ok, lane);
                     }
                 }
             } else {
@@ -1476,7 +1579,9 @@ __global__ void scale_c_kernel(int32_t M, int32_t N, const void* C, void* D, int
         const int64_t off = i * ldc + j;
         float v = beta != 0.0f ? beta * load_elem<OUT>(C, off) : 0.0f;
         if (bias) v += bias[j];
-        store_elem<OUT>(D, off, ep_act(act, v));
+        float a[1] = {v};
+        ep_act_w<1>(act, a);
+        store_elem<OUT>(D, off, a[0]);
     }
 }
 
