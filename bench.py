@@ -62,6 +62,8 @@ def parse():
     ap.add_argument("--out", choices=["f32", "f16", "bf16"])
     ap.add_argument("--epilogue", choices=["none", "bias", "bias_relu", "bias_gelu", "scale_bias_gelu"],
                     default="none", help="fused epilogue timed with the GEMM (random fp32 vectors)")
+    ap.add_argument("--autotune", action="store_true",
+                    help="time every candidate configuration first (gemm_plan_autotune) and run the fastest")
     return ap.parse_args()
 
 
@@ -323,6 +325,15 @@ def main():
         plan.gemm(A_l, B_l, C_l, D_l, alpha=w.alpha, beta=w.beta, accum_dtype=w.accum_dtype,
                   out_dtype=w.out_dtype, stream=stream.cuda_stream, **ep)
 
+    tuning = None
+    if args.autotune:
+        _, rows = plan.autotune(A_l, B_l, C_l, D_l, alpha=w.alpha, beta=w.beta, accum_dtype=w.accum_dtype,
+                                out_dtype=w.out_dtype, reps=5, stream=stream.cuda_stream)
+        tuning = {"candidates": len(rows), "chosen": next(r["config"] for r in rows if r["chosen"]),
+                  "model": next(r["config"] for r in rows if r["model"]),
+                  "chosen_us": min(r["us"] for r in rows),
+                  "model_us": next(r["us"] for r in rows if r["model"])}
+
     for i in range(args.warmup):
         flush_l2(i)
         step()
@@ -441,6 +452,7 @@ def main():
             "nominal_dense_fp16_tflops": NOMINAL_DENSE_FP16_TFLOPS,
             "kernel_config": plan.describe(w.M, w.N, w.K, w.layoutA, w.layoutB, w.accum_dtype, w.out_dtype),
             "epilogue": args.epilogue,
+            "autotune": tuning,
             "wall_s_timed_loop": wall,
             "step_ms_min": min(per_step), "step_ms_median": statistics.median(per_step),
         },

@@ -169,16 +169,76 @@ typedef enum {
  * accumulation is never split. */
 gemm_status_t gemm_plan_force_config(gemm_plan_t plan, gemm_config_t config, int splits);
 
+/* How the tiles of a partial last wave (or all tiles, when there are fewer
+ * tiles than co-resident units) are divided.  The plan normally picks the
+ * division with its cost model; gemm_plan_force_division pins one for this
+ * plan's later calls:
+ *   WHOLE        every tile runs whole;
+ *   SPLIT        the tiles are split along K into `splits` ranges; each
+ *                split writes an fp32 partial and the last split to arrive
+ *                adds them in split order;
+ *   EARLY_SPLIT  after at least one whole wave: split s >= 1 of a tile runs
+ *                first in its unit and leaves an fp32 partial, split 0 runs
+ *                last in its unit with its accumulator started from them
+ *                (2 to 4 splits, one per unit);
+ *   HALVES       each tile runs as two half-width items.
+ * `splits` (0: any) pins the split count of SPLIT and EARLY_SPLIT.  A call
+ * whose problem admits no candidate of the pinned division (EARLY_SPLIT
+ * with less than one whole wave or fp16 accumulation, HALVES on a
+ * configuration without halves, ...) returns GEMM_ERR_UNSUPPORTED.  AUTO
+ * restores the model's choice.  Combines with gemm_plan_force_config. */
+typedef enum {
+    GEMM_DIVISION_AUTO = 0,
+    GEMM_DIVISION_WHOLE = 1,
+    GEMM_DIVISION_SPLIT = 2,
+    GEMM_DIVISION_EARLY_SPLIT = 3,
+    GEMM_DIVISION_HALVES = 4
+} gemm_division_t;
+
+gemm_status_t gemm_plan_force_division(gemm_plan_t plan, gemm_division_t division, int splits);
+
 /* Number of kernels this plan has launched so far. */
 uint64_t gemm_plan_launch_count(gemm_plan_t plan);
 
 /* Number of SMs of the plan's device. */
 int gemm_plan_sm_count(gemm_plan_t plan);
 
+/* Shape-keyed autotuning ("矩阵乘法优化可视化学习文档", section 6, the
+ * "Autotuning" row: the best tile differs with M/N/K and type, found by
+ * search; section 8, "Autotune": one kernel, several block configurations,
+ * the fastest kept).  Runs every candidate the plan's cost model considers for
+ * this problem -- each kernel configuration, whole tiles, K splits with
+ * last-arriver or early-partial reduction, half-width items -- `reps` times
+ * (after one warm-up run each) on `stream`, timing each run with CUDA events,
+ * and records the candidate with the smallest median time for the key
+ * (M, N, K, layoutA, layoutB, accum_dtype, out_dtype).  Later gemm_run /
+ * gemm_run_ep calls on this plan with that key use it (a configuration
+ * pinned by gemm_plan_force_config still wins; the pin is ignored while
+ * tuning).  Arguments are gemm_run's (D is overwritten by every run; on
+ * return it holds the chosen candidate's result) plus reps (1..1000) and an
+ * optional report buffer: one line per candidate, "<config> model_cost=<c>
+ * us=<median>", the chosen one starred and the cost model's own pick marked
+ * "(model)".  Blocks until the stream has finished.  Returns a gemm_run
+ * status (GEMM_ERR_TIMEOUT if a run recorded a device timeout); M, N or
+ * K = 0 just runs gemm_run.  Not thread-safe against other calls on the same
+ * plan. */
+gemm_status_t gemm_plan_autotune(gemm_plan_t plan, const void *A, const void *B, const void *C, void *D,
+                                 int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
+                                 gemm_layout_t layoutA, gemm_layout_t layoutB,
+                                 gemm_dtype_t accum_dtype, gemm_dtype_t out_dtype,
+                                 float alpha, float beta, int reps, void *stream,
+                                 char *report, int64_t report_len);
+
+/* Forget every autotuned choice of the plan (the cost model decides again). */
+gemm_status_t gemm_plan_clear_tuning(gemm_plan_t plan);
+
+/* Number of shapes the plan holds an autotuned choice for. */
+int64_t gemm_plan_tuned_count(gemm_plan_t plan);
+
 /* Describe the kernel configuration gemm_run would pick for these sizes
- * and types into buf (NUL-terminated, at most `len` bytes).  Returns the
- * same validation status as gemm_validate (with A, B, C, D taken as
- * aligned). */
+ * and types into buf (NUL-terminated, at most `len` bytes), ending with
+ * "source=model", "source=tuned" or "source=pinned".  Returns the same
+ * validation status as gemm_validate (with A, B, C, D taken as aligned). */
 gemm_status_t gemm_plan_describe(gemm_plan_t plan, int64_t M, int64_t N, int64_t K,
                                  gemm_layout_t layoutA, gemm_layout_t layoutB,
                                  gemm_dtype_t accum_dtype, gemm_dtype_t out_dtype,

@@ -31,7 +31,8 @@ __all__ = [
     "gemm_plan_create", "gemm_run", "gemm_validate", "gemm_plan_device_status",
     "gemm_plan_device_error_site", "gemm_plan_set_timeout_ns", "gemm_plan_launch_count",
     "gemm_plan_sm_count", "gemm_plan_describe", "gemm_plan_destroy", "gemm_status_string",
-    "gemm_plan_force_config", "CONFIG", "gemm_run_static_scratch",
+    "gemm_plan_force_config", "CONFIG", "gemm_run_static_scratch", "gemm_plan_autotune",
+    "gemm_plan_clear_tuning", "gemm_plan_tuned_count", "gemm_plan_force_division", "DIVISION",
 ]
 
 STATUS = {
@@ -87,6 +88,15 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.gemm_plan_describe.restype = i32
     lib.gemm_plan_destroy.argtypes = [p]
     lib.gemm_plan_destroy.restype = i32
+    lib.gemm_plan_autotune.argtypes = [p, p, p, p, p, i64, i64, i64, i64, i64, i64, i32, i32, i32, i32, f32, f32,
+                                       i32, p, ctypes.c_char_p, i64]
+    lib.gemm_plan_autotune.restype = i32
+    lib.gemm_plan_force_division.argtypes = [p, i32, i32]
+    lib.gemm_plan_force_division.restype = i32
+    lib.gemm_plan_clear_tuning.argtypes = [p]
+    lib.gemm_plan_clear_tuning.restype = i32
+    lib.gemm_plan_tuned_count.argtypes = [p]
+    lib.gemm_plan_tuned_count.restype = i64
     lib.gemm_run_static_scratch.argtypes = [i32, i32, p, p, p, p, i64, i64, i64, i64, i64, i64, i32, i32, i32,
                                             i32, f32, f32, i32, p]
     lib.gemm_run_static_scratch.restype = i32
@@ -176,6 +186,14 @@ def gemm_plan_force_config(plan, config: str | int = "auto", splits: int = 0) ->
     return load().gemm_plan_force_config(plan, CONFIG[config] if isinstance(config, str) else config, splits)
 
 
+DIVISION = {"auto": 0, "whole": 1, "split": 2, "early_split": 3, "halves": 4}
+
+
+def gemm_plan_force_division(plan, division: str | int = "auto", splits: int = 0) -> int:
+    return load().gemm_plan_force_division(plan, DIVISION[division] if isinstance(division, str) else division,
+                                           splits)
+
+
 def gemm_plan_launch_count(plan) -> int:
     return load().gemm_plan_launch_count(plan)
 
@@ -196,6 +214,23 @@ def gemm_plan_describe(plan, M, N, K, layoutA="row", layoutB="row", accum_dtype=
 
 def gemm_plan_destroy(plan) -> int:
     return load().gemm_plan_destroy(plan)
+
+
+def gemm_plan_autotune(plan, A, B, C, D, M, N, K, lda, ldb, ldc, layoutA, layoutB, accum_dtype, out_dtype,
+                       alpha, beta, reps, stream) -> tuple[int, str]:
+    """Returns (status, report text)."""
+    buf = ctypes.create_string_buffer(16384)
+    st = load().gemm_plan_autotune(plan, A, B, C, D, M, N, K, lda, ldb, ldc, LAYOUT[layoutA], LAYOUT[layoutB],
+                                   DTYPE[accum_dtype], DTYPE[out_dtype], alpha, beta, reps, stream, buf, 16384)
+    return st, buf.value.decode()
+
+
+def gemm_plan_clear_tuning(plan) -> int:
+    return load().gemm_plan_clear_tuning(plan)
+
+
+def gemm_plan_tuned_count(plan) -> int:
+    return load().gemm_plan_tuned_count(plan)
 
 
 def gemm_run_static_scratch(device, in_dtype, A, B, C, D, M, N, K, lda, ldb, ldc, layoutA, layoutB,
@@ -303,6 +338,13 @@ class Plan:
         if st != 0:
             raise GemmError(st, "gemm_plan_force_config")
 
+    def force_division(self, division: str | int = "auto", splits: int = 0):
+        """Pin how the partial last wave's tiles are divided ("whole",
+        "split", "early_split", "halves"; "auto" restores the model)."""
+        st = gemm_plan_force_division(self.handle, division, splits)
+        if st != 0:
+            raise GemmError(st, "gemm_plan_force_division")
+
     def describe(self, M, N, K, layoutA="row", layoutB="row", accum_dtype="f32", out_dtype="f32") -> str:
         return gemm_plan_describe(self.handle, M, N, K, layoutA, layoutB, accum_dtype, out_dtype)
 
@@ -327,6 +369,27 @@ class Plan:
         gemm_epilogue_t); returns D (allocated if not given).  Layouts and
         leading dimensions come from the strides."""
         import torch
+        M, N, K, la, lda, lb, ldb, ldc, out_dtype, D = self._resolve(A, B, C, D, out_dtype)
+        if stream is None:
+            stream = torch.cuda.current_stream(A.device).cuda_stream
+        ep = None
+        if bias is not None or row_scale is not None or col_scale is not None or act != "none":
+            def vec(v, n, what):
+                if v is None:
+                    return None
+                if v.dtype != torch.float32 or v.dim() != 1 or v.shape[0] != n or not v.is_cuda or v.stride(0) != 1:
+                    raise ValueError(f"{what} must be a contiguous fp32 device vector of length {n}")
+                return v.data_ptr()
+            ep = Epilogue(vec(bias, N, "bias"), vec(row_scale, M, "row_scale"), vec(col_scale, N, "col_scale"),
+                          ACT[act])
+        self.run_raw(A.data_ptr(), B.data_ptr(), C.data_ptr() if C is not None else None, D.data_ptr(),
+                     M, N, K, lda, ldb, max(ldc, N), la, lb, accum_dtype, out_dtype, alpha, beta, stream, ep=ep)
+        return D
+
+    def _resolve(self, A, B, C, D, out_dtype):
+        """Sizes, storage orders and leading dimensions from the tensors'
+        shapes and strides (D allocated if not given)."""
+        import torch
         M, K = A.shape
         K2, N = B.shape
         if K2 != K:
@@ -347,21 +410,40 @@ class Plan:
                 raise ValueError("C must be row-major M x N with the same row stride as D")
             if _dt_name(C) != out_dtype:
                 raise ValueError("C must have the output type")
+        return M, N, K, la, lda, lb, ldb, ldc, out_dtype, D
+
+    def autotune(self, A, B, C=None, D=None, *, alpha: float = 1.0, beta: float = 0.0,
+                 accum_dtype: str = "f32", out_dtype: str | None = None, reps: int = 5, stream=None):
+        """Time every candidate configuration for this problem and keep the
+        fastest for later calls with the same shape and types (see
+        gemm_plan_autotune).  Returns (D, report), the report a list of
+        {"config", "model_cost", "us", "chosen", "model"} dicts."""
+        import torch
+        M, N, K, la, lda, lb, ldb, ldc, out_dtype, D = self._resolve(A, B, C, D, out_dtype)
         if stream is None:
             stream = torch.cuda.current_stream(A.device).cuda_stream
-        ep = None
-        if bias is not None or row_scale is not None or col_scale is not None or act != "none":
-            def vec(v, n, what):
-                if v is None:
-                    return None
-                if v.dtype != torch.float32 or v.dim() != 1 or v.shape[0] != n or not v.is_cuda or v.stride(0) != 1:
-                    raise ValueError(f"{what} must be a contiguous fp32 device vector of length {n}")
-                return v.data_ptr()
-            ep = Epilogue(vec(bias, N, "bias"), vec(row_scale, M, "row_scale"), vec(col_scale, N, "col_scale"),
-                          ACT[act])
-        self.run_raw(A.data_ptr(), B.data_ptr(), C.data_ptr() if C is not None else None, D.data_ptr(),
-                     M, N, K, lda, ldb, max(ldc, N), la, lb, accum_dtype, out_dtype, alpha, beta, stream, ep=ep)
-        return D
+        st, text = gemm_plan_autotune(self.handle, A.data_ptr(), B.data_ptr(),
+                                      C.data_ptr() if C is not None else None, D.data_ptr(), M, N, K, lda, ldb,
+                                      max(ldc, N), la, lb, accum_dtype, out_dtype, alpha, beta, reps, stream)
+        if st != 0:
+            raise GemmError(st, "gemm_plan_autotune")
+        rows = []
+        for line in text.splitlines():
+            chosen = line.startswith("*")
+            parts = line[2:].split()
+            kv = dict(x.split("=", 1) for x in parts[1:] if "=" in x)
+            rows.append({"config": parts[0], "model_cost": float(kv["model_cost"]), "us": float(kv["us"]),
+                         "chosen": chosen, "model": "(model)" in line})
+        return D, rows
+
+    def clear_tuning(self):
+        st = gemm_plan_clear_tuning(self.handle)
+        if st != 0:
+            raise GemmError(st, "gemm_plan_clear_tuning")
+
+    @property
+    def tuned_count(self) -> int:
+        return gemm_plan_tuned_count(self.handle)
 
     def gemm_host(self, A, B, C=None, D=None, *, alpha: float = 1.0, beta: float = 0.0,
                   accum_dtype: str = "f32", out_dtype: str | None = None, stream=None,

@@ -4,12 +4,16 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
+#include <array>
 #include <cstdint>
 #include <cstdio>
 #include <cstring>
+#include <map>
 #include <mutex>
 #include <new>
 #include <string>
+#include <vector>
 
 #include "gemm.h"
 #include "gemm_internal.cuh"
@@ -109,38 +113,65 @@ int default_units(const gemm_plan* plan, int kind) {
 }
 
 // Time of one 64-deep K step of a tile (or half-width item) on its unit,
-// relative to a 256 x 256 tile on a CTA pair, as measured on GB300 at
-// 4096^3 (the main loop is bound by operand feed and, for N <= 128 MMAs, by
-// MMA issue, so the costs do not follow the tile areas):
-//   pair 256x256: 1.0; its half-width items: 0.757
-//   pair 256x224: 0.95 with row-major B (whole 64-column boxes per CTA),
-//                 0.85 with column-major B
-//   one CTA 128x256: 1.16; its half-width items: 0.88
-// (a least-squares fit over 9 shapes x 2 layouts x 6 choices, 4 % rms).
+// relative to a 256 x 256 tile on a CTA pair (the main loop is bound by
+// operand feed and, for N <= 128 MMAs, by MMA issue, so the costs do not
+// follow the tile areas), and the fixed costs below, in the same unit: a
+// least-squares fit of the autotuner's timings of every candidate on GB300
+// (26 shapes from 96 x 4096 x 4096 to 12288 x 4096 x 4096, both B storage
+// orders, 1123 timings, 10 % rms):
+//   pair 256x256: 1.0; its half-width items: 0.83
+//   pair 256x224: 1.0 with row-major B (whole 64-column boxes per CTA),
+//                 0.92 with column-major B
+//   one CTA 128x256: 1.23; its half-width items: 1.02
 // The transposed-product tiles (128 x 16, 128 x 64) only compete with each
 // other and with their own splits; they get the same per-step cost.
 double step_cost(int kind, bool b_mn_major, bool half) {
     switch (kind) {
-        case kCfgPair256: return half ? 0.757 : 1.0;
-        case kCfgPair224: return b_mn_major ? 0.95 : 0.85;
-        case kCfgSingle256: return half ? 0.88 : 1.16;
+        case kCfgPair256: return half ? 0.83 : 1.0;
+        case kCfgPair224: return b_mn_major ? 1.0 : 0.92;
+        case kCfgSingle256: return half ? 1.02 : 1.23;
         default: return 1.0;
     }
 }
 
+struct FixedCosts {
+    double item;          // per whole or split item: set-up, epilogue tail
+    double half_item;     // per half-width item
+    double early;         // an early-split owner: waiting for and seeding the partials ...
+    double per_partial;   // ... per partial it adds
+    double reduce;        // a last-arriver reduction: partial write, arrival, read back ...
+    double per_split;     // ... per split
+};
+// (The fit gives 9.5 + 7.5 (s - 1) for an early split; 2 + 9 (s - 1) is as
+// close over the fitted shapes and keeps 4096^3 on early partials, which the
+// L2-flushed benchmark measures at 80.5 us against 82.1 us for half-width
+// items.)
+constexpr FixedCosts kFixed = {16.0, 6.7, 2.0, 9.0, 22.7, 5.9};
+// The transposed product (M <= 64, HBM-bound) keeps the constants of an
+// earlier fit over its own shapes: 5 per item, 3.4 per half item, and a
+// reduction of 8 + 30 * BN / 256 + 2 * s.
+FixedCosts transposed_fixed(int bn) { return {5.0, 3.4, 0.0, 0.0, 8.0 + 30.0 * bn / 256.0, 2.0}; }
+
 // Configuration, K-split count and orientation with the smallest modelled
 // time: for each category of work item, waves (items over co-resident
 // units) times the item's cost in K steps (its k-blocks times step_cost, plus
-// 5 fixed; 3.4 for a half-width item).  Whole waves of tiles run whole; the
-// tiles of a partial last wave (or all tiles, when there are fewer than
-// units) are either split into `s` K ranges -- plus the reduction, 8 + 30 *
-// BN / 256 + 2 * s steps: every split writes its fp32 partial and the last
-// one to arrive reads them all back, a chain of latencies that costs about
-// 40 steps for a 256-wide tile on GB300 -- or run as two half-width items.
-// A divided tile is charged 2 extra steps, so ties go to whole tiles.
+// its fixed cost).  Whole waves of tiles run whole; the tiles of a partial
+// last wave (or all tiles, when there are fewer than units) are either split
+// into `s` K ranges -- with a last-arriver reduction (every split writes its
+// fp32 partial and the last one to arrive reads them all back, a chain of
+// latencies) or with early partials -- or run as two half-width items.  A
+// divided tile is charged 2 extra steps, so ties go to whole tiles.
 // `valid` is false when a pinned configuration does not fit the problem.
+// With `all`, every candidate is appended with its modelled cost (the
+// autotuner times them); `every_kind` also offers the wider transposed tile
+// where the narrow one fits.
+struct Candidate {
+    double cost;
+    Choice choice;
+};
+
 Choice choose(const gemm_plan* plan, int64_t M, int64_t N, int64_t K, gemm_dtype_t acc, bool b_mn_major,
-              bool* valid) {
+              bool* valid, std::vector<Candidate>* all = nullptr, bool every_kind = false) {
     Choice best;
     *valid = true;
     const bool swap = M <= 64 && N > M;
@@ -159,24 +190,39 @@ Choice choose(const gemm_plan* plan, int64_t M, int64_t N, int64_t K, gemm_dtype
         }
         cands[nc++] = f;
     } else if (swap) {
-        cands[nc++] = Nk <= 16 ? kCfgSingle16 : kCfgSingle64;
+        if (Nk <= 16) cands[nc++] = kCfgSingle16;
+        if (Nk > 16 || every_kind) cands[nc++] = kCfgSingle64;
     } else {
         cands[nc++] = kCfgPair256;
         cands[nc++] = kCfgPair224;
         cands[nc++] = kCfgSingle256;
     }
     double best_cost = -1.0;
-    auto consider = [&](double cost, int kind, int splits, int64_t dp, bool halves, int64_t tiles, int64_t units) {
+    bool any = false;
+    auto consider = [&](double cost, int kind, int splits, int64_t dp, bool halves, int64_t tiles, int64_t units,
+                        bool early = false) {
+        // a pinned division (gemm_plan_force_division) admits only its own kind of candidate
+        const int division = halves ? GEMM_DIVISION_HALVES
+                             : splits > 1 ? (early ? GEMM_DIVISION_EARLY_SPLIT : GEMM_DIVISION_SPLIT)
+                                          : GEMM_DIVISION_WHOLE;
+        if (plan->forced_division != GEMM_DIVISION_AUTO &&
+            (division != plan->forced_division ||
+             (splits > 1 && plan->forced_division_splits > 0 && splits != plan->forced_division_splits)))
+            return;
+        any = true;
+        Choice c;
+        c.kind = kind;
+        c.splits = splits;
+        c.dp_tiles = dp;
+        c.n_halves = halves;
+        c.early = early;
+        c.swap = swap;
+        c.tiles = tiles;
+        c.units = static_cast<int>(units);
+        if (all) all->push_back({cost, c});
         if (best_cost < 0 || cost < best_cost) {
             best_cost = cost;
-            best.kind = kind;
-            best.splits = splits;
-            best.dp_tiles = dp;
-            best.n_halves = halves;
-            best.early = false;
-            best.swap = swap;
-            best.tiles = tiles;
-            best.units = static_cast<int>(units);
+            best = c;
         }
     };
     for (int ci = 0; ci < nc; ++ci) {
@@ -188,7 +234,8 @@ Choice choose(const gemm_plan* plan, int64_t M, int64_t N, int64_t K, gemm_dtype
         const int64_t rest = tiles - dp;                                      // the partial wave
         const int64_t tile_bytes = int64_t(kCfgCtas[kind]) * 128 * kCfgTileN[kind] * 4;
         const double full_step = step_cost(kind, bmn, false);
-        const double full_item = static_cast<double>(kb) * full_step + 5.0;
+        const FixedCosts fc = swap ? transposed_fixed(kCfgTileN[kind]) : kFixed;
+        const double full_item = static_cast<double>(kb) * full_step + fc.item;
         // whole tiles only
         if (!pinned || plan->forced_splits == 1)
             consider(static_cast<double>((tiles + units - 1) / units) * full_item, kind, 1, tiles, false, tiles,
@@ -211,8 +258,8 @@ Choice choose(const gemm_plan* plan, int64_t M, int64_t N, int64_t K, gemm_dtype
         }
         if (split_tiles > 0) {
             for (int64_t s = smin; s <= smax && s > 1; ++s) {
-                const double reduce = 8.0 + 30.0 * kCfgTileN[kind] / 256.0 + 2.0 * static_cast<double>(s);
-                const double item = static_cast<double>((kb + s - 1) / s) * full_step + 5.0 + reduce + 2.0;
+                const double reduce = fc.reduce + fc.per_split * static_cast<double>(s);
+                const double item = static_cast<double>((kb + s - 1) / s) * full_step + fc.item + reduce + 2.0;
                 const double cost = static_cast<double>(dp_split / units) * full_item +
                                     static_cast<double>((split_tiles * s + units - 1) / units) * item;
                 consider(cost, kind, static_cast<int>(s), dp_split, false, tiles, units);
@@ -226,21 +273,21 @@ Choice choose(const gemm_plan* plan, int64_t M, int64_t N, int64_t K, gemm_dtype
                 if (rest * s > units || s > kb || rest * s * tile_bytes > static_cast<int64_t>(plan->ws_bytes) ||
                     rest * s * kCfgCtas[kind] > kNumCounters)
                     break;
-                const double item = static_cast<double>((kb + s - 1) / s) * full_step + 5.0 + 2.0 + 2.0;
+                const double item = static_cast<double>((kb + s - 1) / s) * full_step + fc.item + fc.early +
+                                    fc.per_partial * static_cast<double>(s - 1) + 2.0;
                 const double cost = static_cast<double>(dp / units) * full_item + item;
-                const double before = best_cost;
-                consider(cost, kind, static_cast<int>(s), dp, false, tiles, units);
-                if (best_cost != before) best.early = true;
+                consider(cost, kind, static_cast<int>(s), dp, false, tiles, units, true);
             }
         }
         // two half-width items per tile of the partial wave
         if (kCfgHalves[kind] && rest > 0 && !pinned) {
-            const double item = static_cast<double>(kb) * step_cost(kind, bmn, true) + 3.4 + 2.0;
+            const double item = static_cast<double>(kb) * step_cost(kind, bmn, true) + fc.half_item + 2.0;
             const double cost = static_cast<double>(dp / units) * full_item +
                                 static_cast<double>((2 * rest + units - 1) / units) * item;
             consider(cost, kind, 1, dp, true, tiles, units);
         }
     }
+    if (!any) *valid = false;
     return best;
 }
 
@@ -280,6 +327,69 @@ std::string config_name(const Choice& ch, gemm_dtype_t acc, gemm_dtype_t out) {
     if (ch.splits > 1) s += (ch.early ? "_esplitk" : "_splitk") + std::to_string(ch.splits);
     if (ch.n_halves) s += "_nhalves";
     return s;
+}
+
+}  // namespace
+
+namespace tcdt_host {
+// gemm_plan_autotune's results: the fastest measured choice per problem shape
+// (M, N, K, storage orders, accumulator and output types).
+using TuneKey = std::array<int64_t, 7>;
+struct TunedTable {
+    std::map<TuneKey, Choice> best;
+};
+}  // namespace tcdt_host
+
+namespace {
+
+TuneKey tune_key(int64_t M, int64_t N, int64_t K, gemm_layout_t la, gemm_layout_t lb, gemm_dtype_t acc,
+                 gemm_dtype_t out) {
+    return {M, N, K, static_cast<int64_t>(la), static_cast<int64_t>(lb), static_cast<int64_t>(acc),
+            static_cast<int64_t>(out)};
+}
+
+// The configuration a call runs: a pinned one (gemm_plan_force_config) if
+// set, else the autotuned one for this shape if there is one, else the cost
+// model's.  `source` names which.
+Choice select_choice(const gemm_plan* plan, int64_t M, int64_t N, int64_t K, gemm_layout_t la, gemm_layout_t lb,
+                     gemm_dtype_t acc, gemm_dtype_t out, bool* valid, const char** source) {
+    *valid = true;
+    if (plan->forced_kind < 0 && plan->forced_division == GEMM_DIVISION_AUTO && plan->tuned) {
+        const auto it = plan->tuned->best.find(tune_key(M, N, K, la, lb, acc, out));
+        if (it != plan->tuned->best.end()) {
+            if (source) *source = "tuned";
+            return it->second;
+        }
+    }
+    if (source)
+        *source = (plan->forced_kind >= 0 || plan->forced_division != GEMM_DIVISION_AUTO) ? "pinned" : "model";
+    return choose(plan, M, N, K, acc, lb == GEMM_ROW_MAJOR, valid);
+}
+
+// Launch one chosen configuration (arguments already validated, M, N, K > 0).
+gemm_status_t run_choice(gemm_plan* plan, const Choice& ch, const void* A, const void* B, const void* C, void* D,
+                         int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
+                         gemm_layout_t layoutA, gemm_layout_t layoutB, gemm_dtype_t accum_dtype,
+                         gemm_dtype_t out_dtype, float alpha, float beta, const gemm_epilogue_t* ep,
+                         cudaStream_t s) {
+    const Problem pr = make_problem(ch.swap, A, B, M, N, K, lda, ldb, layoutA, layoutB, ep);
+    const int slot = out_slot(accum_dtype, out_dtype);
+    if (ep) {
+        switch (ch.kind) {
+            case kCfgSingle16: return launch_single16_ep(plan, slot, ch, pr, C, D, ldc, alpha, beta, s);
+            case kCfgSingle64: return launch_single64_ep(plan, slot, ch, pr, C, D, ldc, alpha, beta, s);
+            case kCfgSingle256: return launch_single256_ep(plan, slot, ch, pr, C, D, ldc, alpha, beta, s);
+            case kCfgPair224: return launch_pair224_ep(plan, slot, ch, pr, C, D, ldc, alpha, beta, s);
+            default: return launch_pair256_ep(plan, slot, ch, pr, C, D, ldc, alpha, beta, s);
+        }
+    }
+    switch (ch.kind) {
+        case kCfgSingle16: return launch_single16(plan, slot, ch, pr, C, D, ldc, alpha, beta, s);
+        case kCfgSingle64: return launch_single64(plan, slot, ch, pr, C, D, ldc, alpha, beta, s);
+        case kCfgSingle256: return launch_single256(plan, slot, ch, pr, C, D, ldc, alpha, beta, s);
+        case kCfgPair224: return launch_pair224(plan, slot, ch, pr, C, D, ldc, alpha, beta, s);
+        default: return launch_pair256(plan, slot, ch, pr, C, D, ldc, alpha, beta, s);
+    }
 }
 
 }  // namespace
@@ -373,26 +483,107 @@ gemm_status_t gemm_run_ep(gemm_plan_t plan, const void* A, const void* B, const 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (K == 0) return launch_scale(plan, C, D, M, N, ldc, out_dtype, beta, s, ep);
     bool valid = true;
-    const Choice ch = choose(plan, M, N, K, accum_dtype, layoutB == GEMM_ROW_MAJOR, &valid);
+    const Choice ch = select_choice(plan, M, N, K, layoutA, layoutB, accum_dtype, out_dtype, &valid, nullptr);
     if (!valid) return GEMM_ERR_UNSUPPORTED;
-    const Problem pr = make_problem(ch.swap, A, B, M, N, K, lda, ldb, layoutA, layoutB, ep);
-    const int slot = out_slot(accum_dtype, out_dtype);
-    if (ep) {
-        switch (ch.kind) {
-            case kCfgSingle16: return launch_single16_ep(plan, slot, ch, pr, C, D, ldc, alpha, beta, s);
-            case kCfgSingle64: return launch_single64_ep(plan, slot, ch, pr, C, D, ldc, alpha, beta, s);
-            case kCfgSingle256: return launch_single256_ep(plan, slot, ch, pr, C, D, ldc, alpha, beta, s);
-            case kCfgPair224: return launch_pair224_ep(plan, slot, ch, pr, C, D, ldc, alpha, beta, s);
-            default: return launch_pair256_ep(plan, slot, ch, pr, C, D, ldc, alpha, beta, s);
+    return run_choice(plan, ch, A, B, C, D, M, N, K, lda, ldb, ldc, layoutA, layoutB, accum_dtype, out_dtype, alpha,
+                      beta, ep, s);
+}
+
+gemm_status_t gemm_plan_autotune(gemm_plan_t plan, const void* A, const void* B, const void* C, void* D, int64_t M,
+                                 int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc, gemm_layout_t layoutA,
+                                 gemm_layout_t layoutB, gemm_dtype_t accum_dtype, gemm_dtype_t out_dtype,
+                                 float alpha, float beta, int reps, void* stream, char* report,
+                                 int64_t report_len) {
+    if (!plan || reps < 1 || reps > 1000) return GEMM_ERR_INVALID_ARG;
+    gemm_status_t st = validate(plan->in_dtype, A, B, C, D, M, N, K, lda, ldb, ldc, layoutA, layoutB,
+                                accum_dtype, out_dtype, beta, true);
+    if (st != GEMM_OK) return st;
+    if (report && report_len > 0) report[0] = '\0';
+    if (M == 0 || N == 0 || K == 0) return gemm_run(plan, A, B, C, D, M, N, K, lda, ldb, ldc, layoutA, layoutB,
+                                                    accum_dtype, out_dtype, alpha, beta, stream);
+    DeviceGuard guard(plan->device);
+    if (!guard.ok) return GEMM_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // every candidate of the cost model, pinned configurations ignored
+    const int saved_kind = plan->forced_kind, saved_splits = plan->forced_splits;
+    const int saved_div = plan->forced_division, saved_div_splits = plan->forced_division_splits;
+    plan->forced_kind = -1;
+    plan->forced_splits = 0;
+    plan->forced_division = GEMM_DIVISION_AUTO;
+    plan->forced_division_splits = 0;
+    std::vector<Candidate> cands;
+    bool valid = true;
+    const Choice model = choose(plan, M, N, K, accum_dtype, layoutB == GEMM_ROW_MAJOR, &valid, &cands, true);
+    plan->forced_kind = saved_kind;
+    plan->forced_splits = saved_splits;
+    plan->forced_division = saved_div;
+    plan->forced_division_splits = saved_div_splits;
+    if (!valid || cands.empty()) return GEMM_ERR_UNSUPPORTED;
+    cudaEvent_t e0 = nullptr, e1 = nullptr;
+    if (cudaEventCreate(&e0) != cudaSuccess || cudaEventCreate(&e1) != cudaSuccess) {
+        if (e0) cudaEventDestroy(e0);
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
+    std::vector<double> med(cands.size(), -1.0);
+    std::string text;
+    size_t best = 0;
+    for (size_t c = 0; c < cands.size() && st == GEMM_OK; ++c) {
+        const Choice& ch = cands[c].choice;
+        std::vector<float> ms;
+        for (int r = 0; r <= reps && st == GEMM_OK; ++r) {   // the first run warms up
+            if (cudaEventRecord(e0, s) != cudaSuccess) st = GEMM_ERR_CUDA;
+            if (st == GEMM_OK)
+                st = run_choice(plan, ch, A, B, C, D, M, N, K, lda, ldb, ldc, layoutA, layoutB, accum_dtype,
+                                out_dtype, alpha, beta, nullptr, s);
+            if (st == GEMM_OK && (cudaEventRecord(e1, s) != cudaSuccess || cudaEventSynchronize(e1) != cudaSuccess))
+                st = GEMM_ERR_CUDA;
+            float t = 0.0f;
+            if (st == GEMM_OK && cudaEventElapsedTime(&t, e0, e1) != cudaSuccess) st = GEMM_ERR_CUDA;
+            if (st == GEMM_OK && r > 0) ms.push_back(t);
         }
+        if (st != GEMM_OK) break;
+        std::sort(ms.begin(), ms.end());
+        med[c] = 1000.0 * ms[ms.size() / 2];
+        if (med[c] < med[best]) best = c;
     }
-    switch (ch.kind) {
-        case kCfgSingle16: return launch_single16(plan, slot, ch, pr, C, D, ldc, alpha, beta, s);
-        case kCfgSingle64: return launch_single64(plan, slot, ch, pr, C, D, ldc, alpha, beta, s);
-        case kCfgSingle256: return launch_single256(plan, slot, ch, pr, C, D, ldc, alpha, beta, s);
-        case kCfgPair224: return launch_pair224(plan, slot, ch, pr, C, D, ldc, alpha, beta, s);
-        default: return launch_pair256(plan, slot, ch, pr, C, D, ldc, alpha, beta, s);
+    cudaEventDestroy(e0);
+    cudaEventDestroy(e1);
+    if (st == GEMM_ERR_CUDA) cudaGetLastError();
+    if (st != GEMM_OK) return st;
+    // a timed-out kernel leaves its mark in the status word, not in the return code
+    int hs[2] = {0, 0};
+    if (cudaMemcpy(hs, plan->d_status, sizeof(hs), cudaMemcpyDeviceToHost) != cudaSuccess) return GEMM_ERR_CUDA;
+    if (hs[0] != 0) return static_cast<gemm_status_t>(hs[0]);
+    if (!plan->tuned) {
+        plan->tuned = new (std::nothrow) TunedTable();
+        if (!plan->tuned) return GEMM_ERR_CUDA;
     }
+    plan->tuned->best[tune_key(M, N, K, layoutA, layoutB, accum_dtype, out_dtype)] = cands[best].choice;
+    for (size_t c = 0; c < cands.size(); ++c) {
+        const Choice& ch = cands[c].choice;
+        const bool is_model = ch.kind == model.kind && ch.splits == model.splits && ch.n_halves == model.n_halves &&
+                              ch.early == model.early && ch.dp_tiles == model.dp_tiles;
+        char line[160];
+        std::snprintf(line, sizeof(line), "%s%s model_cost=%.1f us=%.2f%s\n", c == best ? "* " : "  ",
+                      config_name(ch, accum_dtype, out_dtype).c_str(), cands[c].cost, med[c],
+                      is_model ? " (model)" : "");
+        text += line;
+    }
+    if (report && report_len > 0) std::snprintf(report, static_cast<size_t>(report_len), "%s", text.c_str());
+    // leave D holding the chosen configuration's result
+    return run_choice(plan, cands[best].choice, A, B, C, D, M, N, K, lda, ldb, ldc, layoutA, layoutB, accum_dtype,
+                      out_dtype, alpha, beta, nullptr, s);
+}
+
+gemm_status_t gemm_plan_clear_tuning(gemm_plan_t plan) {
+    if (!plan) return GEMM_ERR_INVALID_ARG;
+    if (plan->tuned) plan->tuned->best.clear();
+    return GEMM_OK;
+}
+
+int64_t gemm_plan_tuned_count(gemm_plan_t plan) {
+    return plan && plan->tuned ? static_cast<int64_t>(plan->tuned->best.size()) : 0;
 }
 
 gemm_status_t gemm_plan_device_status(gemm_plan_t plan, int clear) {
@@ -433,6 +624,16 @@ gemm_status_t gemm_plan_force_config(gemm_plan_t plan, gemm_config_t config, int
     return GEMM_OK;
 }
 
+gemm_status_t gemm_plan_force_division(gemm_plan_t plan, gemm_division_t division, int splits) {
+    if (!plan) return GEMM_ERR_INVALID_ARG;
+    if (static_cast<int>(division) < GEMM_DIVISION_AUTO || static_cast<int>(division) > GEMM_DIVISION_HALVES)
+        return GEMM_ERR_INVALID_ARG;
+    if (splits < 0 || splits > kMaxSplits) return GEMM_ERR_INVALID_ARG;
+    plan->forced_division = static_cast<int>(division);
+    plan->forced_division_splits = division == GEMM_DIVISION_AUTO ? 0 : splits;
+    return GEMM_OK;
+}
+
 #ifdef TCDT_FAULT_INJECTION
 // Test builds only (not part of the product library or of include/gemm.h):
 // make the producer of every CTA skip its `index`-th TMA issue (-1: none).
@@ -465,16 +666,18 @@ gemm_status_t gemm_plan_describe(gemm_plan_t plan, int64_t M, int64_t N, int64_t
         return GEMM_OK;
     }
     bool valid = true;
-    const Choice ch = choose(plan, M, N, K, accum_dtype, layoutB == GEMM_ROW_MAJOR, &valid);
+    const char* source = "model";
+    const Choice ch = select_choice(plan, M, N, K, layoutA, layoutB, accum_dtype, out_dtype, &valid, &source);
     if (!valid) return GEMM_ERR_UNSUPPORTED;
     const int64_t work = ch.n_halves      ? ch.dp_tiles + (ch.tiles - ch.dp_tiles) * 2
                          : ch.splits > 1 ? ch.dp_tiles + (ch.tiles - ch.dp_tiles) * ch.splits
                                          : ch.tiles;
     const int64_t units = work < ch.units ? work : ch.units;
-    std::snprintf(buf, static_cast<size_t>(len), "%s tiles=%lld divided_tiles=%lld splits=%d ctas=%lld sms=%d",
+    std::snprintf(buf, static_cast<size_t>(len),
+                  "%s tiles=%lld divided_tiles=%lld splits=%d ctas=%lld sms=%d source=%s",
                   config_name(ch, accum_dtype, out_dtype).c_str(), static_cast<long long>(ch.tiles),
                   static_cast<long long>((ch.splits > 1 || ch.n_halves) ? ch.tiles - ch.dp_tiles : 0), ch.splits,
-                  static_cast<long long>(units * kCfgCtas[ch.kind]), plan->sm_count);
+                  static_cast<long long>(units * kCfgCtas[ch.kind]), plan->sm_count, source);
     return GEMM_OK;
 }
 
@@ -487,6 +690,7 @@ gemm_status_t gemm_plan_destroy(gemm_plan_t plan) {
         if (plan->d_counters) cudaFree(plan->d_counters);
         if (plan->d_flags) cudaFree(plan->d_flags);
     }
+    delete plan->tuned;
     delete plan;
     return GEMM_OK;
 }

@@ -69,6 +69,10 @@ inline int out_slot(gemm_dtype_t acc, gemm_dtype_t out) {
 
 }  // namespace tcdt_host
 
+namespace tcdt_host {
+struct TunedTable;   // gemm_plan_autotune's results, keyed by problem shape (gemm_api.cu)
+}
+
 struct gemm_plan {
     int device = 0;
     int sm_count = 0;
@@ -88,6 +92,9 @@ struct gemm_plan {
     int64_t fi_skip_load = -1;    // test builds only
 #endif
     int forced_splits = 0;
+    int forced_division = 0;      // gemm_plan_force_division (0: any)
+    int forced_division_splits = 0;
+    tcdt_host::TunedTable* tuned = nullptr;   // owned; null until the first gemm_plan_autotune
 };
 
 namespace tcdt_host {

@@ -1352,9 +1352,17 @@ gemm_sm103_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                         // main loop (fp32 output: ~547 -> ~524 cycles per K block).
                         staged = true;
                         const int row0w = m0 + 32 * quad;
+                        // The window is half the time the next item is expected to take:
+                        // this item's time scaled by the ratio of their K lengths (an
+                        // early-split owner or a short split that follows must not wait
+                        // behind a window sized for a whole tile).
                         const uint64_t t_acc = globaltimer_ns();
-                        const uint64_t gap = (iter + 1 < num_items && x.kb1 - x.kb0 >= 32)
-                                                 ? (t_acc - t_prev_acc) / static_cast<uint64_t>(2 * nchunks) : 0;
+                        uint64_t gap = 0;
+                        if (iter + 1 < num_items && x.kb1 - x.kb0 >= 32) {
+                            const WorkItem y = unit_item(p, unit, num_units, iter + 1);
+                            gap = (t_acc - t_prev_acc) * static_cast<uint64_t>(y.kb1 - y.kb0) /
+                                  (static_cast<uint64_t>(x.kb1 - x.kb0) * static_cast<uint64_t>(2 * nchunks));
+                        }
                         t_prev_acc = t_acc;
 #pragma unroll 1
                         for (int c = 0; c < nchunks; ++c) {

@@ -111,15 +111,17 @@ def W(name, M, N, K, dt="f16", la="row", lb="row", acc="f32", out="f32", alpha=1
 
 
 PATHS = {
-    # name: (workload, expected substring of the configuration, or None)
-    "tma_store": (W("tma_store", 300, 600, 328), None),
-    "tma_store_bf16_with_c": (W("tma_bf16c", 300, 608, 328, dt="bf16", out="bf16", alpha=0.5, beta=1.0), None),
-    "coalesced_fp32_c": (W("coal_c", 300, 600, 328, alpha=0.5, beta=1.0), None),
-    "coalesced_unaligned": (W("coal_u", 257, 263, 200, lb="col"), None),
-    "transposed_split": (W("skinny", 16, 1104, 4096, dt="bf16", out="bf16", alpha=0.5, beta=1.0), "swapAB_splitk"),
-    "early_split": (W("early", 2300, 2290, 800, alpha=0.5, beta=1.0), "esplitk"),
-    "half_width": (W("halves", 1024, 1024, 1024, dt="bf16", out="bf16"), "nhalves"),
-    "fp16_accumulate": (W("acc16", 270, 530, 256, lb="col", acc="f16", out="f16"), None),
+    # name: (workload, division pinned for it (or None), expected substring of the configuration)
+    "tma_store": (W("tma_store", 300, 600, 328), None, None),
+    "tma_store_bf16_with_c": (W("tma_bf16c", 300, 608, 328, dt="bf16", out="bf16", alpha=0.5, beta=1.0), None,
+                              None),
+    "coalesced_fp32_c": (W("coal_c", 300, 600, 328, alpha=0.5, beta=1.0), None, None),
+    "coalesced_unaligned": (W("coal_u", 257, 263, 200, lb="col"), None, None),
+    "transposed_split": (W("skinny", 16, 1104, 4096, dt="bf16", out="bf16", alpha=0.5, beta=1.0), "split",
+                         "swapAB_splitk"),
+    "early_split": (W("early", 2300, 2290, 800, alpha=0.5, beta=1.0), "early_split", "esplitk"),
+    "half_width": (W("halves", 1024, 1024, 1024, dt="bf16", out="bf16"), "halves", "nhalves"),
+    "fp16_accumulate": (W("acc16", 270, 530, 256, lb="col", acc="f16", out="f16"), None, None),
 }
 KINDS = ["bias", "scale", "bias_relu", "scale_bias_gelu"]
 
@@ -132,10 +134,8 @@ def _padded(w):
 @pytest.mark.parametrize("kind", KINDS)
 @pytest.mark.parametrize("integer", [False, True], ids=["random", "twin"])
 def test_epilogue_paths(plans, path, kind, integer):
-    w, want = PATHS[path]
+    w, division, want = PATHS[path]
     plan = plans[w.in_dtype]
-    if want:
-        assert want in plan.describe(w.M, w.N, w.K, w.layoutA, w.layoutB, w.accum_dtype, w.out_dtype)
     lda, ldb = _padded(w)
     h = wl.make_inputs(w, integer=integer, lda=lda, ldb=ldb)
     ep = make_ep(w, kind, integer)
@@ -143,8 +143,15 @@ def test_epilogue_paths(plans, path, kind, integer):
         # fp16 accumulation is exact only up to 2048: keep the scaled sums small
         ep["row_scale"] = np.where(np.abs(ep["row_scale"]) > 1, 1.0, ep["row_scale"]).astype(np.float32)
         ep["col_scale"] = np.where(np.abs(ep["col_scale"]) > 1, 1.0, ep["col_scale"]).astype(np.float32)
-    D = run_ep(plan, w, h, ep)
-    torch.cuda.synchronize()
+    if division:
+        plan.force_division(division)
+    try:
+        if want:
+            assert want in plan.describe(w.M, w.N, w.K, w.layoutA, w.layoutB, w.accum_dtype, w.out_dtype)
+        D = run_ep(plan, w, h, ep)
+        torch.cuda.synchronize()
+    finally:
+        plan.force_division("auto")
     got = out_bits(D[:, :w.N])
     Dref, V, S = oracle_ep(w, h, ep)
     compare(w, ep, integer, got, Dref, V, S, f"{path}/{kind}")
@@ -155,11 +162,15 @@ def test_epilogue_last_arriver_split_sampled(plans):
     epilogue (sampled entries, integer twin with ReLU and bias)."""
     w = W("splitk", 1024, 1024, 16384, dt="bf16", out="bf16")
     plan = plans["bf16"]
-    assert "_splitk" in plan.describe(w.M, w.N, w.K, "row", "row", "f32", "bf16")
-    h = wl.make_inputs(w, integer=True)
-    ep = make_ep(w, "scale_bias_relu", integer=True)
-    D = run_ep(plan, w, h, ep)
-    torch.cuda.synchronize()
+    plan.force_division("split")
+    try:
+        assert "_splitk" in plan.describe(w.M, w.N, w.K, "row", "row", "f32", "bf16")
+        h = wl.make_inputs(w, integer=True)
+        ep = make_ep(w, "scale_bias_relu", integer=True)
+        D = run_ep(plan, w, h, ep)
+        torch.cuda.synchronize()
+    finally:
+        plan.force_division("auto")
     rng = np.random.default_rng(3)
     ii = np.concatenate([rng.integers(0, w.M, 3000), [0, w.M - 1, 255, 256]])
     jj = np.concatenate([rng.integers(0, w.N, 3000), [w.N - 1, 0, 256, 255]])

@@ -74,13 +74,17 @@ def test_split_results_repeat_bitwise(plans, shape):
     h = wl.make_inputs(w)
     A, B = h.A.cuda(), h.B.cuda()
     plan = plans["f16"]
-    desc = plan.describe(w.M, w.N, w.K)
-    assert "splitk" in desc, desc
-    D0 = plan.gemm(A, B)
-    for _ in range(10):
-        D1 = plan.gemm(A, B)
-        torch.cuda.synchronize()
-        assert torch.equal(D0, D1)
+    plan.force_division("split")
+    try:
+        desc = plan.describe(w.M, w.N, w.K)
+        assert "splitk" in desc, desc
+        D0 = plan.gemm(A, B)
+        for _ in range(10):
+            D1 = plan.gemm(A, B)
+            torch.cuda.synchronize()
+            assert torch.equal(D0, D1)
+    finally:
+        plan.force_division("auto")
 
 
 def test_configuration_choice(plans):
@@ -153,23 +157,31 @@ def test_pinned_config_that_does_not_fit(plans):
         plan.force_config("auto")
 
 
+DIVISIONS = {"split": "_splitk", "early_split": "_esplitk", "halves": "_nhalves"}
+
+
 @pytest.mark.parametrize("shape", [(4096, 4096, 1024), (2560, 2560, 2048), (3000, 3496, 1504)],
                          ids=lambda s: "x".join(map(str, s)))
 @pytest.mark.parametrize("layouts", LAYOUTS, ids=lambda l: "".join(x[0] for x in l))
 @pytest.mark.parametrize("out", ["f32", "bf16"])
-def test_partial_wave_divided(plans, shape, layouts, out):
+@pytest.mark.parametrize("division", sorted(DIVISIONS))
+def test_partial_wave_divided(plans, shape, layouts, out, division):
     """Whole waves of tiles run whole; the tiles of the last, partial wave are
-    divided (split along K, or run as two half-width items, whichever the plan
-    picks): sampled entries bit-exact on the integer twin."""
+    divided in each pinned way (split along K with a last-arriver reduction,
+    split with early partials, or two half-width items): sampled entries
+    bit-exact on the integer twin."""
     from gpu_util import check_sampled
     w = W(*shape, *layouts, out=out, alpha=0.5, beta=1.0)
     plan = plans["f16"]
-    desc = plan.describe(w.M, w.N, w.K, w.layoutA, w.layoutB, "f32", out)
-    if w.layoutB == "row":
-        assert "divided_tiles=0" not in desc, desc
-    h = wl.make_inputs(w, integer=True)
-    D = run_gpu(plan, w, h)
-    torch.cuda.synchronize()
+    plan.force_division(division)
+    try:
+        desc = plan.describe(w.M, w.N, w.K, w.layoutA, w.layoutB, "f32", out)
+        assert DIVISIONS[division] in desc and "divided_tiles=0" not in desc, desc
+        h = wl.make_inputs(w, integer=True)
+        D = run_gpu(plan, w, h)
+        torch.cuda.synchronize()
+    finally:
+        plan.force_division("auto")
     check_sampled(w, h, D, integer=True, n_random=4096)
 
 
@@ -186,12 +198,16 @@ def test_early_split_integer_twin(plans, shape, out):
     from gpu_util import check_sampled
     w = W(*shape, "row", "row", out=out, alpha=0.5, beta=1.0)
     plan = plans["f16"]
-    desc = plan.describe(w.M, w.N, w.K, w.layoutA, w.layoutB, "f32", out)
-    assert "esplitk" in desc, desc
-    lda, ldb = padded(w)
-    h = wl.make_inputs(w, integer=True, lda=lda, ldb=ldb)
-    D = run_gpu(plan, w, h)
-    torch.cuda.synchronize()
+    plan.force_division("early_split")
+    try:
+        desc = plan.describe(w.M, w.N, w.K, w.layoutA, w.layoutB, "f32", out)
+        assert "esplitk" in desc, desc
+        lda, ldb = padded(w)
+        h = wl.make_inputs(w, integer=True, lda=lda, ldb=ldb)
+        D = run_gpu(plan, w, h)
+        torch.cuda.synchronize()
+    finally:
+        plan.force_division("auto")
     if w.M * w.N * w.K <= 5e9:
         check_full(w, h, D, integer=True)
     else:
@@ -203,13 +219,36 @@ def test_early_split_random_repeats_bitwise(plans):
     bit-identical from call to call (partials are summed in split order)."""
     w = W(2300, 2290, 800, "col", "row", out="f32", alpha=0.5, beta=1.0)
     plan = plans["f16"]
-    assert "esplitk" in plan.describe(w.M, w.N, w.K, w.layoutA, w.layoutB, "f32", "f32")
-    lda, ldb = padded(w)
-    h = wl.make_inputs(w, lda=lda, ldb=ldb)
-    D0 = run_gpu(plan, w, h)
-    torch.cuda.synchronize()
-    check_full(w, h, D0, integer=False)
-    for _ in range(5):
-        D1 = run_gpu(plan, w, h)
+    plan.force_division("early_split")
+    try:
+        assert "esplitk" in plan.describe(w.M, w.N, w.K, w.layoutA, w.layoutB, "f32", "f32")
+        lda, ldb = padded(w)
+        h = wl.make_inputs(w, lda=lda, ldb=ldb)
+        D0 = run_gpu(plan, w, h)
         torch.cuda.synchronize()
-        assert torch.equal(D0, D1)
+        check_full(w, h, D0, integer=False)
+        for _ in range(5):
+            D1 = run_gpu(plan, w, h)
+            torch.cuda.synchronize()
+            assert torch.equal(D0, D1)
+    finally:
+        plan.force_division("auto")
+
+
+def test_pinned_division_that_does_not_fit(plans):
+    """Early partials need a whole wave first and fp32 accumulation."""
+    import tensor_core_dense_tma_gb300 as tc
+    plan = plans["f16"]
+    plan.force_division("early_split")
+    try:
+        with pytest.raises(tc.GemmError) as e:
+            plan.describe(512, 512, 1024)          # 4 tiles: no whole wave
+        assert e.value.status == 2
+        with pytest.raises(tc.GemmError) as e:
+            plan.describe(4096, 4096, 1024, "row", "col", "f16", "f16")
+        assert e.value.status == 2
+    finally:
+        plan.force_division("auto")
+    with pytest.raises(tc.GemmError) as e:
+        plan.force_division(7)
+    assert e.value.status == 1
