@@ -9,9 +9,12 @@ The arithmetic lives in ``oracle.c`` (binary64 triple loop, exact
 binary16/bfloat16 decode, one RNE rounding to the output type); this module
 only compiles it with gcc and marshals numpy arrays through ctypes.
 
-Inputs are numpy arrays: ``uint16`` bit patterns for fp16/bf16 matrices and
-``float32`` for an fp32 C.  Dtype names are the strings ``"f16"``, ``"bf16"``,
-``"f32"``; layouts are ``"row"`` / ``"col"``.
+Inputs are numpy arrays: ``uint16`` bit patterns for fp16/bf16 matrices,
+``uint8`` bit patterns for the 8-bit float formats E4M3 / E5M2, ``uint32``
+(or ``float32``) words for TF32 operands (stored as binary32), and
+``float32`` for an fp32 C.  Dtype names are the strings ``"f16"``,
+``"bf16"``, ``"f32"``, ``"e4m3"``, ``"e5m2"``, ``"tf32"``; layouts are
+``"row"`` / ``"col"``.
 """
 from __future__ import annotations
 
@@ -27,7 +30,7 @@ _SRC = os.path.join(_HERE, "oracle.c")
 _OUT_DIR = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_OUT_DIR, "liboracle.so")
 
-_DT = {"f16": 0, "bf16": 1, "f32": 2}
+_DT = {"f16": 0, "bf16": 1, "f32": 2, "e4m3": 3, "e5m2": 4, "tf32": 5}
 _LAYOUT = {"row": 0, "col": 1}
 
 # -ffp-contract=off: no fused multiply-add, so x86 and Arm hosts produce the
@@ -59,6 +62,12 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.oracle_f16_encode.restype = ctypes.c_uint16
     lib.oracle_bf16_encode.argtypes = [f64]
     lib.oracle_bf16_encode.restype = ctypes.c_uint16
+    lib.oracle_e4m3_decode.argtypes = [ctypes.c_uint8]
+    lib.oracle_e4m3_decode.restype = f64
+    lib.oracle_e5m2_decode.argtypes = [ctypes.c_uint8]
+    lib.oracle_e5m2_decode.restype = f64
+    lib.oracle_f32_decode.argtypes = [ctypes.c_uint32]
+    lib.oracle_f32_decode.restype = f64
     lib.oracle_gemm.argtypes = [i32, p, p, p, p, i64, p, p, i64, i64, i64, i64, i64, i64,
                                 i32, i32, i32, f64, f64, i32]
     lib.oracle_gemm.restype = i32
@@ -94,10 +103,18 @@ def _ptr(a: np.ndarray | None) -> int | None:
     return None if a is None else a.ctypes.data
 
 
-def _in_bits(a: np.ndarray) -> np.ndarray:
+_IN_NP = {"f16": np.uint16, "bf16": np.uint16, "e4m3": np.uint8, "e5m2": np.uint8, "tf32": np.uint32}
+
+
+def _in_bits(a: np.ndarray, dtype: str = "f16") -> np.ndarray:
+    """Bit patterns of an input matrix of the given type (float32 arrays are
+    taken as TF32 operands' words)."""
     a = np.ascontiguousarray(a)
-    if a.dtype != np.uint16:
-        raise TypeError(f"fp16/bf16 inputs are passed as uint16 bit patterns, got {a.dtype}")
+    if dtype == "tf32" and a.dtype == np.float32:
+        a = a.view(np.uint32)
+    want = _IN_NP[dtype]
+    if a.dtype != want:
+        raise TypeError(f"{dtype} inputs are passed as {np.dtype(want)} bit patterns, got {a.dtype}")
     return a
 
 
@@ -140,8 +157,8 @@ def gemm(in_dtype: str, A: np.ndarray, B: np.ndarray, C: np.ndarray | None,
     epilogue (float32 vectors bias[N], row_scale[M], col_scale[N] and
     act in none/relu/gelu) is applied as oracle.c defines it."""
     lib = lib or load_library()
-    A = _in_bits(A)
-    B = _in_bits(B)
+    A = _in_bits(A, in_dtype)
+    B = _in_bits(B, in_dtype)
     Cc = _c_array(C, out_dtype)
     bv, rv, cv = _vec(bias, N, "bias"), _vec(row_scale, M, "row_scale"), _vec(col_scale, N, "col_scale")
     D = np.zeros((M, N), dtype=_out_np_dtype(out_dtype))
@@ -168,8 +185,8 @@ def gemm_entries(in_dtype: str, A: np.ndarray, B: np.ndarray, C: np.ndarray | No
     rounded values (out_dtype storage), the unrounded binary64 values and
     the error scale."""
     lib = lib or load_library()
-    A = _in_bits(A)
-    B = _in_bits(B)
+    A = _in_bits(A, in_dtype)
+    B = _in_bits(B, in_dtype)
     Cc = _c_array(C, out_dtype)
     bv, rv, cv = _vec(bias, N, "bias"), _vec(row_scale, M, "row_scale"), _vec(col_scale, N, "col_scale")
     ii = np.ascontiguousarray(rows, dtype=np.int64)
@@ -198,9 +215,10 @@ def round_to(v: np.ndarray, out_dtype: str, lib: ctypes.CDLL | None = None) -> n
 
 
 def decode(bits: np.ndarray, dtype: str, lib: ctypes.CDLL | None = None) -> np.ndarray:
-    """Exact binary64 values of fp16/bf16 bit patterns."""
+    """Exact binary64 values of input bit patterns (fp16, bf16, e4m3, e5m2,
+    tf32 = binary32 words)."""
     lib = lib or load_library()
-    bits = _in_bits(bits)
+    bits = _in_bits(bits, dtype)
     out = np.zeros(bits.shape, dtype=np.float64)
     lib.oracle_decode(_ptr(bits), bits.size, _DT[dtype], _ptr(out))
     return out

@@ -24,7 +24,15 @@
  *    contiguous extent the offsets become i*ld + j and j*ld + i (same page,
  *    section 4.2, ldm).
  *  - Inputs are IEEE binary16 or bfloat16 bit patterns, decoded exactly to
- *    binary64 from the format definitions (no CUDA header is used).
+ *    binary64 from the format definitions (no CUDA header is used).  The
+ *    other tensor-core input types the pages list for Blackwell ("深入CUDA
+ *    Tensor Core与WMMA", section 2.3: FP8 and TF32) are decoded the same
+ *    way: the two 8-bit float formats E4M3 and E5M2 from their bit layouts,
+ *    and TF32 operands -- stored as binary32 -- as the binary32 value
+ *    itself (the product of the matrices as given; the reduced precision
+ *    with which the tensor cores read them is a property of the device
+ *    path, bounded by the tests' tolerance, and exact for inputs whose low
+ *    13 fraction bits are zero).
  *  - Arithmetic is binary64 throughout.  Every product of two 11-bit (or
  *    8-bit) significands is exact in binary64; the K-sum has a relative
  *    error of at most K * 2^-53, far below any tolerance used against it.
@@ -60,7 +68,7 @@
 #include <string.h>
 
 /* Type and layout codes of this file (independent of the product's enums). */
-enum { OR_F16 = 0, OR_BF16 = 1, OR_F32 = 2 };
+enum { OR_F16 = 0, OR_BF16 = 1, OR_F32 = 2, OR_E4M3 = 3, OR_E5M2 = 4, OR_TF32 = 5 };
 enum { OR_ROW = 0, OR_COL = 1 };
 
 /* ---------------------------------------------------------------------- */
@@ -95,6 +103,55 @@ double oracle_bf16_decode(uint16_t h)
         v = f ? NAN : INFINITY;
     else
         v = ldexp((double)(128 + f), e - 134);
+    return s ? -v : v;
+}
+
+/* E4M3: 1 sign bit, 4 exponent bits (bias 7), 3 fraction bits; no
+ * infinities, exponent 15 with fraction 7 is NaN (so the largest finite
+ * value is 1.75 * 2^8 = 448).
+ * normal:    (8 + f) * 2^(e-10);  subnormal: f * 2^-9                   */
+double oracle_e4m3_decode(uint8_t h)
+{
+    int s = (h >> 7) & 1, e = (h >> 3) & 0xf, f = h & 0x7;
+    double v;
+    if (e == 0)
+        v = ldexp((double)f, -9);
+    else if (e == 15 && f == 7)
+        v = NAN;
+    else
+        v = ldexp((double)(8 + f), e - 10);
+    return s ? -v : v;
+}
+
+/* E5M2: 1 sign bit, 5 exponent bits (bias 15), 2 fraction bits; exponent
+ * 31 holds infinities (fraction 0) and NaNs, as in binary16.
+ * normal:    (4 + f) * 2^(e-17);  subnormal: f * 2^-16                  */
+double oracle_e5m2_decode(uint8_t h)
+{
+    int s = (h >> 7) & 1, e = (h >> 2) & 0x1f, f = h & 0x3;
+    double v;
+    if (e == 0)
+        v = ldexp((double)f, -16);
+    else if (e == 31)
+        v = f ? NAN : INFINITY;
+    else
+        v = ldexp((double)(4 + f), e - 17);
+    return s ? -v : v;
+}
+
+/* binary32: 1 sign bit, 8 exponent bits (bias 127), 23 fraction bits.
+ * normal:    (2^23 + f) * 2^(e-150);  subnormal: f * 2^-149             */
+double oracle_f32_decode(uint32_t w)
+{
+    int s = (w >> 31) & 1, e = (w >> 23) & 0xff;
+    uint32_t f = w & 0x7fffffu;
+    double v;
+    if (e == 0)
+        v = ldexp((double)f, -149);
+    else if (e == 255)
+        v = f ? NAN : INFINITY;
+    else
+        v = ldexp((double)(8388608u + f), e - 150);
     return s ? -v : v;
 }
 
@@ -145,8 +202,8 @@ uint16_t oracle_bf16_encode(double x) { return encode_rne(x, 7, 8); }
 /* ---------------------------------------------------------------------- */
 
 typedef struct {
-    int in_dtype;               /* OR_F16 or OR_BF16 */
-    const uint16_t *A, *B;      /* bit patterns */
+    int in_dtype;               /* OR_F16, OR_BF16, OR_E4M3, OR_E5M2 or OR_TF32 */
+    const void *A, *B;          /* bit patterns: 16-bit, 8-bit or 32-bit elements */
     const void *C;              /* out_dtype elements, row-major, ld = ldc; may be NULL if beta == 0 */
     int64_t M, N, K, lda, ldb, ldc;
     int layoutA, layoutB;       /* OR_ROW / OR_COL */
@@ -166,18 +223,29 @@ static double decode_in(int dt, uint16_t h)
     return dt == OR_F16 ? oracle_f16_decode(h) : oracle_bf16_decode(h);
 }
 
+/* element `off` of an input matrix of type dt */
+static double input_at(int dt, const void *m, int64_t off)
+{
+    switch (dt) {
+    case OR_E4M3: return oracle_e4m3_decode(((const uint8_t *)m)[off]);
+    case OR_E5M2: return oracle_e5m2_decode(((const uint8_t *)m)[off]);
+    case OR_TF32: return oracle_f32_decode(((const uint32_t *)m)[off]);
+    default: return decode_in(dt, ((const uint16_t *)m)[off]);
+    }
+}
+
 /* a(i,k): element (i,k) of the M x K matrix A in its storage order */
 static double a_at(const gemm_args *g, int64_t i, int64_t k)
 {
     int64_t off = g->layoutA == OR_ROW ? i * g->lda + k : k * g->lda + i;
-    return decode_in(g->in_dtype, g->A[off]);
+    return input_at(g->in_dtype, g->A, off);
 }
 
 /* b(k,j): element (k,j) of the K x N matrix B in its storage order */
 static double b_at(const gemm_args *g, int64_t k, int64_t j)
 {
     int64_t off = g->layoutB == OR_ROW ? k * g->ldb + j : j * g->ldb + k;
-    return decode_in(g->in_dtype, g->B[off]);
+    return input_at(g->in_dtype, g->B, off);
 }
 
 /* c(i,j): element (i,j) of the row-major M x N matrix C */
@@ -275,7 +343,8 @@ static void *run_entries(void *p)
 
 static int check(const gemm_args *g)
 {
-    if (g->in_dtype != OR_F16 && g->in_dtype != OR_BF16)
+    if (g->in_dtype != OR_F16 && g->in_dtype != OR_BF16 && g->in_dtype != OR_E4M3 && g->in_dtype != OR_E5M2 &&
+        g->in_dtype != OR_TF32)
         return 1;
     if (g->out_dtype != OR_F16 && g->out_dtype != OR_BF16 && g->out_dtype != OR_F32)
         return 1;
@@ -305,7 +374,7 @@ static int clamp_threads(int nthreads, int64_t units)
 
 /* Full product with the fused epilogue.  D (ldd), V and S may each be NULL.
  * Rows [0, M) are split over `nthreads` threads.  Returns 0 on success. */
-int oracle_gemm_ep(int in_dtype, const uint16_t *A, const uint16_t *B, const void *C,
+int oracle_gemm_ep(int in_dtype, const void *A, const void *B, const void *C,
                    void *D, int64_t ldd, double *V, double *S,
                    int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
                    int layoutA, int layoutB, int out_dtype, double alpha, double beta,
@@ -338,7 +407,7 @@ int oracle_gemm_ep(int in_dtype, const uint16_t *A, const uint16_t *B, const voi
 }
 
 /* Full product, plain epilogue (D = alpha A B + beta C). */
-int oracle_gemm(int in_dtype, const uint16_t *A, const uint16_t *B, const void *C,
+int oracle_gemm(int in_dtype, const void *A, const void *B, const void *C,
                 void *D, int64_t ldd, double *V, double *S,
                 int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
                 int layoutA, int layoutB, int out_dtype, double alpha, double beta,
@@ -349,7 +418,7 @@ int oracle_gemm(int in_dtype, const uint16_t *A, const uint16_t *B, const void *
 }
 
 /* Selected entries (ii[e], jj[e]) only, with the fused epilogue: V and S. */
-int oracle_gemm_entries_ep(int in_dtype, const uint16_t *A, const uint16_t *B, const void *C,
+int oracle_gemm_entries_ep(int in_dtype, const void *A, const void *B, const void *C,
                            const int64_t *ii, const int64_t *jj, int64_t n_entries,
                            double *V, double *S,
                            int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
@@ -386,7 +455,7 @@ int oracle_gemm_entries_ep(int in_dtype, const uint16_t *A, const uint16_t *B, c
 }
 
 /* Selected entries, plain epilogue. */
-int oracle_gemm_entries(int in_dtype, const uint16_t *A, const uint16_t *B, const void *C,
+int oracle_gemm_entries(int in_dtype, const void *A, const void *B, const void *C,
                         const int64_t *ii, const int64_t *jj, int64_t n_entries,
                         double *V, double *S,
                         int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
@@ -408,9 +477,9 @@ int oracle_round(const double *v, int64_t n, int out_dtype, void *out)
     return 0;
 }
 
-/* Vector decoders for the tests. */
-void oracle_decode(const uint16_t *h, int64_t n, int dtype, double *out)
+/* Vector decoders for the tests (elements of the input type's width). */
+void oracle_decode(const void *h, int64_t n, int dtype, double *out)
 {
     for (int64_t e = 0; e < n; ++e)
-        out[e] = decode_in(dtype, h[e]);
+        out[e] = input_at(dtype, h, e);
 }

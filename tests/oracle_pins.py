@@ -17,6 +17,11 @@ What each pin checks against:
   * layout pin         -- the 2x3 example of the pages (tests/golden).
   * epilogue pins      -- alpha/beta on integer data against numpy; beta == 0
                           never reads C.
+  * 8-bit / tf32 pins  -- every E4M3 and E5M2 pattern against torch's
+                          float8 conversions and the formats' fixed values;
+                          binary32 words against numpy; integer products of
+                          E4M3 / E5M2 / TF32 operands against numpy's int64
+                          matmul; real TF32 operands against float64 matmul.
 """
 from __future__ import annotations
 
@@ -446,6 +451,105 @@ def pin_activation_after_bias(lib):
     x = np.array([[-1.0, 1.0]])
     V, _ = _ep_identity(lib, x, act="relu", bias=np.array([2.0, -2.0], dtype=np.float32))
     assert np.array_equal(V, np.array([[1.0, 0.0]]))
+
+
+# --------------------------------------------------------------------------
+# 8-bit float and TF32 operands
+# --------------------------------------------------------------------------
+
+def pin_e4m3_known_values(lib):
+    """E4M3 (bias 7, no infinities): 1.0, the largest finite 448, the
+    smallest subnormal 2^-9 and normal 2^-6, NaN only at S.1111.111."""
+    d = lambda h: lib.oracle_e4m3_decode(h)
+    assert d(0x38) == 1.0 and d(0xB8) == -1.0
+    assert d(0x7E) == 448.0 and d(0x78) == 256.0
+    assert d(0x01) == 2.0 ** -9 and d(0x07) == 7 * 2.0 ** -9
+    assert d(0x08) == 2.0 ** -6
+    assert math.isnan(d(0x7F)) and math.isnan(d(0xFF))
+    assert d(0x00) == 0.0 and math.copysign(1.0, d(0x80)) == -1.0
+
+
+def pin_e5m2_known_values(lib):
+    """E5M2 (bias 15): 1.0, the largest finite 57344, infinities at
+    exponent 31 with fraction 0, the smallest subnormal 2^-16."""
+    d = lambda h: lib.oracle_e5m2_decode(h)
+    assert d(0x3C) == 1.0
+    assert d(0x7B) == 57344.0
+    assert d(0x7C) == math.inf and d(0xFC) == -math.inf
+    assert math.isnan(d(0x7D)) and math.isnan(d(0x7F))
+    assert d(0x01) == 2.0 ** -16 and d(0x04) == 2.0 ** -14
+
+
+def pin_fp8_decode_matches_torch(lib):
+    """All 256 patterns of each 8-bit format against torch's float8 types."""
+    import torch
+    bits = np.arange(256, dtype=np.uint8)
+    for name, tdt in (("e4m3", torch.float8_e4m3fn), ("e5m2", torch.float8_e5m2)):
+        got = oracle.decode(bits, name, lib=lib)
+        want = torch.from_numpy(bits.copy()).view(tdt).to(torch.float64).numpy()
+        same = (got == want) | (np.isnan(got) & np.isnan(want))
+        assert same.all(), (name, np.flatnonzero(~same)[:5])
+
+
+def pin_binary32_decode_matches_numpy(lib):
+    """TF32 operands are binary32 words: random words and the special ones
+    decode to numpy's float32 values."""
+    rng = np.random.default_rng(31)
+    w = np.concatenate([rng.integers(0, 2 ** 32, 20000, dtype=np.uint64).astype(np.uint32),
+                        np.array([0, 0x80000000, 1, 0x007FFFFF, 0x00800000, 0x7F7FFFFF, 0x7F800000,
+                                  0xFF800000, 0x3F800000, 0x3F802000], dtype=np.uint32)])
+    got = oracle.decode(w, "tf32", lib=lib)
+    want = w.view(np.float32).astype(np.float64)
+    assert ((got == want) | (np.isnan(got) & np.isnan(want))).all()
+
+
+def _fp8_bits(x, name):
+    import torch
+    tdt = torch.float8_e4m3fn if name == "e4m3" else torch.float8_e5m2
+    return torch.from_numpy(np.asarray(x, dtype=np.float32).copy()).to(tdt).view(torch.uint8).numpy()
+
+
+def pin_narrow_inputs_integer_matmul(lib):
+    """Integer operands in E4M3, E5M2 and TF32 (A row-major, B column-major,
+    padded leading dimensions): the product equals numpy's int64 matmul,
+    on the m16n8k16 tile and a ragged 19 x 13 x 40 case."""
+    rng = np.random.default_rng(33)
+    for (M, N, K) in ((16, 8, 16), (19, 13, 40)):
+        a = _int_matrix(rng, M, K, -8, 8)
+        b = _int_matrix(rng, K, N, -8, 8)
+        want = (a.astype(np.int64) @ b.astype(np.int64)).astype(np.float64)
+        for name in ("e4m3", "e5m2", "tf32"):
+            if name == "tf32":
+                A = a.astype(np.float32).view(np.uint32)
+                B = b.T.astype(np.float32).view(np.uint32)
+                pad = 0x7FC00000
+            else:
+                A = _fp8_bits(a, name)
+                B = _fp8_bits(b.T, name)
+                pad = 0x7F
+            Ab, lda = _store(A, "row", K + 4, pad_bits=pad)
+            Bb, ldb = _store(B.T, "col", K + 4, pad_bits=pad)
+            D, V, S = oracle.gemm(name, Ab, Bb, None, M, N, K, lda, ldb, N, "row", "col", "f32",
+                                  want_exact=True, lib=lib)
+            assert np.array_equal(V, want), name
+            assert np.array_equal(S, np.abs(a).astype(np.float64) @ np.abs(b).astype(np.float64)), name
+
+
+def pin_tf32_real_against_float64_matmul(lib):
+    """Real TF32-exact operands (10 fraction bits): the oracle's exact value
+    agrees with numpy's float64 matmul to its rounding error."""
+    rng = np.random.default_rng(34)
+    M, N, K = 24, 17, 64
+    a = rng.standard_normal((M, K)).astype(np.float32)
+    b = rng.standard_normal((K, N)).astype(np.float32)
+    keep = np.uint32(0xFFFFE000)   # clear the 13 low fraction bits
+    a = (a.view(np.uint32) & keep).view(np.float32)
+    b = (b.view(np.uint32) & keep).view(np.float32)
+    D, V, S = oracle.gemm("tf32", a.view(np.uint32), np.ascontiguousarray(b.T).view(np.uint32), None,
+                          M, N, K, K, K, N, "row", "col", "f32", want_exact=True, lib=lib)
+    want = a.astype(np.float64) @ b.astype(np.float64)
+    assert np.allclose(V, want, rtol=1e-13, atol=1e-13)
+    assert np.array_equal(D, V.astype(np.float32))
 
 
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

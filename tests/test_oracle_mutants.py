@@ -42,6 +42,12 @@ MUTANTS = {
                                 "v = 0.5 * v * (1.0 + tanh(0.7978845608028654 * (v + 0.044715 * v * v * v)));"),
     "relu_as_abs": ("v = v > 0.0 ? v : 0.0;", "v = fabs(v);"),
     "activation_ignored": ("if (g->act == OR_ACT_RELU)", "if (0)"),
+    "e4m3_bias": ("ldexp((double)(8 + f), e - 10)", "ldexp((double)(8 + f), e - 9)"),
+    "e4m3_without_nan": ("else if (e == 15 && f == 7)", "else if (0)"),
+    "e5m2_subnormal_scale": ("ldexp((double)f, -16)", "ldexp((double)f, -17)"),
+    "e5m2_read_as_e4m3": ("case OR_E5M2: return oracle_e5m2_decode", "case OR_E5M2: return oracle_e4m3_decode"),
+    "tf32_low_bits_dropped": ("ldexp((double)(8388608u + f), e - 150)",
+                              "ldexp((double)(8388608u + (f & 0x7fe000u)), e - 150)"),
 }
 
 
