@@ -34,6 +34,10 @@ if ROOT not in sys.path:
 
 METRIC = "HGEMM TFLOP/s at M=N=K=4096 fp16→fp32 acc; % of GB300 dense FP16 tensor peak"
 NOMINAL_DENSE_FP16_TFLOPS = 2250.0       # GB300 dense fp16/bf16 tensor peak (datasheet)
+# datasheet dense rates of the other operand kinds relative to fp16/bf16
+# (fp8 4.5 PFLOP/s, tf32 1.1 PFLOP/s): the measured bf16 peak times this
+# ratio is the roofline peak of a kind with no measurement of its own
+NOMINAL_RATIO = {"f16": 1.0, "bf16": 1.0, "e4m3": 2.0, "e5m2": 2.0, "tf32": 1100.0 / 2250.0}
 FALLBACK_BF16_TFLOPS = 1900.0            # used only when no measured peak file is present
 FALLBACK_HBM_GBS = 6800.0
 L2_FLUSH_BYTES = 256 << 20
@@ -77,6 +81,14 @@ def select_workload(args):
     if over:
         w = dataclasses.replace(w, name=w.name + "+" + ",".join(f"{k}={v}" for k, v in over.items()), **over)
     return w
+
+
+def metric_for(w) -> str:
+    """The headline metric for its own workload; a plain description for the others."""
+    if w.name == "sq4096":
+        return METRIC
+    return (f"GEMM TFLOP/s at M={w.M} N={w.N} K={w.K} {w.in_dtype}->{w.accum_dtype} acc->{w.out_dtype} "
+            f"(2*M*N*K per step)")
 
 
 def measured_peaks():
@@ -247,7 +259,7 @@ def run_reference(args):
     flops = 2.0 * rows * w.N * w.K * args.steps
     val = flops / dt / 1e12
     out = {
-        "impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "impl": "reference", "metric": metric_for(w), "value": val, "unit": "TFLOP/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
@@ -412,13 +424,16 @@ def main():
     peaks, peak_src = measured_peaks()
     avg_s = ms_per_step * 1e-3
     achieved = w.flops / avg_s / 1e12
-    peak = float(peaks.get("bf16_tflops", FALLBACK_BF16_TFLOPS))   # fp16 dense rate = bf16 dense rate
+    ratio = NOMINAL_RATIO[w.in_dtype]
+    peak = float(peaks.get("bf16_tflops", FALLBACK_BF16_TFLOPS)) * ratio   # fp16 dense rate = bf16 dense rate
     kernel_tag = plan.describe(w.M, w.N, w.K, w.layoutA, w.layoutB, w.accum_dtype, w.out_dtype).split()[0]
     traffic = traffic_from_profiles(kernel_tag)
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak, "traffic": traffic,
-                "peak_source": f"{peak_src} bf16 dense GEMM burst (MEASURED_PEAKS.json), fp16:bf16 = 1:1"
-                               if peak_src == "measured" else "fallback 1.9 PFLOP/s bf16 burst",
+                "peak_source": (f"{peak_src} bf16 dense GEMM burst (MEASURED_PEAKS.json)"
+                                if peak_src == "measured" else "fallback 1.9 PFLOP/s bf16 burst")
+                               + (", fp16:bf16 = 1:1" if ratio == 1.0 else
+                                  f", x {ratio:.3g} = the datasheet ratio of {w.in_dtype} to bf16 dense rates"),
                 "kernel": kernel_tag,
                 "algorithmic": f"2*M*N*K = {w.flops:.4g} flop per launch"}
     try:
@@ -435,9 +450,9 @@ def main():
     if not args.no_cpu_baseline and world == 1:
         cpu = cpu_baseline(w, h)
     out = {
-        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "metric": metric_for(w), "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+        "vs_baseline": None, "dtype": w.in_dtype, "data": "synthetic",
         "config": {
             "workload": workload_desc(w),
             "accumulate": w.accum_dtype, "out": w.out_dtype,
@@ -450,6 +465,7 @@ def main():
             "parallelism": "replicas" if world > 1 else "single",
             "pct_of_nominal_dense_fp16": 100.0 * value / world / NOMINAL_DENSE_FP16_TFLOPS,
             "nominal_dense_fp16_tflops": NOMINAL_DENSE_FP16_TFLOPS,
+            "pct_of_nominal_dense_same_kind": 100.0 * value / world / (NOMINAL_DENSE_FP16_TFLOPS * ratio),
             "kernel_config": plan.describe(w.M, w.N, w.K, w.layoutA, w.layoutB, w.accum_dtype, w.out_dtype),
             "epilogue": args.epilogue,
             "autotune": tuning,

@@ -73,10 +73,34 @@ typedef enum {
 
 typedef enum { GEMM_ROW_MAJOR = 0, GEMM_COL_MAJOR = 1 } gemm_layout_t;
 
-typedef enum { GEMM_F16 = 0, GEMM_BF16 = 1, GEMM_F32 = 2 } gemm_dtype_t;
+/* Element types.  GEMM_F16, GEMM_BF16 and GEMM_F32 serve as input,
+ * accumulator and output types as listed at gemm_run.  The others are input
+ * types only ("深入CUDA Tensor Core与WMMA：从基础原理到高性能混合精度矩阵乘实战",
+ * section 2.3, the architecture table: Blackwell tensor cores take FP8 and
+ * TF32 besides FP16/BF16):
+ *   GEMM_E4M3  8-bit float, 1 sign, 4 exponent (bias 7), 3 mantissa bits;
+ *              no infinities, S.1111.111 is NaN, largest finite 448;
+ *   GEMM_E5M2  8-bit float, 1 sign, 5 exponent (bias 15), 2 mantissa bits;
+ *              IEEE-style infinities and NaNs, largest finite 57344;
+ *   GEMM_TF32  fp32 storage, multiplied by the tensor cores as TF32 (the
+ *              sign, the 8 exponent bits and the top 10 mantissa bits; values
+ *              whose low 13 mantissa bits are zero are used exactly).
+ * The three are multiplied with fp32 accumulation into fp32, fp16 or bf16
+ * outputs, with A row-major and B column-major (both K-contiguous; other
+ * storage orders return GEMM_ERR_UNSUPPORTED), and without the fused
+ * epilogue.  INT8 is not offered: the sm_103a tensor cores have no
+ * tcgen05.mma kind::i8 (ptxas rejects it for this target). */
+typedef enum {
+    GEMM_F16 = 0,
+    GEMM_BF16 = 1,
+    GEMM_F32 = 2,
+    GEMM_E4M3 = 3,
+    GEMM_E5M2 = 4,
+    GEMM_TF32 = 5
+} gemm_dtype_t;
 
 /* Create a plan for `device` (a CUDA ordinal) and input type `in_dtype`
- * (GEMM_F16 or GEMM_BF16).  Queries the device (it must be compute
+ * (GEMM_F16, GEMM_BF16, GEMM_E4M3, GEMM_E5M2 or GEMM_TF32).  Queries the device (it must be compute
  * capability 10.3), allocates the plan's device status word and resolves
  * the driver's tensor-map encoder.  Makes `device` current on the calling
  * thread.  On failure *out is set to NULL. */
@@ -286,15 +310,15 @@ gemm_status_t gemm_run_static_scratch(int device, gemm_dtype_t in_dtype, const v
                                       void *stream);
 
 /* Tensor-core rate probe (no memory traffic): the median number of SM
- * cycles one tcgen05.mma kind::f16 with M = 256 (a CTA pair), N = `n`
- * columns (16..256, a multiple of 16) and K = 16 takes when issued as the
- * GEMM kernel issues it (one elected lane, four MMAs and one commit per
- * stage, a six-deep ring of stage barriers), on every SM pair of `device`,
- * and the SM clock measured meanwhile (cycles per nanosecond x 1000).  Each
- * SM of the pair does 2 * 128 * n * 16 flop per MMA, so the tensor peak at
- * that clock is sm_count * 2 * 128 * n * 16 / cycles_per_mma * sm_mhz * 1e6.
- * in_dtype GEMM_F16 or GEMM_BF16; accum_dtype GEMM_F32, or GEMM_F16 with
- * fp16 input.  Launches its own kernels and synchronises the device; takes
+ * cycles one tcgen05.mma with M = 256 (a CTA pair), N = `n` columns
+ * (16..256, a multiple of 16) and 32 bytes of K (K = 16 for GEMM_F16 /
+ * GEMM_BF16, 32 for GEMM_E4M3 / GEMM_E5M2, 8 for GEMM_TF32) takes when
+ * issued as the GEMM kernel issues it (one elected lane, four MMAs and one
+ * commit per stage, a six-deep ring of stage barriers), on every SM pair of
+ * `device`, and the SM clock measured meanwhile (cycles per nanosecond x
+ * 1000).  Each SM of the pair does 2 * 128 * n * K flop per MMA, so the
+ * tensor peak at that clock is sm_count * 2 * 128 * n * K / cycles_per_mma
+ * * sm_mhz * 1e6.  accum_dtype GEMM_F32, or GEMM_F16 with fp16 input.  Launches its own kernels and synchronises the device; takes
  * a few milliseconds.  Returns GEMM_ERR_TIMEOUT if a wait inside ran out. */
 gemm_status_t gemm_measure_mma_rate(int device, gemm_dtype_t in_dtype, gemm_dtype_t accum_dtype, int n,
                                     double *cycles_per_mma, double *sm_mhz);

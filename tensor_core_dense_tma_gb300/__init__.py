@@ -39,7 +39,9 @@ STATUS = {
     0: "GEMM_OK", 1: "GEMM_ERR_INVALID_ARG", 2: "GEMM_ERR_UNSUPPORTED", 3: "GEMM_ERR_MISALIGNED",
     4: "GEMM_ERR_CUDA", 5: "GEMM_ERR_TIMEOUT", 6: "GEMM_ERR_NO_DEVICE",
 }
-DTYPE = {"f16": 0, "bf16": 1, "f32": 2}
+DTYPE = {"f16": 0, "bf16": 1, "f32": 2, "e4m3": 3, "e5m2": 4, "tf32": 5}
+# K elements of one tcgen05.mma (32 bytes of each operand row)
+MMA_K = {"f16": 16, "bf16": 16, "e4m3": 32, "e5m2": 32, "tf32": 8}
 LAYOUT = {"row": 0, "col": 1}
 
 _lock = threading.Lock()
@@ -248,9 +250,9 @@ def gemm_status_string(status: int) -> str:
 
 def gemm_measure_mma_rate(device: int = 0, in_dtype: str = "f16", accum_dtype: str = "f32",
                           n: int = 256) -> dict:
-    """Tensor-core rate probe (see gemm.h): cycles per 256 x n x 16 MMA on a
-    CTA pair, the SM clock meanwhile, the flop per SM per cycle and the peak
-    at that clock over all SMs."""
+    """Tensor-core rate probe (see gemm.h): cycles per 256 x n x K MMA on a
+    CTA pair (K = 32 bytes of the operand type), the SM clock meanwhile, the
+    flop per SM per cycle and the peak at that clock over all SMs."""
     cyc, mhz = ctypes.c_double(), ctypes.c_double()
     st = load().gemm_measure_mma_rate(device, DTYPE[in_dtype], DTYPE[accum_dtype], n, ctypes.byref(cyc),
                                       ctypes.byref(mhz))
@@ -258,7 +260,7 @@ def gemm_measure_mma_rate(device: int = 0, in_dtype: str = "f16", accum_dtype: s
         raise GemmError(st, "gemm_measure_mma_rate")
     import torch
     sms = torch.cuda.get_device_properties(device).multi_processor_count
-    flop_clk = 2.0 * 128 * n * 16 / cyc.value
+    flop_clk = 2.0 * 128 * n * MMA_K[in_dtype] / cyc.value
     return {"cycles_per_mma": cyc.value, "sm_mhz": mhz.value, "flop_per_clk_per_sm": flop_clk,
             "peak_tflops_at_clock": sms * flop_clk * mhz.value * 1e6 / 1e12, "sms": sms, "n": n,
             "in_dtype": in_dtype, "accum_dtype": accum_dtype}
@@ -271,7 +273,8 @@ _TORCH_DT = {"f16": "float16", "bf16": "bfloat16", "f32": "float32"}
 
 def _dt_name(t) -> str:
     import torch
-    return {torch.float16: "f16", torch.bfloat16: "bf16", torch.float32: "f32"}[t.dtype]
+    return {torch.float16: "f16", torch.bfloat16: "bf16", torch.float32: "f32", torch.float8_e4m3fn: "e4m3",
+            torch.float8_e5m2: "e5m2"}[t.dtype]
 
 
 def _operand_layout(t, what: str):
@@ -394,8 +397,9 @@ class Plan:
         K2, N = B.shape
         if K2 != K:
             raise ValueError("inner dimensions differ")
-        if _dt_name(A) != self.in_dtype or _dt_name(B) != self.in_dtype:
-            raise ValueError(f"A and B must be {self.in_dtype}")
+        want = "f32" if self.in_dtype == "tf32" else self.in_dtype   # tf32 operands are stored as fp32
+        if _dt_name(A) != want or _dt_name(B) != want:
+            raise ValueError(f"A and B must be {want}")
         la, lda = _operand_layout(A, "A")
         lb, ldb = _operand_layout(B, "B")
         if out_dtype is None:

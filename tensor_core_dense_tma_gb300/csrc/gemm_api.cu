@@ -24,11 +24,15 @@ namespace {
 
 constexpr int64_t kMaxDim = 0x7FFFF000;   // TMA coordinates are int32; keep tile origins in range
 
-bool valid_dtype(int d) { return d == GEMM_F16 || d == GEMM_BF16 || d == GEMM_F32; }
+bool valid_dtype(int d) { return d >= GEMM_F16 && d <= GEMM_TF32; }
+bool out_dtype_ok(gemm_dtype_t d) { return d == GEMM_F16 || d == GEMM_BF16 || d == GEMM_F32; }
 bool valid_layout(int l) { return l == GEMM_ROW_MAJOR || l == GEMM_COL_MAJOR; }
 
 gemm_status_t check_types(gemm_dtype_t in, gemm_dtype_t acc, gemm_dtype_t out) {
     if (!valid_dtype(in) || !valid_dtype(acc) || !valid_dtype(out)) return GEMM_ERR_INVALID_ARG;
+    if (!out_dtype_ok(acc) || !out_dtype_ok(out)) return GEMM_ERR_UNSUPPORTED;
+    if (in == GEMM_E4M3 || in == GEMM_E5M2 || in == GEMM_TF32)
+        return acc == GEMM_F32 ? GEMM_OK : GEMM_ERR_UNSUPPORTED;   // -> f32 / f16 / bf16
     if (in == GEMM_F16) {
         if (acc == GEMM_F32) return GEMM_OK;                          // -> f32 / f16 / bf16
         if (acc == GEMM_F16 && out == GEMM_F16) return GEMM_OK;
@@ -38,7 +42,7 @@ gemm_status_t check_types(gemm_dtype_t in, gemm_dtype_t acc, gemm_dtype_t out) {
         if (acc == GEMM_F32 && (out == GEMM_F32 || out == GEMM_BF16)) return GEMM_OK;
         return GEMM_ERR_UNSUPPORTED;
     }
-    return GEMM_ERR_UNSUPPORTED;   // fp32 inputs are not a tensor-core kind::f16 operand
+    return GEMM_ERR_UNSUPPORTED;   // fp32 inputs: ask for GEMM_TF32
 }
 
 gemm_status_t validate(gemm_dtype_t in, const void* A, const void* B, const void* C, const void* D,
@@ -66,13 +70,17 @@ gemm_status_t validate(gemm_dtype_t in, const void* A, const void* B, const void
     const int64_t lda_min = la == GEMM_ROW_MAJOR ? K : M;
     const int64_t ldb_min = lb == GEMM_ROW_MAJOR ? N : K;
     if (lda < lda_min || ldb < ldb_min) return GEMM_ERR_INVALID_ARG;
-    if (lda * 2 >= (int64_t(1) << 40) || ldb * 2 >= (int64_t(1) << 40)) return GEMM_ERR_UNSUPPORTED;
+    // 8-bit and tf32 operands are read K-major only: A row-major, B column-major
+    if (input_kind(in) != tcdt::kInF16 && (la != GEMM_ROW_MAJOR || lb != GEMM_COL_MAJOR))
+        return GEMM_ERR_UNSUPPORTED;
+    const int64_t in_esz = dtype_bytes(in);
+    if (lda * in_esz >= (int64_t(1) << 40) || ldb * in_esz >= (int64_t(1) << 40)) return GEMM_ERR_UNSUPPORTED;
     if (check_pointers) {
         if (!A || !B) return GEMM_ERR_INVALID_ARG;
         if (reinterpret_cast<uintptr_t>(A) % 16 || reinterpret_cast<uintptr_t>(B) % 16)
             return GEMM_ERR_MISALIGNED;
     }
-    if ((lda * 2) % 16 || (ldb * 2) % 16) return GEMM_ERR_MISALIGNED;
+    if ((lda * in_esz) % 16 || (ldb * in_esz) % 16) return GEMM_ERR_MISALIGNED;
     return GEMM_OK;
 }
 
@@ -177,14 +185,15 @@ Choice choose(const gemm_plan* plan, int64_t M, int64_t N, int64_t K, gemm_dtype
     const bool swap = M <= 64 && N > M;
     const int64_t Mk = swap ? N : M, Nk = swap ? M : N;
     const bool bmn = swap ? false : b_mn_major;   // swapped: B is the small A^T, its layout does not matter
-    const int64_t kb = (K + 63) / 64;
+    const int64_t kb = (K + k_block(plan->in_dtype) - 1) / k_block(plan->in_dtype);
     const bool pinned = plan->forced_kind >= 0 && plan->forced_splits > 0;
+    const bool f16_kind = input_kind(plan->in_dtype) == tcdt::kInF16;
     int cands[3];
     int nc = 0;
     if (plan->forced_kind >= 0) {
         const int f = plan->forced_kind;
         const bool f_swap = f == kCfgSingle16 || f == kCfgSingle64;
-        if (f_swap != swap || (f_swap && Nk > kCfgTileN[f])) {
+        if (f_swap != swap || (f_swap && Nk > kCfgTileN[f]) || (!f16_kind && f == kCfgPair224)) {
             *valid = false;
             return best;
         }
@@ -194,7 +203,7 @@ Choice choose(const gemm_plan* plan, int64_t M, int64_t N, int64_t K, gemm_dtype
         if (Nk > 16 || every_kind) cands[nc++] = kCfgSingle64;
     } else {
         cands[nc++] = kCfgPair256;
-        cands[nc++] = kCfgPair224;
+        if (f16_kind) cands[nc++] = kCfgPair224;   // 256 x 224 tiles are built for 16-bit operands only
         cands[nc++] = kCfgSingle256;
     }
     double best_cost = -1.0;
@@ -291,7 +300,12 @@ Choice choose(const gemm_plan* plan, int64_t M, int64_t N, int64_t K, gemm_dtype
     return best;
 }
 
+// Shared-memory opt-in and co-residency of the plan's fp32-output kernels
+// (the others are prepared on first use).  The flags in attr_set are per
+// plan, and a plan has one operand kind: only that kind's kernels are
+// prepared here.
 gemm_status_t prepare_all(gemm_plan* plan) {
+    if (input_kind(plan->in_dtype) != tcdt::kInF16) return GEMM_OK;
     gemm_status_t st = prepare_single16(plan, 0);
     if (st == GEMM_OK) st = prepare_single64(plan, 0);
     if (st == GEMM_OK) st = prepare_single256(plan, 0);
@@ -374,6 +388,26 @@ gemm_status_t run_choice(gemm_plan* plan, const Choice& ch, const void* A, const
                          cudaStream_t s) {
     const Problem pr = make_problem(ch.swap, A, B, M, N, K, lda, ldb, layoutA, layoutB, ep);
     const int slot = out_slot(accum_dtype, out_dtype);
+    const int in_kind = input_kind(plan->in_dtype);
+    if (in_kind != tcdt::kInF16) {
+        if (ep) return GEMM_ERR_UNSUPPORTED;   // the fused epilogue is built for 16-bit operands
+        const bool f8 = in_kind == tcdt::kInF8;
+        switch (ch.kind) {
+            case kCfgSingle16:
+                return f8 ? launch_single16_f8(plan, slot, ch, pr, C, D, ldc, alpha, beta, s)
+                          : launch_single16_tf32(plan, slot, ch, pr, C, D, ldc, alpha, beta, s);
+            case kCfgSingle64:
+                return f8 ? launch_single64_f8(plan, slot, ch, pr, C, D, ldc, alpha, beta, s)
+                          : launch_single64_tf32(plan, slot, ch, pr, C, D, ldc, alpha, beta, s);
+            case kCfgSingle256:
+                return f8 ? launch_single256_f8(plan, slot, ch, pr, C, D, ldc, alpha, beta, s)
+                          : launch_single256_tf32(plan, slot, ch, pr, C, D, ldc, alpha, beta, s);
+            case kCfgPair256:
+                return f8 ? launch_pair256_f8(plan, slot, ch, pr, C, D, ldc, alpha, beta, s)
+                          : launch_pair256_tf32(plan, slot, ch, pr, C, D, ldc, alpha, beta, s);
+            default: return GEMM_ERR_UNSUPPORTED;
+        }
+    }
     if (ep) {
         switch (ch.kind) {
             case kCfgSingle16: return launch_single16_ep(plan, slot, ch, pr, C, D, ldc, alpha, beta, s);
@@ -400,7 +434,7 @@ gemm_status_t gemm_plan_create(gemm_plan_t* out, int device, gemm_dtype_t in_dty
     if (!out) return GEMM_ERR_INVALID_ARG;
     *out = nullptr;
     if (!valid_dtype(in_dtype)) return GEMM_ERR_INVALID_ARG;
-    if (in_dtype == GEMM_F32) return GEMM_ERR_UNSUPPORTED;
+    if (in_dtype == GEMM_F32) return GEMM_ERR_UNSUPPORTED;   // fp32 storage with tensor cores: GEMM_TF32
     int count = 0;
     if (cudaGetDeviceCount(&count) != cudaSuccess || count <= 0) {
         cudaGetLastError();
@@ -653,9 +687,11 @@ gemm_status_t gemm_plan_describe(gemm_plan_t plan, int64_t M, int64_t N, int64_t
                                  char* buf, int64_t len) {
     if (!plan || !buf || len <= 0) return GEMM_ERR_INVALID_ARG;
     const int64_t lda = layoutA == GEMM_ROW_MAJOR ? K : M, ldb = layoutB == GEMM_ROW_MAJOR ? N : K;
+    const int64_t pad = 16 / dtype_bytes(plan->in_dtype);   // leading dimensions taken as 16-byte multiples
     gemm_status_t st = validate(plan->in_dtype, nullptr, nullptr, nullptr, nullptr, M, N, K,
-                                lda < 8 ? 8 : (lda + 7) / 8 * 8, ldb < 8 ? 8 : (ldb + 7) / 8 * 8, N,
-                                layoutA, layoutB, accum_dtype, out_dtype, 0.0f, false);
+                                lda < pad ? pad : (lda + pad - 1) / pad * pad,
+                                ldb < pad ? pad : (ldb + pad - 1) / pad * pad, N, layoutA, layoutB, accum_dtype,
+                                out_dtype, 0.0f, false);
     if (st != GEMM_OK) return st;
     if (M == 0 || N == 0) {
         std::snprintf(buf, static_cast<size_t>(len), "none (empty output)");

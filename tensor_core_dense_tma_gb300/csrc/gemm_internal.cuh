@@ -36,16 +36,32 @@ constexpr int kMaxSplits = 16;
 //  pair256             : CTA pair (cta_group::2), 256 x 256, 6 stages of 32 KB per CTA;
 //  pair224             : CTA pair, 256 x 224 (fills whole waves where 256 leaves a
 //                        partial one, e.g. N = 4096: 19 column tiles x 16 = 4 x 76 pairs).
-template <bool ACC16, int OUT>
-using CfgSingle16 = tcdt::TileConfig<16, 8, 1, ACC16, OUT>;
-template <bool ACC16, int OUT>
-using CfgSingle64 = tcdt::TileConfig<64, 8, 1, ACC16, OUT>;
-template <bool ACC16, int OUT>
-using CfgSingle256 = tcdt::TileConfig<256, 4, 1, ACC16, OUT>;
-template <bool ACC16, int OUT>
-using CfgPair256 = tcdt::TileConfig<256, 6, 2, ACC16, OUT>;
-template <bool ACC16, int OUT>
-using CfgPair224 = tcdt::TileConfig<224, 6, 2, ACC16, OUT>;
+// IN: the operand kind (tcdt::kInF16, kInF8, kInTF32).
+template <bool ACC16, int OUT, int IN = tcdt::kInF16>
+using CfgSingle16 = tcdt::TileConfig<16, 8, 1, ACC16, OUT, IN>;
+template <bool ACC16, int OUT, int IN = tcdt::kInF16>
+using CfgSingle64 = tcdt::TileConfig<64, 8, 1, ACC16, OUT, IN>;
+template <bool ACC16, int OUT, int IN = tcdt::kInF16>
+using CfgSingle256 = tcdt::TileConfig<256, 4, 1, ACC16, OUT, IN>;
+template <bool ACC16, int OUT, int IN = tcdt::kInF16>
+using CfgPair256 = tcdt::TileConfig<256, 6, 2, ACC16, OUT, IN>;
+template <bool ACC16, int OUT, int IN = tcdt::kInF16>
+using CfgPair224 = tcdt::TileConfig<224, 6, 2, ACC16, OUT, IN>;
+
+// Operand types: the tensor-core kind, the element size, and the format
+// field of the instruction descriptor (kind::f16: f16 0, bf16 1;
+// kind::tf32: tf32 2; kind::f8f6f4: e4m3 0, e5m2 1).
+inline int input_kind(gemm_dtype_t in) {
+    return (in == GEMM_E4M3 || in == GEMM_E5M2) ? tcdt::kInF8 : in == GEMM_TF32 ? tcdt::kInTF32 : tcdt::kInF16;
+}
+inline int64_t dtype_bytes(gemm_dtype_t t) {
+    return (t == GEMM_E4M3 || t == GEMM_E5M2) ? 1 : (t == GEMM_F32 || t == GEMM_TF32) ? 4 : 2;
+}
+inline uint32_t input_format(gemm_dtype_t in) {
+    return (in == GEMM_BF16 || in == GEMM_E5M2) ? 1u : in == GEMM_TF32 ? 2u : 0u;
+}
+// K elements per 128-byte block of an operand row
+inline int64_t k_block(gemm_dtype_t in) { return 128 / dtype_bytes(in); }
 
 enum ConfigId : int {
     kCfgSingle16 = 0,
@@ -140,34 +156,50 @@ TCDT_DECLARE_KIND(single256)
 TCDT_DECLARE_KIND(pair256)
 TCDT_DECLARE_KIND(pair224)
 #undef TCDT_DECLARE_KIND
+// 8-bit and tf32 operands (no fused epilogue, no 256 x 224 tiles)
+#define TCDT_DECLARE_KIND_IN(name, suffix)                                                               \
+    gemm_status_t launch_##name##_##suffix(gemm_plan* plan, int slot, const Choice& ch, const Problem& pr, \
+                                           const void* C, void* D, int64_t ldc, float alpha, float beta, \
+                                           cudaStream_t s);
+TCDT_DECLARE_KIND_IN(single16, f8)
+TCDT_DECLARE_KIND_IN(single64, f8)
+TCDT_DECLARE_KIND_IN(single256, f8)
+TCDT_DECLARE_KIND_IN(pair256, f8)
+TCDT_DECLARE_KIND_IN(single16, tf32)
+TCDT_DECLARE_KIND_IN(single64, tf32)
+TCDT_DECLARE_KIND_IN(single256, tf32)
+TCDT_DECLARE_KIND_IN(pair256, tf32)
+#undef TCDT_DECLARE_KIND_IN
 
 // 2-D tensor map over a matrix whose contiguous dimension has `inner`
 // elements (rows of `ld` elements), 128-byte swizzle, zero fill outside.
 inline gemm_status_t encode_map(const gemm_plan* plan, CUtensorMap* map, const void* ptr, uint64_t inner,
                                 uint64_t outer, uint64_t ld, uint32_t box_inner, uint32_t box_outer,
                                 gemm_dtype_t dtype, CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
-    const uint64_t esz = dtype == GEMM_F32 ? 4 : 2;
+    const uint64_t esz = static_cast<uint64_t>(dtype_bytes(dtype));
     const cuuint64_t dims[2] = {inner, outer};
     const cuuint64_t strides[1] = {ld * esz};
     const cuuint32_t box[2] = {box_inner, box_outer};
     const cuuint32_t estr[2] = {1, 1};
-    const CUtensorMapDataType dt = dtype == GEMM_F32   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
-                                   : dtype == GEMM_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
-                                                       : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    // fp8 moves as bytes and tf32 as fp32 words: the copy keeps every bit
+    const CUtensorMapDataType dt = (dtype == GEMM_F32 || dtype == GEMM_TF32) ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                   : dtype == GEMM_F16                       ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                   : dtype == GEMM_BF16                      ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                                             : CU_TENSOR_MAP_DATA_TYPE_UINT8;
     CUresult r = plan->encode(map, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr,
                               CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
-// tcgen05 instruction descriptor, kind::f16:
-//   [4,6) D type (0 f16, 1 f32)   [7,10) A type (0 f16, 1 bf16)   [10,13) B type
+// tcgen05 instruction descriptor (kind::f16, kind::tf32, kind::f8f6f4):
+//   [4,6) D type (0 f16, 1 f32)   [7,10) A format   [10,13) B format (input_format)
 //   [15] A MN-major   [16] B MN-major   [17,23) N >> 3   [24,29) M >> 4
-inline uint32_t make_idesc(bool acc_f32, bool bf16, bool a_mn, bool b_mn, int mma_m, int mma_n) {
+inline uint32_t make_idesc(bool acc_f32, uint32_t fmt, bool a_mn, bool b_mn, int mma_m, int mma_n) {
     uint32_t d = 0;
     d |= (acc_f32 ? 1u : 0u) << 4;
-    d |= (bf16 ? 1u : 0u) << 7;
-    d |= (bf16 ? 1u : 0u) << 10;
+    d |= fmt << 7;
+    d |= fmt << 10;
     d |= (a_mn ? 1u : 0u) << 15;
     d |= (b_mn ? 1u : 0u) << 16;
     d |= static_cast<uint32_t>(mma_n >> 3) << 17;
@@ -223,14 +255,15 @@ gemm_status_t launch_tc(gemm_plan* plan, const Choice& ch, const Problem& pr, co
                         int64_t ldc, float alpha, float beta, gemm_dtype_t out_dtype, cudaStream_t stream) {
     const bool a_mn = pr.la == GEMM_COL_MAJOR;   // column-major A is M-contiguous
     const bool b_mn = pr.lb == GEMM_ROW_MAJOR;   // row-major B is N-contiguous
+    if ((a_mn || b_mn) && !Cfg::MN_OK) return GEMM_ERR_UNSUPPORTED;
     CUtensorMap tmA, tmB;
     gemm_status_t st;
     const gemm_dtype_t in_dt = plan->in_dtype;
     if (a_mn) st = encode_map(plan, &tmA, pr.A, pr.M, pr.K, pr.lda, 64, 64, in_dt);
-    else st = encode_map(plan, &tmA, pr.A, pr.K, pr.M, pr.lda, 64, Cfg::BM, in_dt);
+    else st = encode_map(plan, &tmA, pr.A, pr.K, pr.M, pr.lda, Cfg::BK, Cfg::BM, in_dt);
     if (st != GEMM_OK) return st;
     if (b_mn) st = encode_map(plan, &tmB, pr.B, pr.N, pr.K, pr.ldb, 64, 64, in_dt);
-    else st = encode_map(plan, &tmB, pr.B, pr.K, pr.N, pr.ldb, 64, Cfg::BN_CTA, in_dt);
+    else st = encode_map(plan, &tmB, pr.B, pr.K, pr.N, pr.ldb, Cfg::BK, Cfg::BN_CTA, in_dt);
     if (st != GEMM_OK) return st;
     // D through TMA stores: 32 x 32 boxes, rows of 128 bytes (fp32, 128-byte
     // swizzle) or 64 bytes (16-bit, 64-byte swizzle); needs 16-byte aligned rows
@@ -244,7 +277,7 @@ gemm_status_t launch_tc(gemm_plan* plan, const Choice& ch, const Problem& pr, co
     const bool n_halves = ch.n_halves && Cfg::HALVES_OK && ch.splits == 1;
     if (n_halves && !b_mn) {
         // K-major B of a half-width item: half as many rows per CTA
-        st = encode_map(plan, &tmBh, pr.B, pr.K, pr.N, pr.ldb, 64, Cfg::BN_CTA_HALF, in_dt);
+        st = encode_map(plan, &tmBh, pr.B, pr.K, pr.N, pr.ldb, Cfg::BK, Cfg::BN_CTA_HALF, in_dt);
         if (st != GEMM_OK) return st;
     }
     if (d_tma) {
@@ -276,8 +309,10 @@ gemm_status_t launch_tc(gemm_plan* plan, const Choice& ch, const Problem& pr, co
     p.D = D;
     p.alpha = alpha;
     p.beta = beta;
-    p.idesc = make_idesc(!Cfg::ACC_F16, plan->in_dtype == GEMM_BF16, a_mn, b_mn, Cfg::UMMA_M, Cfg::BN);
-    p.idesc_half = make_idesc(!Cfg::ACC_F16, plan->in_dtype == GEMM_BF16, a_mn, b_mn, Cfg::UMMA_M, Cfg::BN / 2);
+    if (input_kind(plan->in_dtype) != Cfg::IN) return GEMM_ERR_UNSUPPORTED;
+    const uint32_t fmt = input_format(plan->in_dtype);
+    p.idesc = make_idesc(!Cfg::ACC_F16, fmt, a_mn, b_mn, Cfg::UMMA_M, Cfg::BN);
+    p.idesc_half = make_idesc(!Cfg::ACC_F16, fmt, a_mn, b_mn, Cfg::UMMA_M, Cfg::BN / 2);
     p.a_mn_major = a_mn;
     p.b_mn_major = b_mn;
     p.trans_out = pr.swap ? 1u : 0u;
@@ -316,26 +351,36 @@ gemm_status_t launch_tc(gemm_plan* plan, const Choice& ch, const Problem& pr, co
     return GEMM_OK;
 }
 
-template <template <bool, int> class CfgT, bool EP = false>
+// Output slots: 0 fp32, 1 fp16, 2 bf16 (fp32 accumulation), 3 fp16 with fp16
+// accumulation (16-bit operands only).
+template <template <bool, int, int> class CfgT, int IN = tcdt::kInF16, bool EP = false>
 gemm_status_t prepare_kind(gemm_plan* plan, int kind, int slot) {
     switch (slot) {
-        case 0: return prepare<CfgT<false, tcdt::kOutF32>, EP>(plan, kind, slot);
-        case 1: return prepare<CfgT<false, tcdt::kOutF16>, EP>(plan, kind, slot);
-        case 2: return prepare<CfgT<false, tcdt::kOutBF16>, EP>(plan, kind, slot);
-        default: return prepare<CfgT<true, tcdt::kOutF16>, EP>(plan, kind, slot);
+        case 0: return prepare<CfgT<false, tcdt::kOutF32, IN>, EP>(plan, kind, slot);
+        case 1: return prepare<CfgT<false, tcdt::kOutF16, IN>, EP>(plan, kind, slot);
+        case 2: return prepare<CfgT<false, tcdt::kOutBF16, IN>, EP>(plan, kind, slot);
+        default:
+            if constexpr (IN == tcdt::kInF16) return prepare<CfgT<true, tcdt::kOutF16, IN>, EP>(plan, kind, slot);
+            else return GEMM_ERR_UNSUPPORTED;
     }
 }
 
-template <template <bool, int> class CfgT, bool EP = false>
+template <template <bool, int, int> class CfgT, int IN = tcdt::kInF16, bool EP = false>
 gemm_status_t launch_kind(gemm_plan* plan, int slot, const Choice& ch, const Problem& pr, const void* C, void* D,
                           int64_t ldc, float alpha, float beta, cudaStream_t s) {
-    gemm_status_t st = prepare_kind<CfgT, EP>(plan, ch.kind, slot);
+    gemm_status_t st = prepare_kind<CfgT, IN, EP>(plan, ch.kind, slot);
     if (st != GEMM_OK) return st;
     switch (slot) {
-        case 0: return launch_tc<CfgT<false, tcdt::kOutF32>, EP>(plan, ch, pr, C, D, ldc, alpha, beta, GEMM_F32, s);
-        case 1: return launch_tc<CfgT<false, tcdt::kOutF16>, EP>(plan, ch, pr, C, D, ldc, alpha, beta, GEMM_F16, s);
-        case 2: return launch_tc<CfgT<false, tcdt::kOutBF16>, EP>(plan, ch, pr, C, D, ldc, alpha, beta, GEMM_BF16, s);
-        default: return launch_tc<CfgT<true, tcdt::kOutF16>, EP>(plan, ch, pr, C, D, ldc, alpha, beta, GEMM_F16, s);
+        case 0:
+            return launch_tc<CfgT<false, tcdt::kOutF32, IN>, EP>(plan, ch, pr, C, D, ldc, alpha, beta, GEMM_F32, s);
+        case 1:
+            return launch_tc<CfgT<false, tcdt::kOutF16, IN>, EP>(plan, ch, pr, C, D, ldc, alpha, beta, GEMM_F16, s);
+        case 2:
+            return launch_tc<CfgT<false, tcdt::kOutBF16, IN>, EP>(plan, ch, pr, C, D, ldc, alpha, beta, GEMM_BF16, s);
+        default:
+            if constexpr (IN == tcdt::kInF16)
+                return launch_tc<CfgT<true, tcdt::kOutF16, IN>, EP>(plan, ch, pr, C, D, ldc, alpha, beta, GEMM_F16, s);
+            else return GEMM_ERR_UNSUPPORTED;
     }
 }
 
@@ -351,7 +396,14 @@ gemm_status_t launch_kind(gemm_plan* plan, int slot, const Choice& ch, const Pro
     gemm_status_t launch_##name##_ep(gemm_plan* plan, int slot, const Choice& ch, const Problem& pr,     \
                                      const void* C, void* D, int64_t ldc, float alpha, float beta,       \
                                      cudaStream_t s) {                                                    \
-        return launch_kind<CfgT, true>(plan, slot, ch, pr, C, D, ldc, alpha, beta, s);                  \
+        return launch_kind<CfgT, tcdt::kInF16, true>(plan, slot, ch, pr, C, D, ldc, alpha, beta, s);    \
+    }
+
+#define TCDT_DEFINE_KIND_IN(name, CfgT, suffix, IN)                                                      \
+    gemm_status_t launch_##name##_##suffix(gemm_plan* plan, int slot, const Choice& ch, const Problem& pr, \
+                                           const void* C, void* D, int64_t ldc, float alpha, float beta, \
+                                           cudaStream_t s) {                                              \
+        return launch_kind<CfgT, IN>(plan, slot, ch, pr, C, D, ldc, alpha, beta, s);                    \
     }
 
 }  // namespace tcdt_host

@@ -101,28 +101,35 @@ struct KernelParams {
 // One output tile is UMMA_M x BN (UMMA_M = 128 * CG).  With CG == 2 a
 // cluster of two CTAs on two SMs computes it with one tcgen05.mma stream:
 // each CTA stages 128 rows of A and BN/2 columns of B and receives 128
-// rows of the accumulator in its own tensor memory.
-template <int BN_, int STAGES_, int CG_, bool ACC_F16_, int OUT_>
+// rows of the accumulator in its own tensor memory.  IN_ is the operand
+// kind (kInF16, kInF8, kInTF32): a K block is always one 128-byte swizzle
+// row of each operand row (64, 128 or 32 elements) and an MMA 32 bytes of it.
+template <int BN_, int STAGES_, int CG_, bool ACC_F16_, int OUT_, int IN_ = kInF16>
 struct TileConfig {
     static constexpr int CG = CG_;                 // CTAs per MMA (1 or 2)
     static constexpr int BM = 128;                 // accumulator rows per CTA (TMEM lanes)
     static constexpr int UMMA_M = 128 * CG;        // tile rows
     static constexpr int BN = BN_;                 // tile columns (MMA N)
     static constexpr int BN_CTA = BN / CG;         // B columns staged per CTA
-    static constexpr int BK = 64;                  // 64 x 2 bytes = one 128-byte swizzle row
-    static constexpr int UMMA_K = 16;              // K per tcgen05.mma kind::f16
+    static constexpr int IN = IN_;
+    static constexpr int IN_ESZ = IN == kInF8 ? 1 : IN == kInTF32 ? 4 : 2;   // operand element bytes
+    static constexpr int BK = 128 / IN_ESZ;        // K elements per block: one 128-byte swizzle row
+    static constexpr int UMMA_K = 32 / IN_ESZ;     // K per tcgen05.mma (32 bytes)
+    // MN-major operands are staged for 16-bit kinds only (the host passes the
+    // other kinds K-major)
+    static constexpr bool MN_OK = IN == kInF16;
     static constexpr int STAGES = STAGES_;
     static constexpr bool ACC_F16 = ACC_F16_;
     static constexpr int OUT = OUT_;
     static constexpr int W = BN < 32 ? BN : 32;    // accumulator columns per tcgen05.ld
-    static constexpr uint32_t MN_CHUNK_BYTES = 64 * BK * 2;    // 64 MN-elements x BK rows
+    static constexpr uint32_t MN_CHUNK_BYTES = 64 * BK * 2;    // 64 MN-elements x BK rows (16-bit)
     static constexpr int B_CHUNKS = (BN_CTA + 63) / 64;        // MN-major B: 64-column TMA boxes
     static constexpr int BN_CTA_HALF = BN_CTA / 2;             // B columns per CTA of a half-width item
     static constexpr int B_CHUNKS_HALF = (BN_CTA_HALF + 63) / 64;
     // half-width items need whole 32-column epilogue chunks and whole 8-row atoms
     static constexpr bool HALVES_OK = (BN / 2) % 32 == 0 && BN_CTA_HALF % 8 == 0;
-    static constexpr int A_BYTES = BM * BK * 2;
-    static constexpr int B_BYTES = B_CHUNKS * 64 * BK * 2;     // room for whole MN-major chunks
+    static constexpr int A_BYTES = BM * 128;
+    static constexpr int B_BYTES = B_CHUNKS * 64 * 128;        // room for whole MN-major chunks
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int ACC_COLS = BN;            // one 32-bit TMEM column per output column
     static constexpr int TMEM_COLS = 2 * ACC_COLS <= 32 ? 32 : 2 * ACC_COLS <= 64 ? 64
@@ -979,6 +986,8 @@ gemm_sm103_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     const int num_units = CG == 1 ? static_cast<int>(gridDim.x) : static_cast<int>(num_clusters_x());
     const bool leader = rank == 0;
     const int num_items = unit_items(p, unit, num_units);
+    const bool a_mn = Cfg::MN_OK && p.a_mn_major;   // A is M-contiguous
+    const bool b_mn = Cfg::MN_OK && p.b_mn_major;   // B is N-contiguous
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < Cfg::STAGES; ++s) {
@@ -1000,7 +1009,7 @@ gemm_sm103_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         tma_prefetch_desc(&tmB);
     }
     if (warp == 2 && lane == 0) {
-        if (p.n_halves && !p.b_mn_major) tma_prefetch_desc(&tmBh);
+        if (p.n_halves && !b_mn) tma_prefetch_desc(&tmBh);
         if (p.d_tma) tma_prefetch_desc(&tmD);
         if (p.splits > 1) tma_prefetch_desc(&tmW);
     }
@@ -1025,10 +1034,10 @@ gemm_sm103_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             uint32_t phase = 0;
             int64_t issued = 0;
             bool ok = true;
-            const uint32_t b_tx_full = p.b_mn_major ? static_cast<uint32_t>(Cfg::B_BYTES)
-                                                    : static_cast<uint32_t>(Cfg::BN_CTA * Cfg::BK * 2);
-            const uint32_t b_tx_half = p.b_mn_major ? static_cast<uint32_t>(Cfg::B_CHUNKS_HALF * 64 * Cfg::BK * 2)
-                                                    : static_cast<uint32_t>(Cfg::BN_CTA_HALF * Cfg::BK * 2);
+            const uint32_t b_tx_full = b_mn ? static_cast<uint32_t>(Cfg::B_BYTES)
+                                            : static_cast<uint32_t>(Cfg::BN_CTA * 128);
+            const uint32_t b_tx_half = b_mn ? static_cast<uint32_t>(Cfg::B_CHUNKS_HALF * 64 * 128)
+                                            : static_cast<uint32_t>(Cfg::BN_CTA_HALF * 128);
             for (int it = 0; ok && it < num_items; ++it) {
                 const WorkItem x = unit_item(p, unit, num_units, it);
                 int mb, nb;
@@ -1036,7 +1045,7 @@ gemm_sm103_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 const bool half = Cfg::HALVES_OK && x.half >= 0;
                 const uint32_t stage_tx = CG * (Cfg::A_BYTES + (half ? b_tx_half : b_tx_full));
                 const int b_chunks = half ? Cfg::B_CHUNKS_HALF : Cfg::B_CHUNKS;
-                const void* tmb = half && !p.b_mn_major ? static_cast<const void*>(&tmBh)
+                const void* tmb = half && !b_mn ? static_cast<const void*>(&tmBh)
                                                         : static_cast<const void*>(&tmB);
                 const int m0 = mb * Cfg::UMMA_M + Cfg::BM * static_cast<int>(rank);
                 const int n0 = half ? nb * Cfg::BN + x.half * (Cfg::BN / 2) + Cfg::BN_CTA_HALF * static_cast<int>(rank)
@@ -1060,14 +1069,14 @@ gemm_sm103_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                         if (leader) mbar_arrive_expect_tx(fb_local, stage_tx);
                         if (skip) {
                         } else if constexpr (CG == 1) {
-                            if (p.a_mn_major) {
+                            if (a_mn) {
 #pragma unroll
                                 for (int c = 0; c < Cfg::BM / 64; ++c)
                                     tma_load_2d(sa + c * Cfg::MN_CHUNK_BYTES, &tmA, fb_local, m0 + 64 * c, k0);
                             } else {
                                 tma_load_2d(sa, &tmA, fb_local, k0, m0);
                             }
-                            if (p.b_mn_major) {
+                            if (b_mn) {
 #pragma unroll 1
                                 for (int c = 0; c < b_chunks; ++c)
                                     tma_load_2d(sb + c * Cfg::MN_CHUNK_BYTES, &tmB, fb_local, n0 + 64 * c, k0);
@@ -1076,14 +1085,14 @@ gemm_sm103_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                             }
                         } else {
                             const uint32_t fb = map_to_cta(fb_local, 0);   // the leader's barrier
-                            if (p.a_mn_major) {
+                            if (a_mn) {
 #pragma unroll
                                 for (int c = 0; c < Cfg::BM / 64; ++c)
                                     tma_load_2d_pair(sa + c * Cfg::MN_CHUNK_BYTES, &tmA, fb, m0 + 64 * c, k0);
                             } else {
                                 tma_load_2d_pair(sa, &tmA, fb, k0, m0);
                             }
-                            if (p.b_mn_major) {
+                            if (b_mn) {
 #pragma unroll 1
                                 for (int c = 0; c < b_chunks; ++c)
                                     tma_load_2d_pair(sb + c * Cfg::MN_CHUNK_BYTES, &tmB, fb, n0 + 64 * c, k0);
@@ -1132,10 +1141,10 @@ gemm_sm103_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             // a 16-deep K step is 32 bytes along the row.
             // MN-major operands: 64-element chunks MN_CHUNK_BYTES apart (LBO),
             // 8-row K groups 1024 bytes apart (SBO); a 16-deep K step is 16 rows.
-            const uint32_t a_lbo = p.a_mn_major ? Cfg::MN_CHUNK_BYTES : 16u;
-            const uint32_t b_lbo = p.b_mn_major ? Cfg::MN_CHUNK_BYTES : 16u;
-            const uint32_t a_kstep = p.a_mn_major ? 16u * 128u : 32u;
-            const uint32_t b_kstep = p.b_mn_major ? 16u * 128u : 32u;
+            const uint32_t a_lbo = a_mn ? Cfg::MN_CHUNK_BYTES : 16u;
+            const uint32_t b_lbo = b_mn ? Cfg::MN_CHUNK_BYTES : 16u;
+            const uint32_t a_kstep = a_mn ? 16u * 128u : 32u;
+            const uint32_t b_kstep = b_mn ? 16u * 128u : 32u;
             uint32_t init_phase = 0;
             for (int it = 0; ok && it < num_items; ++it) {
                 const WorkItem x = unit_item(p, unit, num_units, it);
@@ -1170,7 +1179,7 @@ gemm_sm103_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                         for (int k = 0; k < Cfg::BK / Cfg::UMMA_K; ++k) {
                             const uint64_t adesc = smem_desc_sw128(sa + k * a_kstep, a_lbo, 1024u);
                             const uint64_t bdesc = smem_desc_sw128(sb + k * b_kstep, b_lbo, 1024u);
-                            umma_f16_ss<CG>(d_tmem, adesc, bdesc, idesc, (seeded || kb != x.kb0 || k != 0) ? 1u : 0u);
+                            umma_ss<CG, Cfg::IN>(d_tmem, adesc, bdesc, idesc, (seeded || kb != x.kb0 || k != 0) ? 1u : 0u);
                         }
                         // the stage is reusable once these MMAs finish; after the
                         // item's last K block the accumulator is complete (the same

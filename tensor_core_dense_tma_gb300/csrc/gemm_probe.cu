@@ -1,11 +1,12 @@
 // gemm_probe.cu -- tensor-core issue/execution rate probe (no memory traffic)
 //
-// Measures how many SM cycles one tcgen05.mma kind::f16 (M = 256 on a CTA
-// pair, N columns, K = 16) takes when it is issued the way the GEMM kernel
-// issues it: one elected lane of a warp-uniform loop, four MMAs per stage,
-// a commit per stage and a six-deep ring of stage barriers, with operands
-// already in shared memory.  From it the per-SM tensor rate and the peak at
-// the measured clock follow (2 * 128 * N * 16 flop per SM per MMA).
+// Measures how many SM cycles one tcgen05.mma (M = 256 on a CTA pair, N
+// columns, 32 bytes of K: K = 16 for kind::f16, 32 for kind::f8f6f4 with
+// 8-bit operands, 8 for kind::tf32) takes when it is issued the way the GEMM
+// kernel issues it: one elected lane of a warp-uniform loop, four MMAs per
+// stage, a commit per stage and a six-deep ring of stage barriers, with
+// operands already in shared memory.  From it the per-SM tensor rate and the
+// peak at the measured clock follow (2 * 128 * N * K flop per SM per MMA).
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -44,6 +45,7 @@ __device__ __forceinline__ unsigned long long probe_clock() {
 }
 
 // out[2 * pair] = cycles, out[2 * pair + 1] = nanoseconds for `iters` stages of 4 MMAs
+template <int IN>
 __global__ void __launch_bounds__(kProbeThreads, 1)
 mma_probe_kernel(uint32_t idesc, int iters, unsigned long long* out, int* err) {
     extern __shared__ uint8_t smem_raw[];
@@ -81,7 +83,7 @@ mma_probe_kernel(uint32_t idesc, int iters, unsigned long long* out, int* err) {
             tc_fence_after_sync();
             if (elect_one_sync()) {
 #pragma unroll
-                for (int k = 0; k < 4; ++k) umma_f16_ss<2>(tmem, a0 + 2 * k, b0 + 2 * k, idesc, (it | k) ? 1u : 0u);
+                for (int k = 0; k < 4; ++k) umma_ss<2, IN>(tmem, a0 + 2 * k, b0 + 2 * k, idesc, (it | k) ? 1u : 0u);
                 umma_commit<2>(bars + 8 * s, 3);
             }
             __syncwarp();
@@ -110,9 +112,11 @@ mma_probe_kernel(uint32_t idesc, int iters, unsigned long long* out, int* err) {
 extern "C" gemm_status_t gemm_measure_mma_rate(int device, gemm_dtype_t in_dtype, gemm_dtype_t accum_dtype,
                                                int n, double* cycles_per_mma, double* sm_mhz) {
     if (!cycles_per_mma || !sm_mhz) return GEMM_ERR_INVALID_ARG;
-    if ((in_dtype != GEMM_F16 && in_dtype != GEMM_BF16) || (accum_dtype != GEMM_F32 && accum_dtype != GEMM_F16))
+    if ((in_dtype != GEMM_F16 && in_dtype != GEMM_BF16 && in_dtype != GEMM_E4M3 && in_dtype != GEMM_E5M2 &&
+         in_dtype != GEMM_TF32) ||
+        (accum_dtype != GEMM_F32 && accum_dtype != GEMM_F16))
         return GEMM_ERR_INVALID_ARG;
-    if (in_dtype == GEMM_BF16 && accum_dtype == GEMM_F16) return GEMM_ERR_UNSUPPORTED;
+    if (in_dtype != GEMM_F16 && accum_dtype == GEMM_F16) return GEMM_ERR_UNSUPPORTED;
     if (n < 16 || n > 256 || n % 16 != 0) return GEMM_ERR_INVALID_ARG;
     int count = 0;
     if (cudaGetDeviceCount(&count) != cudaSuccess || count <= 0) {
@@ -131,17 +135,21 @@ extern "C" gemm_status_t gemm_measure_mma_rate(int device, gemm_dtype_t in_dtype
     int* d_err = nullptr;
     const int pairs = sms / 2;
     const int iters = 4096;
-    // instruction descriptor: D type, A/B type, K-major operands, N >> 3, M >> 4 (M = 256)
-    const uint32_t idesc = ((accum_dtype == GEMM_F32 ? 1u : 0u) << 4) | ((in_dtype == GEMM_BF16 ? 1u : 0u) << 7) |
-                           ((in_dtype == GEMM_BF16 ? 1u : 0u) << 10) | (static_cast<uint32_t>(n >> 3) << 17) |
-                           (static_cast<uint32_t>(256 >> 4) << 24);
+    // instruction descriptor: D type, A/B format (kind::f16: f16 0, bf16 1;
+    // kind::f8f6f4: e4m3 0, e5m2 1; kind::tf32: 2), K-major operands, N >> 3, M >> 4 (M = 256)
+    const uint32_t fmt = (in_dtype == GEMM_BF16 || in_dtype == GEMM_E5M2) ? 1u : in_dtype == GEMM_TF32 ? 2u : 0u;
+    const uint32_t idesc = ((accum_dtype == GEMM_F32 ? 1u : 0u) << 4) | (fmt << 7) | (fmt << 10) |
+                           (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(256 >> 4) << 24);
+    const bool f8 = in_dtype == GEMM_E4M3 || in_dtype == GEMM_E5M2;
+    void (*kern)(uint32_t, int, unsigned long long*, int*) =
+        f8 ? mma_probe_kernel<kInF8> : in_dtype == GEMM_TF32 ? mma_probe_kernel<kInTF32> : mma_probe_kernel<kInF16>;
     std::vector<double> cyc;
     std::vector<double> mhz;
     if (major != 10 || minor != 3 || pairs < 1) {
         st = GEMM_ERR_NO_DEVICE;
     } else if (cudaMalloc(&d_out, 2 * pairs * sizeof(unsigned long long)) != cudaSuccess ||
                cudaMalloc(&d_err, sizeof(int)) != cudaSuccess || cudaMemset(d_err, 0, sizeof(int)) != cudaSuccess ||
-               cudaFuncSetAttribute(mma_probe_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kProbeSmem) !=
+               cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kProbeSmem) !=
                    cudaSuccess) {
         st = GEMM_ERR_CUDA;
     } else {
@@ -158,7 +166,7 @@ extern "C" gemm_status_t gemm_measure_mma_rate(int device, gemm_dtype_t in_dtype
         cfg.numAttrs = 1;
         std::vector<unsigned long long> h(2 * pairs);
         for (int rep = 0; rep < 3 && st == GEMM_OK; ++rep) {   // the first launch warms up
-            if (cudaLaunchKernelEx(&cfg, mma_probe_kernel, idesc, iters, d_out, d_err) != cudaSuccess ||
+            if (cudaLaunchKernelEx(&cfg, kern, idesc, iters, d_out, d_err) != cudaSuccess ||
                 cudaDeviceSynchronize() != cudaSuccess ||
                 cudaMemcpy(h.data(), d_out, h.size() * sizeof(unsigned long long), cudaMemcpyDeviceToHost) !=
                     cudaSuccess) {

@@ -328,6 +328,36 @@ __device__ __forceinline__ void umma_f16_ss(uint32_t d_tmem, uint64_t a_desc, ui
             : "memory");
 }
 
+// Input kinds of tcgen05.mma used here: kind::f16 (fp16 / bf16, K = 16 per
+// instruction), kind::f8f6f4 with 8-bit operands (E4M3 / E5M2, K = 32) and
+// kind::tf32 (K = 8); each instruction covers 32 bytes of K.  The operand
+// formats within a kind are fields of the instruction descriptor.
+constexpr int kInF16 = 0, kInF8 = 1, kInTF32 = 2;
+
+template <int CG, int IN>
+__device__ __forceinline__ void umma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                        uint32_t accumulate) {
+    static_assert(CG == 1 || CG == 2, "CTA group");
+    if constexpr (IN == kInF8 && CG == 1)
+        asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                     "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+                     "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
+    else if constexpr (IN == kInF8)
+        asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                     "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+                     "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
+    else if constexpr (IN == kInTF32 && CG == 1)
+        asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                     "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+                     "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
+    else if constexpr (IN == kInTF32)
+        asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                     "tcgen05.mma.cta_group::2.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+                     "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
+    else
+        umma_f16_ss<CG>(d_tmem, a_desc, b_desc, idesc, accumulate);
+}
+
 // Arrive on `bar` once every tcgen05 operation issued so far by this thread
 // has completed.  With CG == 2 the arrival goes to the barrier at the same
 // offset in every CTA of `cta_mask` (multicast within the cluster).

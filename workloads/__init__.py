@@ -20,6 +20,11 @@ The workloads are the ones the pages measure or describe, made synthetic
 * ``skinny``   -- bf16 M=16, N=K=8192, same recipe (memory-bound).
 * ``sq8192``   -- 8192^3 with the ``sq4096`` recipe (the second size of the
   throughput target).
+* ``e4m3_8192``, ``e5m2_8192``, ``tf32_4096`` -- the other tensor-core input
+  types (8-bit floats, TF32), A row-major and B column-major, U[-1,1], fp32
+  accumulate, bf16 (8-bit) or fp32 (TF32) output.  TF32 operands are fp32
+  values whose 13 low fraction bits are cleared, so the tensor cores read
+  them exactly.
 
 Every workload also has an integer twin: entries drawn uniformly from
 {-2,-1,0,1,2} (and C too, where beta != 0), for which every partial sum is an
@@ -35,7 +40,9 @@ from dataclasses import dataclass, replace
 
 import torch
 
-DTYPES = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}
+DTYPES = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32, "e4m3": torch.float8_e4m3fn,
+          "e5m2": torch.float8_e5m2, "tf32": torch.float32}
+ELEMENT_BYTES = {"f16": 2, "bf16": 2, "f32": 4, "e4m3": 1, "e5m2": 1, "tf32": 4}
 
 
 @dataclass(frozen=True)
@@ -45,7 +52,7 @@ class Workload:
     M: int
     N: int
     K: int
-    in_dtype: str          # "f16" | "bf16"
+    in_dtype: str          # "f16" | "bf16" | "e4m3" | "e5m2" | "tf32"
     layoutA: str           # "row" | "col"
     layoutB: str
     accum_dtype: str       # "f32" | "f16"
@@ -73,8 +80,8 @@ class Workload:
 
     def algorithmic_bytes(self) -> int:
         """|A| + |B| + |C if beta != 0| + |D|, each read or written once."""
-        e_in = 2
-        e_out = 4 if self.out_dtype == "f32" else 2
+        e_in = ELEMENT_BYTES[self.in_dtype]
+        e_out = ELEMENT_BYTES[self.out_dtype]
         b = (self.M * self.K + self.K * self.N) * e_in + self.M * self.N * e_out
         if self.beta != 0.0:
             b += self.M * self.N * e_out
@@ -98,6 +105,10 @@ WORKLOADS: dict[str, Workload] = {
         Workload("skinny", 5, 16, 8192, 8192, "bf16", "row", "row", "f32", "bf16", 1.0, 0.0, "u1"),
         # the second square size the throughput target names (fp16 -> fp32 at 8192^3)
         Workload("sq8192", 6, 8192, 8192, 8192, "f16", "row", "row", "f32", "f32", 1.0, 0.0, "u1"),
+        # the other tensor-core input kinds (K-major operands)
+        Workload("e4m3_8192", 7, 8192, 8192, 8192, "e4m3", "row", "col", "f32", "bf16", 1.0, 0.0, "u1"),
+        Workload("e5m2_8192", 8, 8192, 8192, 8192, "e5m2", "row", "col", "f32", "bf16", 1.0, 0.0, "u1"),
+        Workload("tf32_4096", 9, 4096, 4096, 4096, "tf32", "row", "col", "f32", "f32", 1.0, 0.0, "u1"),
     ]
 }
 
@@ -122,6 +133,9 @@ def draw(shape, dist: str, dtype: str, seed: int, integer: bool = False) -> torc
         x = torch.randn(shape, generator=g, dtype=torch.float32)
     else:
         raise ValueError(dist)
+    if dtype == "tf32":
+        # fp32 storage with the 13 low fraction bits cleared: TF32-exact values
+        return (x.view(torch.int32) & -8192).view(torch.float32)
     return x.to(DTYPES[dtype])
 
 
@@ -172,10 +186,13 @@ def logical(mat: torch.Tensor, rows: int, cols: int, layout: str) -> torch.Tenso
 
 def bits(t: torch.Tensor):
     """numpy view of a CPU tensor as the oracle wants it: uint16 bit patterns
-    for fp16/bf16, float32 for fp32."""
+    for fp16/bf16, uint8 for the 8-bit floats, float32 for fp32 (and TF32
+    operands)."""
     t = t.contiguous()
     if t.dtype in (torch.float16, torch.bfloat16):
         return t.view(torch.int16).numpy().view("uint16")
+    if t.dtype in (torch.float8_e4m3fn, torch.float8_e5m2):
+        return t.view(torch.uint8).numpy()
     if t.dtype == torch.float32:
         return t.numpy()
     raise TypeError(t.dtype)
