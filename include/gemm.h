@@ -86,9 +86,9 @@ typedef enum { GEMM_ROW_MAJOR = 0, GEMM_COL_MAJOR = 1 } gemm_layout_t;
  *              sign, the 8 exponent bits and the top 10 mantissa bits; values
  *              whose low 13 mantissa bits are zero are used exactly).
  * The three are multiplied with fp32 accumulation into fp32, fp16 or bf16
- * outputs, with A row-major and B column-major (both K-contiguous; other
- * storage orders return GEMM_ERR_UNSUPPORTED), and without the fused
- * epilogue.  INT8 is not offered: the sm_103a tensor cores have no
+ * outputs (the fused epilogue of gemm_run_ep included), with A row-major
+ * and B column-major (both K-contiguous; other storage orders return
+ * GEMM_ERR_UNSUPPORTED).  INT8 is not offered: the sm_103a tensor cores have no
  * tcgen05.mma kind::i8 (ptxas rejects it for this target). */
 typedef enum {
     GEMM_F16 = 0,

@@ -390,23 +390,19 @@ gemm_status_t run_choice(gemm_plan* plan, const Choice& ch, const void* A, const
     const int slot = out_slot(accum_dtype, out_dtype);
     const int in_kind = input_kind(plan->in_dtype);
     if (in_kind != tcdt::kInF16) {
-        if (ep) return GEMM_ERR_UNSUPPORTED;   // the fused epilogue is built for 16-bit operands
-        const bool f8 = in_kind == tcdt::kInF8;
-        switch (ch.kind) {
-            case kCfgSingle16:
-                return f8 ? launch_single16_f8(plan, slot, ch, pr, C, D, ldc, alpha, beta, s)
-                          : launch_single16_tf32(plan, slot, ch, pr, C, D, ldc, alpha, beta, s);
-            case kCfgSingle64:
-                return f8 ? launch_single64_f8(plan, slot, ch, pr, C, D, ldc, alpha, beta, s)
-                          : launch_single64_tf32(plan, slot, ch, pr, C, D, ldc, alpha, beta, s);
-            case kCfgSingle256:
-                return f8 ? launch_single256_f8(plan, slot, ch, pr, C, D, ldc, alpha, beta, s)
-                          : launch_single256_tf32(plan, slot, ch, pr, C, D, ldc, alpha, beta, s);
-            case kCfgPair256:
-                return f8 ? launch_pair256_f8(plan, slot, ch, pr, C, D, ldc, alpha, beta, s)
-                          : launch_pair256_tf32(plan, slot, ch, pr, C, D, ldc, alpha, beta, s);
-            default: return GEMM_ERR_UNSUPPORTED;
-        }
+        // one entry point per (configuration, operand kind, fused epilogue or not)
+        using LaunchFn = gemm_status_t (*)(gemm_plan*, int, const Choice&, const Problem&, const void*, void*,
+                                           int64_t, float, float, cudaStream_t);
+        static const LaunchFn table[4][2][2] = {
+            // [configuration][kind: f8, tf32][epilogue]
+            {{launch_single16_f8, launch_single16_f8_ep}, {launch_single16_tf32, launch_single16_tf32_ep}},
+            {{launch_single64_f8, launch_single64_f8_ep}, {launch_single64_tf32, launch_single64_tf32_ep}},
+            {{launch_single256_f8, launch_single256_f8_ep}, {launch_single256_tf32, launch_single256_tf32_ep}},
+            {{launch_pair256_f8, launch_pair256_f8_ep}, {launch_pair256_tf32, launch_pair256_tf32_ep}},
+        };
+        if (ch.kind < kCfgSingle16 || ch.kind > kCfgPair256) return GEMM_ERR_UNSUPPORTED;
+        const LaunchFn fn = table[ch.kind][in_kind == tcdt::kInF8 ? 0 : 1][ep ? 1 : 0];
+        return fn(plan, slot, ch, pr, C, D, ldc, alpha, beta, s);
     }
     if (ep) {
         switch (ch.kind) {

@@ -156,11 +156,14 @@ TCDT_DECLARE_KIND(single256)
 TCDT_DECLARE_KIND(pair256)
 TCDT_DECLARE_KIND(pair224)
 #undef TCDT_DECLARE_KIND
-// 8-bit and tf32 operands (no fused epilogue, no 256 x 224 tiles)
+// 8-bit and tf32 operands (no 256 x 224 tiles), without and with the fused epilogue
 #define TCDT_DECLARE_KIND_IN(name, suffix)                                                               \
     gemm_status_t launch_##name##_##suffix(gemm_plan* plan, int slot, const Choice& ch, const Problem& pr, \
                                            const void* C, void* D, int64_t ldc, float alpha, float beta, \
-                                           cudaStream_t s);
+                                           cudaStream_t s);                                               \
+    gemm_status_t launch_##name##_##suffix##_ep(gemm_plan* plan, int slot, const Choice& ch,            \
+                                                const Problem& pr, const void* C, void* D, int64_t ldc,  \
+                                                float alpha, float beta, cudaStream_t s);
 TCDT_DECLARE_KIND_IN(single16, f8)
 TCDT_DECLARE_KIND_IN(single64, f8)
 TCDT_DECLARE_KIND_IN(single256, f8)
@@ -404,6 +407,13 @@ gemm_status_t launch_kind(gemm_plan* plan, int slot, const Choice& ch, const Pro
                                            const void* C, void* D, int64_t ldc, float alpha, float beta, \
                                            cudaStream_t s) {                                              \
         return launch_kind<CfgT, IN>(plan, slot, ch, pr, C, D, ldc, alpha, beta, s);                    \
+    }
+
+#define TCDT_DEFINE_KIND_IN_EP(name, CfgT, suffix, IN)                                                   \
+    gemm_status_t launch_##name##_##suffix##_ep(gemm_plan* plan, int slot, const Choice& ch,            \
+                                                const Problem& pr, const void* C, void* D, int64_t ldc,  \
+                                                float alpha, float beta, cudaStream_t s) {               \
+        return launch_kind<CfgT, IN, true>(plan, slot, ch, pr, C, D, ldc, alpha, beta, s);              \
     }
 
 }  // namespace tcdt_host

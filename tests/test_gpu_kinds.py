@@ -125,9 +125,27 @@ def test_tf32_inputs_with_low_bits(plans):
     assert (err <= (2e-3 + 2.0 ** -9) * S + 1e-6).all(), float((err / (S + 1e-30)).max())
 
 
+@pytest.mark.parametrize("kind", KINDS)
+@pytest.mark.parametrize("shape", [(300, 520, 1000), (16, 1104, 520), (2300, 2290, 800)],
+                         ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("ep_kind", ["scale_bias_relu", "scale_bias_gelu"])
+@pytest.mark.parametrize("integer", [False, True], ids=["random", "twin"])
+def test_kind_fused_epilogue(plans, kind, shape, ep_kind, integer):
+    """Per-row/column scales (the usual dequantisation of 8-bit operands),
+    bias and activation fused after the 8-bit / tf32 product."""
+    from test_gpu_epilogue import compare, make_ep, oracle_ep, run_ep
+    w = W(kind, *shape, out="bf16", alpha=0.5, beta=1.0)
+    h = inputs(w, integer)
+    ep = make_ep(w, ep_kind, integer)
+    D = run_ep(plans[kind], w, h, ep)
+    torch.cuda.synchronize()
+    Dref, V, S = oracle_ep(w, h, ep)
+    compare(w, ep, integer, out_bits(D[:, :w.N]), Dref, V, S, f"{kind}/{ep_kind}")
+
+
 def test_kind_rejections(plans):
-    """Storage orders other than A row-major / B column-major, fp16
-    accumulation and the fused epilogue are not offered for these kinds."""
+    """Storage orders other than A row-major / B column-major and fp16
+    accumulation are not offered for these kinds."""
     import tensor_core_dense_tma_gb300 as tc
     plan = plans["e4m3"]
     A = torch.zeros((64, 128), dtype=torch.float8_e4m3fn, device="cuda")
@@ -141,9 +159,6 @@ def test_kind_rejections(plans):
     with pytest.raises(tc.GemmError) as e:
         plan.gemm(Bc.t().t(), Bc.t(), None, D, accum_dtype="f16", out_dtype="f16")
     assert e.value.status in (1, 2)
-    with pytest.raises(tc.GemmError) as e:
-        plan.gemm(A, Bc.t(), None, D, act="relu")
-    assert e.value.status == 2
     torch.cuda.synchronize()
     assert plan.device_status() == 0
 
