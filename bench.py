@@ -66,6 +66,9 @@ def parse():
     ap.add_argument("--out", choices=["f32", "f16", "bf16"])
     ap.add_argument("--epilogue", choices=["none", "bias", "bias_relu", "bias_gelu", "scale_bias_gelu"],
                     default="none", help="fused epilogue timed with the GEMM (random fp32 vectors)")
+    ap.add_argument("--prior-art", choices=["wmma_naive", "wmma_shared", "mma_sync"],
+                    help="time one of the pages' own warp-level kernels instead (fp16 row-major A and B; "
+                         "comparison only)")
     ap.add_argument("--autotune", action="store_true",
                     help="time every candidate configuration first (gemm_plan_autotune) and run the fastest")
     return ap.parse_args()
@@ -334,6 +337,10 @@ def main():
                 ep["act"] = a
 
     def step():
+        if args.prior_art:
+            tc.run_prior_art(args.prior_art, A_l, B_l, D_l, accum_dtype=w.accum_dtype, out_dtype=w.out_dtype,
+                             stream=stream.cuda_stream)
+            return
         plan.gemm(A_l, B_l, C_l, D_l, alpha=w.alpha, beta=w.beta, accum_dtype=w.accum_dtype,
                   out_dtype=w.out_dtype, stream=stream.cuda_stream, **ep)
 
@@ -372,7 +379,7 @@ def main():
     wall = time.perf_counter() - wall0
     if dist:
         dist.barrier()
-    launches = plan.launches - launches0
+    launches = args.steps if args.prior_art else plan.launches - launches0
     clocks = sampler.stop() if rank == 0 else None
     assert plan.device_status() == 0, "device status word reports an error"
 
@@ -387,7 +394,7 @@ def main():
 
     # end to end through the public API with host buffers (pinned), copies timed
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and not args.prior_art:
         hA = h.A.pin_memory()
         hB = h.B.pin_memory()
         hC = None if h.C is None else h.C.pin_memory()
@@ -426,7 +433,8 @@ def main():
     achieved = w.flops / avg_s / 1e12
     ratio = NOMINAL_RATIO[w.in_dtype]
     peak = float(peaks.get("bf16_tflops", FALLBACK_BF16_TFLOPS)) * ratio   # fp16 dense rate = bf16 dense rate
-    kernel_tag = plan.describe(w.M, w.N, w.K, w.layoutA, w.layoutB, w.accum_dtype, w.out_dtype).split()[0]
+    kernel_tag = ("prior_art_" + args.prior_art if args.prior_art else
+                  plan.describe(w.M, w.N, w.K, w.layoutA, w.layoutB, w.accum_dtype, w.out_dtype).split()[0])
     traffic = traffic_from_profiles(kernel_tag)
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak, "traffic": traffic,
@@ -466,7 +474,8 @@ def main():
             "pct_of_nominal_dense_fp16": 100.0 * value / world / NOMINAL_DENSE_FP16_TFLOPS,
             "nominal_dense_fp16_tflops": NOMINAL_DENSE_FP16_TFLOPS,
             "pct_of_nominal_dense_same_kind": 100.0 * value / world / (NOMINAL_DENSE_FP16_TFLOPS * ratio),
-            "kernel_config": plan.describe(w.M, w.N, w.K, w.layoutA, w.layoutB, w.accum_dtype, w.out_dtype),
+            "kernel_config": (kernel_tag if args.prior_art else
+                              plan.describe(w.M, w.N, w.K, w.layoutA, w.layoutB, w.accum_dtype, w.out_dtype)),
             "epilogue": args.epilogue,
             "autotune": tuning,
             "wall_s_timed_loop": wall,

@@ -323,6 +323,45 @@ gemm_status_t gemm_run_static_scratch(int device, gemm_dtype_t in_dtype, const v
 gemm_status_t gemm_measure_mma_rate(int device, gemm_dtype_t in_dtype, gemm_dtype_t accum_dtype, int n,
                                     double *cycles_per_mma, double *sm_mhz);
 
+/* The pages' own tensor-core kernels, rebuilt for sm_103a as a comparison
+ * ladder below the tcgen05 path (no plan; one launch on `stream`):
+ *   GEMM_PRIOR_WMMA_NAIVE   one warp per 16 x 16 tile, WMMA fragments loaded
+ *                           from global memory ("CUDA算子优化(5)：WMMA矩阵乘法",
+ *                           the naive WMMA kernel); M, N, K multiples of 16,
+ *                           lda, ldb multiples of 16, ldd of 8, A, B, D
+ *                           32-byte aligned;
+ *   GEMM_PRIOR_WMMA_SHARED  64 x 64 block tile through shared memory, 8 warps
+ *                           of 16 x 32, K steps of 16 (same page, the shared-
+ *                           memory kernel); any M, N, K;
+ *   GEMM_PRIOR_MMA_SYNC     one warp per 16 x 8 tile, ldmatrix.x4 (A) and
+ *                           ldmatrix.x2.trans (B) then mma.sync.m16n8k16
+ *                           ("hgemm_mma_m16n8k16_naive_kernel详解"); any M, N, K.
+ * D = A B with fp16 A (M x K) and B (K x N), both ROW-major, and row-major D
+ * (leading dimension ldd): fp32 accumulation and output (accum_dtype =
+ * out_dtype = GEMM_F32) for all three, or fp16 accumulation and output
+ * (GEMM_F16 / GEMM_F16, the page's f16.f16.f16.f16 form) for
+ * GEMM_PRIOR_MMA_SYNC.  Other combinations return GEMM_ERR_UNSUPPORTED. */
+typedef enum {
+    GEMM_PRIOR_WMMA_NAIVE = 0,
+    GEMM_PRIOR_WMMA_SHARED = 1,
+    GEMM_PRIOR_MMA_SYNC = 2
+} gemm_prior_art_t;
+
+gemm_status_t gemm_run_prior_art(gemm_prior_art_t kernel, const void *A, const void *B, void *D,
+                                 int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldd,
+                                 gemm_dtype_t accum_dtype, gemm_dtype_t out_dtype, void *stream);
+
+/* The m16n8k16 fragment layout as the hardware delivers it
+ * ("hgemm_mma_m16n8k16_naive_kernel详解", section 4.3, the A and B fragment
+ * formulas, and section 6.2, the C/D formula): one warp loads a 16 x 16 A whose entry (r, c) is 16 r + c with
+ * ldmatrix.x4, a 16 x 8 B whose entry (k, n) is 8 k + n with
+ * ldmatrix.x2.trans, and computes D = I B with mma.sync.m16n8k16.  out (32 x
+ * 16 ints, host memory) receives, for lane l, out[16 l + j]: j < 8 the values
+ * of a0..a7, j = 8..11 those of b0..b3, j = 12..15 those of c0..c3 (so the
+ * coordinates of each element follow from its value).  Synchronises the
+ * device. */
+gemm_status_t gemm_mma_fragment_map(int device, int *out);
+
 /* Free the plan and its device memory.  NULL is accepted (no-op).  The
  * caller must have synchronised any stream still running its launches. */
 gemm_status_t gemm_plan_destroy(gemm_plan_t plan);

@@ -33,6 +33,7 @@ __all__ = [
     "gemm_plan_sm_count", "gemm_plan_describe", "gemm_plan_destroy", "gemm_status_string",
     "gemm_plan_force_config", "CONFIG", "gemm_run_static_scratch", "gemm_plan_autotune",
     "gemm_plan_clear_tuning", "gemm_plan_tuned_count", "gemm_plan_force_division", "DIVISION",
+    "gemm_run_prior_art", "PRIOR_ART", "gemm_mma_fragment_map", "run_prior_art",
 ]
 
 STATUS = {
@@ -93,6 +94,10 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.gemm_plan_autotune.argtypes = [p, p, p, p, p, i64, i64, i64, i64, i64, i64, i32, i32, i32, i32, f32, f32,
                                        i32, p, ctypes.c_char_p, i64]
     lib.gemm_plan_autotune.restype = i32
+    lib.gemm_run_prior_art.argtypes = [i32, p, p, p, i64, i64, i64, i64, i64, i64, i32, i32, p]
+    lib.gemm_run_prior_art.restype = i32
+    lib.gemm_mma_fragment_map.argtypes = [i32, p]
+    lib.gemm_mma_fragment_map.restype = i32
     lib.gemm_plan_force_division.argtypes = [p, i32, i32]
     lib.gemm_plan_force_division.restype = i32
     lib.gemm_plan_clear_tuning.argtypes = [p]
@@ -186,6 +191,50 @@ CONFIG = {"auto": -1, "single_128x16": 0, "single_128x64": 1, "single_128x256": 
 
 def gemm_plan_force_config(plan, config: str | int = "auto", splits: int = 0) -> int:
     return load().gemm_plan_force_config(plan, CONFIG[config] if isinstance(config, str) else config, splits)
+
+
+PRIOR_ART = {"wmma_naive": 0, "wmma_shared": 1, "mma_sync": 2}
+
+
+def gemm_run_prior_art(kernel, A, B, D, M, N, K, lda, ldb, ldd, accum_dtype="f32", out_dtype="f32",
+                       stream=None) -> int:
+    return load().gemm_run_prior_art(PRIOR_ART[kernel] if isinstance(kernel, str) else kernel, A, B, D, M, N, K,
+                                     lda, ldb, ldd, DTYPE[accum_dtype], DTYPE[out_dtype], stream)
+
+
+def run_prior_art(kernel: str, A, B, D=None, *, accum_dtype: str = "f32", out_dtype: str = "f32", stream=None):
+    """The pages' own kernels (see gemm_run_prior_art) on row-major fp16
+    device tensors A (M x K) and B (K x N); returns D (allocated if not
+    given, row-major)."""
+    import torch
+    M, K = A.shape
+    K2, N = B.shape
+    if K2 != K:
+        raise ValueError("inner dimensions differ")
+    if A.dtype != torch.float16 or B.dtype != torch.float16:
+        raise ValueError("A and B must be fp16")
+    if (K > 1 and A.stride(1) != 1) or (N > 1 and B.stride(1) != 1):
+        raise ValueError("A and B must be row-major")
+    if D is None:
+        D = torch.empty((M, N), dtype=getattr(torch, _TORCH_DT[out_dtype]), device=A.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(A.device).cuda_stream
+    st = gemm_run_prior_art(kernel, A.data_ptr(), B.data_ptr(), D.data_ptr(), M, N, K,
+                            A.stride(0) if M > 1 else K, B.stride(0) if K > 1 else N,
+                            D.stride(0) if M > 1 else N, accum_dtype, out_dtype, stream)
+    if st != 0:
+        raise GemmError(st, "gemm_run_prior_art")
+    return D
+
+
+def gemm_mma_fragment_map(device: int = 0):
+    """Observed m16n8k16 fragments (see gemm.h): an int array of shape (32, 16)."""
+    import numpy as np
+    out = np.zeros((32, 16), dtype=np.int32)
+    st = load().gemm_mma_fragment_map(device, out.ctypes.data)
+    if st != 0:
+        raise GemmError(st, "gemm_mma_fragment_map")
+    return out
 
 
 DIVISION = {"auto": 0, "whole": 1, "split": 2, "early_split": 3, "halves": 4}
