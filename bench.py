@@ -223,9 +223,9 @@ def kernel_sources_hash() -> str:
     return hsh.hexdigest()[:16]
 
 
-def traffic_from_profiles(kernel_tag: str):
-    """Per-launch DRAM bytes from the committed ncu summary, if it was taken
-    on the current kernel sources (else None)."""
+def traffic_from_profiles(workload: str, kernel_tag: str):
+    """Per-launch DRAM bytes of this workload's kernel from the committed ncu
+    summaries, if they were taken on the current kernel sources (else None)."""
     path = os.path.join(ROOT, "profiles", "traffic.txt")
     try:
         with open(path) as f:
@@ -234,7 +234,7 @@ def traffic_from_profiles(kernel_tag: str):
         return None
     if kv.get("sources_sha256") != kernel_sources_hash():
         return None
-    val = kv.get(f"{kernel_tag}.bytes_per_launch")
+    val = kv.get(f"{workload}.{kernel_tag}.bytes_per_launch")
     return float(val) if val else None
 
 
@@ -435,7 +435,7 @@ def main():
     peak = float(peaks.get("bf16_tflops", FALLBACK_BF16_TFLOPS)) * ratio   # fp16 dense rate = bf16 dense rate
     kernel_tag = ("prior_art_" + args.prior_art if args.prior_art else
                   plan.describe(w.M, w.N, w.K, w.layoutA, w.layoutB, w.accum_dtype, w.out_dtype).split()[0])
-    traffic = traffic_from_profiles(kernel_tag)
+    traffic = traffic_from_profiles(w.name, kernel_tag)
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak, "traffic": traffic,
                 "peak_source": (f"{peak_src} bf16 dense GEMM burst (MEASURED_PEAKS.json)"
