@@ -86,6 +86,20 @@ def select_workload(args):
     return w
 
 
+def job_throughput(local_total_ms: float, flops_per_step: float, steps: int, world: int, dist=None,
+                   device=None) -> tuple[float, float]:
+    """(slowest rank's total ms, whole-job TFLOP/s): every rank runs `steps`
+    steps of its own replica; the job's time is the maximum over ranks and
+    its work the steps of all ranks."""
+    total_ms = float(local_total_ms)
+    if dist is not None and world > 1:
+        import torch
+        t = torch.tensor([total_ms], device=device, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    return total_ms, flops_per_step * steps * world / (total_ms * 1e-3) / 1e12
+
+
 def metric_for(w) -> str:
     """The headline metric for its own workload; a plain description for the others."""
     if w.name == "sq4096":
@@ -384,13 +398,8 @@ def main():
     assert plan.device_status() == 0, "device status word reports an error"
 
     per_step = [s.elapsed_time(e) for s, e in zip(starts, ends)]   # ms
-    total_ms = sum(per_step)
-    if dist:
-        t = torch.tensor([total_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms, value = job_throughput(sum(per_step), w.flops, args.steps, world, dist, dev)
     ms_per_step = total_ms / args.steps
-    value = w.flops * args.steps * world / (total_ms * 1e-3) / 1e12   # TFLOP/s, whole job
 
     # end to end through the public API with host buffers (pinned), copies timed
     e2e = None
@@ -399,20 +408,20 @@ def main():
         hB = h.B.pin_memory()
         hC = None if h.C is None else h.C.pin_memory()
         hD = torch.empty((w.M, w.N), dtype=wl.DTYPES[w.out_dtype], pin_memory=True)
-        staging = {}
         hA_l = wl.logical(hA, w.M, w.K, w.layoutA)
         hB_l = wl.logical(hB, w.K, w.N, w.layoutB)
         hC_l = None if hC is None else hC[:, :w.N]
         for _ in range(3):
             plan.gemm_host(hA_l, hB_l, hC_l, hD, alpha=w.alpha, beta=w.beta, accum_dtype=w.accum_dtype,
-                           out_dtype=w.out_dtype, staging=staging)
+                           out_dtype=w.out_dtype, stream=stream, **ep)
         torch.cuda.synchronize()
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         for _ in range(args.e2e_steps):
+            # every step copies its inputs in and its result out (ordered on `stream`)
             plan.gemm_host(hA_l, hB_l, hC_l, hD, alpha=w.alpha, beta=w.beta, accum_dtype=w.accum_dtype,
-                           out_dtype=w.out_dtype, staging=staging)
+                           out_dtype=w.out_dtype, stream=stream, sync=False, **ep)
         e1.record(stream)
         torch.cuda.synchronize()
         e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
@@ -421,7 +430,8 @@ def main():
         d2h = hD.numel() * hD.element_size()
         e2e = {"value": w.flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "path": "Plan.gemm_host: pinned host A,B -> device, gemm_run, D -> pinned host"}
+               "path": "gemm_run_host (C ABI) on pinned host A, B (C) and D: copies in, row blocks of D "
+                       "computed and copied back, overlapped on internal streams"}
 
     if rank != 0:
         if dist:

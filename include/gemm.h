@@ -227,6 +227,28 @@ uint64_t gemm_plan_launch_count(gemm_plan_t plan);
 /* Number of SMs of the plan's device. */
 int gemm_plan_sm_count(gemm_plan_t plan);
 
+/* gemm_run_ep on HOST buffers: A, B, C (when beta != 0) and D are host
+ * pointers (page-locked memory, e.g. from cudaHostAlloc, lets the copies run
+ * asynchronously; pageable memory works but the copies then stall the host),
+ * with the layouts, leading dimensions, types and rules of gemm_run; `ep`,
+ * if not NULL, holds DEVICE vectors as for gemm_run_ep.  The plan copies the
+ * operands into device staging buffers that it owns (allocated on first use,
+ * grown when a larger problem comes, freed with the plan) and computes D in
+ * row blocks of about 512 rows: B is copied first, then each block's rows of
+ * A (and C), and each block of D is copied back to the host as soon as it is
+ * computed, on internal streams, so the copies of later blocks, the tensor
+ * cores and the copies back of earlier blocks overlap.  The work starts after
+ * the work already queued on `stream`, and `stream` waits for the last copy
+ * back: synchronise it before reading D.  Calls on one plan are ordered
+ * through their streams; the host buffers must stay valid until then.
+ * Returns gemm_run's statuses; growing the staging buffers synchronises
+ * `stream`. */
+gemm_status_t gemm_run_host(gemm_plan_t plan, const void *A, const void *B, const void *C, void *D,
+                            int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
+                            gemm_layout_t layoutA, gemm_layout_t layoutB,
+                            gemm_dtype_t accum_dtype, gemm_dtype_t out_dtype,
+                            float alpha, float beta, const gemm_epilogue_t *ep, void *stream);
+
 /* Shape-keyed autotuning ("矩阵乘法优化可视化学习文档", section 6, the
  * "Autotuning" row: the best tile differs with M/N/K and type, found by
  * search; section 8, "Autotune": one kernel, several block configurations,

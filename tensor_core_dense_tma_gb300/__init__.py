@@ -94,6 +94,9 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.gemm_plan_autotune.argtypes = [p, p, p, p, p, i64, i64, i64, i64, i64, i64, i32, i32, i32, i32, f32, f32,
                                        i32, p, ctypes.c_char_p, i64]
     lib.gemm_plan_autotune.restype = i32
+    lib.gemm_run_host.argtypes = [p, p, p, p, p, i64, i64, i64, i64, i64, i64, i32, i32, i32, i32, f32, f32,
+                                  ctypes.POINTER(Epilogue), p]
+    lib.gemm_run_host.restype = i32
     lib.gemm_run_prior_art.argtypes = [i32, p, p, p, i64, i64, i64, i64, i64, i64, i32, i32, p]
     lib.gemm_run_prior_art.restype = i32
     lib.gemm_mma_fragment_map.argtypes = [i32, p]
@@ -339,6 +342,21 @@ def _operand_layout(t, what: str):
     raise ValueError(f"{what} must be row- or column-major (strides {t.stride()})")
 
 
+def _make_epilogue(M, N, bias, row_scale, col_scale, act):
+    """The gemm_epilogue_t of optional fp32 DEVICE vectors, or None."""
+    import torch
+    if bias is None and row_scale is None and col_scale is None and act == "none":
+        return None
+
+    def vec(v, n, what):
+        if v is None:
+            return None
+        if v.dtype != torch.float32 or v.dim() != 1 or v.shape[0] != n or not v.is_cuda or v.stride(0) != 1:
+            raise ValueError(f"{what} must be a contiguous fp32 device vector of length {n}")
+        return v.data_ptr()
+    return Epilogue(vec(bias, N, "bias"), vec(row_scale, M, "row_scale"), vec(col_scale, N, "col_scale"), ACT[act])
+
+
 class Plan:
     """A gemm plan bound to one device and one input type."""
 
@@ -424,16 +442,7 @@ class Plan:
         M, N, K, la, lda, lb, ldb, ldc, out_dtype, D = self._resolve(A, B, C, D, out_dtype)
         if stream is None:
             stream = torch.cuda.current_stream(A.device).cuda_stream
-        ep = None
-        if bias is not None or row_scale is not None or col_scale is not None or act != "none":
-            def vec(v, n, what):
-                if v is None:
-                    return None
-                if v.dtype != torch.float32 or v.dim() != 1 or v.shape[0] != n or not v.is_cuda or v.stride(0) != 1:
-                    raise ValueError(f"{what} must be a contiguous fp32 device vector of length {n}")
-                return v.data_ptr()
-            ep = Epilogue(vec(bias, N, "bias"), vec(row_scale, M, "row_scale"), vec(col_scale, N, "col_scale"),
-                          ACT[act])
+        ep = _make_epilogue(M, N, bias, row_scale, col_scale, act)
         self.run_raw(A.data_ptr(), B.data_ptr(), C.data_ptr() if C is not None else None, D.data_ptr(),
                      M, N, K, lda, ldb, max(ldc, N), la, lb, accum_dtype, out_dtype, alpha, beta, stream, ep=ep)
         return D
@@ -500,42 +509,28 @@ class Plan:
 
     def gemm_host(self, A, B, C=None, D=None, *, alpha: float = 1.0, beta: float = 0.0,
                   accum_dtype: str = "f32", out_dtype: str | None = None, stream=None,
-                  staging: dict | None = None):
-        """End-to-end call on HOST tensors (pinned for asynchronous copies):
-        copies A, B (and C) to the device, runs gemm_run, copies D back into
-        the host tensor ``D`` (allocated pinned if not given) and returns it
-        once the stream has finished.  ``staging`` may carry device buffers
-        between calls (keys "A", "B", "C", "D"); they are (re)allocated when
-        missing or of the wrong size."""
+                  bias=None, row_scale=None, col_scale=None, act: str = "none", sync: bool = True):
+        """End-to-end call on HOST tensors through gemm_run_host (pinned
+        tensors let the copies overlap the tensor-core work): D (allocated
+        pinned if not given) receives act(alpha * A B + beta * C + ...);
+        epilogue vectors are fp32 DEVICE tensors.  With ``sync`` the call
+        waits for the stream and returns D ready to read."""
         import torch
+        if A.is_cuda or B.is_cuda or (C is not None and C.is_cuda) or (D is not None and D.is_cuda):
+            raise ValueError("gemm_host takes host tensors")
+        if D is None:
+            od = out_dtype or (_dt_name(C) if C is not None else "f32")
+            D = torch.empty((A.shape[0], B.shape[1]), dtype=getattr(torch, _TORCH_DT[od]), pin_memory=True)
+        M, N, K, la, lda, lb, ldb, ldc, out_dtype, D = self._resolve(A, B, C, D, out_dtype)
         dev = torch.device("cuda", self.device)
-        st = staging if staging is not None else {}
         s = torch.cuda.current_stream(dev) if stream is None else stream
-
-        def stage(key, t):
-            buf = st.get(key)
-            if buf is None or buf.shape != t.shape or buf.dtype != t.dtype or buf.stride() != t.stride():
-                buf = torch.empty_strided(t.shape, t.stride(), dtype=t.dtype, device=dev)
-                st[key] = buf
-            buf.copy_(t, non_blocking=True)
-            return buf
-
-        with torch.cuda.stream(s):
-            Ad = stage("A", A)
-            Bd = stage("B", B)
-            Cd = stage("C", C) if C is not None else None
-            M, N = A.shape[0], B.shape[1]
-            if out_dtype is None:
-                out_dtype = _dt_name(D) if D is not None else (_dt_name(C) if C is not None else "f32")
-            tdt = getattr(torch, _TORCH_DT[out_dtype])
-            Dd = st.get("D")
-            if Dd is None or Dd.shape != (M, N) or Dd.dtype != tdt:
-                Dd = torch.empty((M, N), dtype=tdt, device=dev)
-                st["D"] = Dd
-            self.gemm(Ad, Bd, Cd, Dd, alpha=alpha, beta=beta, accum_dtype=accum_dtype,
-                      out_dtype=out_dtype, stream=s.cuda_stream)
-            if D is None:
-                D = torch.empty((M, N), dtype=tdt, pin_memory=True)
-            D.copy_(Dd, non_blocking=True)
-        s.synchronize()
+        ep = _make_epilogue(M, N, bias, row_scale, col_scale, act)
+        st = load().gemm_run_host(self.handle, A.data_ptr(), B.data_ptr(), C.data_ptr() if C is not None else None,
+                                  D.data_ptr(), M, N, K, lda, ldb, max(ldc, N), LAYOUT[la], LAYOUT[lb],
+                                  DTYPE[accum_dtype], DTYPE[out_dtype], float(alpha), float(beta),
+                                  ctypes.byref(ep) if ep is not None else None, s.cuda_stream)
+        if st != 0:
+            raise GemmError(st, "gemm_run_host")
+        if sync:
+            s.synchronize()
         return D

@@ -721,6 +721,7 @@ gemm_status_t gemm_plan_destroy(gemm_plan_t plan) {
         if (plan->d_ws) cudaFree(plan->d_ws);
         if (plan->d_counters) cudaFree(plan->d_counters);
         if (plan->d_flags) cudaFree(plan->d_flags);
+        destroy_host_pipeline(plan->host_pipe);
     }
     delete plan->tuned;
     delete plan;

@@ -86,7 +86,9 @@ inline int out_slot(gemm_dtype_t acc, gemm_dtype_t out) {
 }  // namespace tcdt_host
 
 namespace tcdt_host {
-struct TunedTable;   // gemm_plan_autotune's results, keyed by problem shape (gemm_api.cu)
+struct TunedTable;     // gemm_plan_autotune's results, keyed by problem shape (gemm_api.cu)
+struct HostPipeline;   // gemm_run_host's streams, events and staging buffers (gemm_host.cu)
+void destroy_host_pipeline(HostPipeline* hp);
 }
 
 struct gemm_plan {
@@ -111,6 +113,7 @@ struct gemm_plan {
     int forced_division = 0;      // gemm_plan_force_division (0: any)
     int forced_division_splits = 0;
     tcdt_host::TunedTable* tuned = nullptr;   // owned; null until the first gemm_plan_autotune
+    tcdt_host::HostPipeline* host_pipe = nullptr;   // owned; null until the first gemm_run_host
 };
 
 namespace tcdt_host {
