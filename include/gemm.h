@@ -234,10 +234,12 @@ int gemm_plan_sm_count(gemm_plan_t plan);
  * if not NULL, holds DEVICE vectors as for gemm_run_ep.  The plan copies the
  * operands into device staging buffers that it owns (allocated on first use,
  * grown when a larger problem comes, freed with the plan) and computes D in
- * row blocks of about 512 rows: B is copied first, then each block's rows of
- * A (and C), and each block of D is copied back to the host as soon as it is
- * computed, on internal streams, so the copies of later blocks, the tensor
- * cores and the copies back of earlier blocks overlap.  The work starts after
+ * blocks of about 1024 x 1024 (at most 8 x 8 blocks): the first row block of
+ * A, then the column blocks of B, then the other row blocks of A (each with
+ * its rows of C) are copied in, each block of D is computed once its rows of
+ * A and columns of B have landed and is copied back to the host as soon as
+ * it is done, on internal streams, so the copies in, the tensor cores and the
+ * copies back overlap.  The epilogue's vectors are cut to each block.  The work starts after
  * the work already queued on `stream`, and `stream` waits for the last copy
  * back: synchronise it before reading D.  Calls on one plan are ordered
  * through their streams; the host buffers must stay valid until then.

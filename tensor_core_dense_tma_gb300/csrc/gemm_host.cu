@@ -4,9 +4,15 @@
 // it is done, so the host->device copies of later blocks, the tensor-core
 // work and the device->host copies of earlier blocks overlap:
 //
-//   h2d stream:  B, then A block 0 (and C block 0), A block 1, ...
-//   compute:     block i once its A (C) block has landed (B came first)
-//   d2h stream:  D block i once it is computed
+//   h2d stream:  A row block 0, B column block 0, the other B column blocks,
+//                then A row blocks 1, 2, ... (each with its rows of C)
+//   compute:     row block 0 in column blocks, each once its B columns have
+//                landed; then row block i (all columns) once its A rows have
+//   d2h stream:  each block of D once it is computed
+//
+// Only the first row block is cut into column blocks: its first piece needs
+// 1/nr of A and 1/nc of B, so the copies back start early, while the later
+// row blocks stay wide enough to keep every SM busy.
 //
 // The caller's stream orders calls: the copies of a call start after the
 // work already queued on it, and it waits for the last block's copy back.
@@ -24,10 +30,10 @@ namespace tcdt_host {
 
 // Streams, events and staging buffers of gemm_run_host, created on first use.
 struct HostPipeline {
-    static constexpr int kMaxBlocks = 16;
+    static constexpr int kMaxSplit = 8;   // row blocks, and column blocks
     cudaStream_t h2d = nullptr, compute = nullptr, d2h = nullptr;
-    cudaEvent_t start = nullptr, b_ready = nullptr, done = nullptr;
-    cudaEvent_t a_ready[kMaxBlocks] = {}, d_ready[kMaxBlocks] = {};
+    cudaEvent_t start = nullptr, done = nullptr;
+    cudaEvent_t a_ready[kMaxSplit] = {}, b_ready[kMaxSplit] = {}, d_ready[kMaxSplit * kMaxSplit] = {};
     void* buf[4] = {nullptr, nullptr, nullptr, nullptr};   // A, B, C, D
     size_t cap[4] = {0, 0, 0, 0};
 };
@@ -36,12 +42,13 @@ void destroy_host_pipeline(HostPipeline* hp) {
     if (!hp) return;
     for (int i = 0; i < 4; ++i)
         if (hp->buf[i]) cudaFree(hp->buf[i]);
-    for (int i = 0; i < HostPipeline::kMaxBlocks; ++i) {
+    for (int i = 0; i < HostPipeline::kMaxSplit; ++i) {
         if (hp->a_ready[i]) cudaEventDestroy(hp->a_ready[i]);
-        if (hp->d_ready[i]) cudaEventDestroy(hp->d_ready[i]);
+        if (hp->b_ready[i]) cudaEventDestroy(hp->b_ready[i]);
     }
+    for (int i = 0; i < HostPipeline::kMaxSplit * HostPipeline::kMaxSplit; ++i)
+        if (hp->d_ready[i]) cudaEventDestroy(hp->d_ready[i]);
     if (hp->start) cudaEventDestroy(hp->start);
-    if (hp->b_ready) cudaEventDestroy(hp->b_ready);
     if (hp->done) cudaEventDestroy(hp->done);
     if (hp->h2d) cudaStreamDestroy(hp->h2d);
     if (hp->compute) cudaStreamDestroy(hp->compute);
@@ -60,11 +67,12 @@ gemm_status_t make_pipeline(HostPipeline** out) {
               cudaStreamCreateWithFlags(&hp->compute, cudaStreamNonBlocking) == cudaSuccess &&
               cudaStreamCreateWithFlags(&hp->d2h, cudaStreamNonBlocking) == cudaSuccess &&
               cudaEventCreateWithFlags(&hp->start, cudaEventDisableTiming) == cudaSuccess &&
-              cudaEventCreateWithFlags(&hp->b_ready, cudaEventDisableTiming) == cudaSuccess &&
               cudaEventCreateWithFlags(&hp->done, cudaEventDisableTiming) == cudaSuccess;
-    for (int i = 0; ok && i < HostPipeline::kMaxBlocks; ++i)
+    for (int i = 0; ok && i < HostPipeline::kMaxSplit; ++i)
         ok = cudaEventCreateWithFlags(&hp->a_ready[i], cudaEventDisableTiming) == cudaSuccess &&
-             cudaEventCreateWithFlags(&hp->d_ready[i], cudaEventDisableTiming) == cudaSuccess;
+             cudaEventCreateWithFlags(&hp->b_ready[i], cudaEventDisableTiming) == cudaSuccess;
+    for (int i = 0; ok && i < HostPipeline::kMaxSplit * HostPipeline::kMaxSplit; ++i)
+        ok = cudaEventCreateWithFlags(&hp->d_ready[i], cudaEventDisableTiming) == cudaSuccess;
     if (!ok) {
         cudaGetLastError();
         destroy_host_pipeline(hp);
@@ -144,59 +152,92 @@ extern "C" gemm_status_t gemm_run_host(gemm_plan_t plan, const void* A, const vo
         (st = staging(hp, 2, need[2], &dC)) != GEMM_OK || (st = staging(hp, 3, need[3], &dD)) != GEMM_OK)
         return st;
 
-    // row blocks of D: about 512 rows each (whole 256-row tiles), at most
-    // kMaxBlocks; problems the kernels compute transposed (M <= 64) in one
-    const int64_t target = 512;
-    int nblk = (M <= 64 || K == 0) ? 1 : static_cast<int>((M + target - 1) / target);
-    if (nblk > HostPipeline::kMaxBlocks) nblk = HostPipeline::kMaxBlocks;
-    const int64_t rows_per = ((M + nblk - 1) / nblk + 255) / 256 * 256;
-    nblk = static_cast<int>((M + rows_per - 1) / rows_per);
+    // row blocks of about 512 rows (whole 256-row tiles), at most kMaxSplit,
+    // the first one cut into column blocks of about 1024 columns; small
+    // problems and the transposed product (M <= 64) run as one block
+    auto split = [](int64_t extent, int64_t target, int64_t quantum) {
+        int64_t n = (extent + target - 1) / target;
+        if (n > HostPipeline::kMaxSplit) n = HostPipeline::kMaxSplit;
+        return ((extent + n - 1) / n + quantum - 1) / quantum * quantum;
+    };
+    const int64_t rows_per = (M <= 256 || K == 0) ? M : split(M, 512, 256);
+    const int64_t cols_per = (M <= 256 || N <= 256 || K == 0) ? N : split(N, 1024, 256);
+    const int nrb = static_cast<int>((M + rows_per - 1) / rows_per);
+    const int ncb = static_cast<int>((N + cols_per - 1) / cols_per);
+    auto rows_of = [&](int i) { return (i + 1) * rows_per <= M ? rows_per : M - i * rows_per; };
+    auto cols_of = [&](int j) { return (j + 1) * cols_per <= N ? cols_per : N - j * cols_per; };
 
     bool ok = cudaEventRecord(hp->start, user) == cudaSuccess && cudaStreamWaitEvent(hp->h2d, hp->start, 0) == cudaSuccess;
-    // B first: every block needs all of it
-    if (ok && K > 0) {
-        ok = b_row ? copy2d(dB, B, ldb, K, N, in_esz, cudaMemcpyHostToDevice, hp->h2d)
-                   : copy2d(dB, B, ldb, N, K, in_esz, cudaMemcpyHostToDevice, hp->h2d);
-    }
-    ok = ok && cudaEventRecord(hp->b_ready, hp->h2d) == cudaSuccess;
-    for (int b = 0; ok && b < nblk; ++b) {
-        const int64_t r0 = b * rows_per, rows = (r0 + rows_per <= M ? rows_per : M - r0);
-        // A rows [r0, r0 + rows): a row block (row-major) or the same rows of every column
+    // rows [r0, r0 + rows) of A: a row block (row-major) or the same rows of every column
+    auto copy_a = [&](int i) {
+        const int64_t r0 = i * rows_per, rows = rows_of(i);
+        bool good = true;
         if (K > 0) {
-            if (a_row) {
-                ok = copy2d(static_cast<char*>(dA) + r0 * lda * in_esz, static_cast<const char*>(A) + r0 * lda * in_esz,
-                            lda, rows, K, in_esz, cudaMemcpyHostToDevice, hp->h2d);
-            } else {
-                ok = copy2d(static_cast<char*>(dA) + r0 * in_esz, static_cast<const char*>(A) + r0 * in_esz, lda, K,
-                            rows, in_esz, cudaMemcpyHostToDevice, hp->h2d);
-            }
+            good = a_row ? copy2d(static_cast<char*>(dA) + r0 * lda * in_esz,
+                                  static_cast<const char*>(A) + r0 * lda * in_esz, lda, rows, K, in_esz,
+                                  cudaMemcpyHostToDevice, hp->h2d)
+                         : copy2d(static_cast<char*>(dA) + r0 * in_esz, static_cast<const char*>(A) + r0 * in_esz,
+                                  lda, K, rows, in_esz, cudaMemcpyHostToDevice, hp->h2d);
         }
-        if (ok && use_c)
-            ok = copy2d(static_cast<char*>(dC) + r0 * ldc * out_esz, static_cast<const char*>(C) + r0 * ldc * out_esz,
-                        ldc, rows, N, out_esz, cudaMemcpyHostToDevice, hp->h2d);
-        ok = ok && cudaEventRecord(hp->a_ready[b], hp->h2d) == cudaSuccess &&
-             cudaStreamWaitEvent(hp->compute, hp->a_ready[b], 0) == cudaSuccess;
-        if (!ok) break;
+        if (good && use_c)
+            good = copy2d(static_cast<char*>(dC) + r0 * ldc * out_esz, static_cast<const char*>(C) + r0 * ldc * out_esz,
+                          ldc, rows, N, out_esz, cudaMemcpyHostToDevice, hp->h2d);
+        return good && cudaEventRecord(hp->a_ready[i], hp->h2d) == cudaSuccess;
+    };
+    // columns [c0, c0 + cols) of B: the same columns of every row (row-major) or a block of rows
+    auto copy_b = [&](int j) {
+        const int64_t c0 = j * cols_per, cols = cols_of(j);
+        bool good = true;
+        if (K > 0) {
+            good = b_row ? copy2d(static_cast<char*>(dB) + c0 * in_esz, static_cast<const char*>(B) + c0 * in_esz,
+                                  ldb, K, cols, in_esz, cudaMemcpyHostToDevice, hp->h2d)
+                         : copy2d(static_cast<char*>(dB) + c0 * ldb * in_esz,
+                                  static_cast<const char*>(B) + c0 * ldb * in_esz, ldb, cols, K, in_esz,
+                                  cudaMemcpyHostToDevice, hp->h2d);
+        }
+        return good && cudaEventRecord(hp->b_ready[j], hp->h2d) == cudaSuccess;
+    };
+    ok = ok && copy_a(0);
+    for (int j = 0; ok && j < ncb; ++j) ok = copy_b(j);
+    for (int i = 1; ok && i < nrb; ++i) ok = copy_a(i);
+    // block (i, j): rows of row block i; column block j of row block 0, or
+    // all columns (j = -1) for the later row blocks
+    auto run_block = [&](int i, int j) {
+        const int64_t r0 = i * rows_per, rows = rows_of(i);
+        const int64_t c0 = j < 0 ? 0 : j * cols_per, cols = j < 0 ? N : cols_of(j);
+        if (cudaStreamWaitEvent(hp->compute, hp->a_ready[i], 0) != cudaSuccess ||
+            cudaStreamWaitEvent(hp->compute, hp->b_ready[j < 0 ? ncb - 1 : j], 0) != cudaSuccess)
+            return GEMM_ERR_CUDA;
         const void* Ab = a_row ? static_cast<const void*>(static_cast<char*>(dA) + r0 * lda * in_esz)
                                : static_cast<const void*>(static_cast<char*>(dA) + r0 * in_esz);
-        const void* Cb = use_c ? static_cast<const void*>(static_cast<char*>(dC) + r0 * ldc * out_esz) : nullptr;
-        void* Db = static_cast<char*>(dD) + r0 * ldc * out_esz;
-        // a row block of the epilogue's row scale belongs to this block
+        const void* Bb = b_row ? static_cast<const void*>(static_cast<char*>(dB) + c0 * in_esz)
+                               : static_cast<const void*>(static_cast<char*>(dB) + c0 * ldb * in_esz);
+        const int64_t doff = (r0 * ldc + c0) * out_esz;
+        const void* Cb = use_c ? static_cast<const void*>(static_cast<char*>(dC) + doff) : nullptr;
+        void* Db = static_cast<char*>(dD) + doff;
+        // the epilogue's vectors, cut to this block
         gemm_epilogue_t epb;
         const gemm_epilogue_t* epp = nullptr;
         if (ep) {
             epb = *ep;
             if (epb.row_scale) epb.row_scale += r0;
+            if (epb.col_scale) epb.col_scale += c0;
+            if (epb.bias) epb.bias += c0;
             epp = &epb;
         }
-        st = gemm_run_ep(plan, Ab, dB, Cb, Db, rows, N, K, lda, ldb, ldc, layoutA, layoutB, accum_dtype, out_dtype,
-                         alpha, beta, epp, hp->compute);
-        if (st != GEMM_OK) break;
-        ok = cudaEventRecord(hp->d_ready[b], hp->compute) == cudaSuccess &&
-             cudaStreamWaitEvent(hp->d2h, hp->d_ready[b], 0) == cudaSuccess &&
-             copy2d(static_cast<char*>(D) + r0 * ldc * out_esz, Db, ldc, rows, N, out_esz, cudaMemcpyDeviceToHost,
-                    hp->d2h);
-    }
+        gemm_status_t bst = gemm_run_ep(plan, Ab, Bb, Cb, Db, rows, cols, K, lda, ldb, ldc, layoutA, layoutB,
+                                        accum_dtype, out_dtype, alpha, beta, epp, hp->compute);
+        if (bst != GEMM_OK) return bst;
+        cudaEvent_t ev = hp->d_ready[i * HostPipeline::kMaxSplit + (j < 0 ? 0 : j)];
+        const bool good = cudaEventRecord(ev, hp->compute) == cudaSuccess &&
+                          cudaStreamWaitEvent(hp->d2h, ev, 0) == cudaSuccess &&
+                          copy2d(static_cast<char*>(D) + doff, Db, ldc, rows, cols, out_esz, cudaMemcpyDeviceToHost,
+                                 hp->d2h);
+        return good ? GEMM_OK : GEMM_ERR_CUDA;
+    };
+    if (!ok) st = GEMM_ERR_CUDA;
+    for (int j = 0; st == GEMM_OK && j < ncb; ++j) st = run_block(0, ncb == 1 ? -1 : j);
+    for (int i = 1; st == GEMM_OK && i < nrb; ++i) st = run_block(i, -1);
     if (st != GEMM_OK) {
         cudaStreamSynchronize(hp->h2d);
         cudaStreamSynchronize(hp->compute);

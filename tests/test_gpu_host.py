@@ -40,7 +40,8 @@ def host_run(plan, w, h, pinned=True, D=None, sync=True, **ep):
 
 
 CASES = [
-    W(4096, 1024, 512),                                           # 8 row blocks
+    W(4096, 1024, 512),                                           # 4 row blocks
+    W(3000, 5000, 300, la="row", lb="row", out="bf16"),           # 3 x 5 blocks, row-major B column blocks
     W(4097, 2055, 1000, la="row", lb="col", alpha=0.5, beta=1.0),  # ragged, C, 9 blocks
     W(1300, 700, 640, la="col", lb="col", out="bf16", dt="bf16"),  # column-major A: strided block copies
     W(40, 3000, 2048, dt="bf16", out="bf16"),                      # transposed product, one block
@@ -83,9 +84,9 @@ def test_host_calls_queue_in_order(plans):
 
 
 def test_host_epilogue_row_scale_blocks(plans):
-    """The row scale is split with the row blocks of D."""
+    """The epilogue's vectors are cut with the blocks of D."""
     from test_gpu_epilogue import compare, make_ep, oracle_ep
-    w = W(2500, 600, 256, alpha=0.5, beta=1.0)
+    w = W(2500, 2600, 256, alpha=0.5, beta=1.0)
     plan = plans["f16"]
     h = wl.make_inputs(w, integer=True)
     ep = make_ep(w, "scale_bias_relu", integer=True)
