@@ -69,6 +69,8 @@ def parse():
     ap.add_argument("--prior-art", choices=["wmma_naive", "wmma_shared", "mma_sync"],
                     help="time one of the pages' own warp-level kernels instead (fp16 row-major A and B; "
                          "comparison only)")
+    ap.add_argument("--division", choices=["auto", "whole", "split", "early_split", "halves", "stream_k"],
+                    default="auto", help="pin how the last wave's tiles are divided (gemm_plan_force_division)")
     ap.add_argument("--autotune", action="store_true",
                     help="time every candidate configuration first (gemm_plan_autotune) and run the fastest")
     return ap.parse_args()
@@ -358,6 +360,8 @@ def main():
         plan.gemm(A_l, B_l, C_l, D_l, alpha=w.alpha, beta=w.beta, accum_dtype=w.accum_dtype,
                   out_dtype=w.out_dtype, stream=stream.cuda_stream, **ep)
 
+    if args.division != "auto":
+        plan.force_division(args.division)
     tuning = None
     if args.autotune:
         _, rows = plan.autotune(A_l, B_l, C_l, D_l, alpha=w.alpha, beta=w.beta, accum_dtype=w.accum_dtype,

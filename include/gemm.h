@@ -205,7 +205,11 @@ gemm_status_t gemm_plan_force_config(gemm_plan_t plan, gemm_config_t config, int
  *                first in its unit and leaves an fp32 partial, split 0 runs
  *                last in its unit with its accumulator started from them
  *                (2 to 4 splits, one per unit);
- *   HALVES       each tile runs as two half-width items.
+ *   HALVES       each tile runs as two half-width items;
+ *   STREAM_K     after at least two whole waves: one wave fewer runs whole,
+ *                and the remaining tiles' K blocks, laid end to end, are
+ *                cut into one equal range per unit; a tile cut between two
+ *                units is joined through an early partial ("Stream-K").
  * `splits` (0: any) pins the split count of SPLIT and EARLY_SPLIT.  A call
  * whose problem admits no candidate of the pinned division (EARLY_SPLIT
  * with less than one whole wave or fp16 accumulation, HALVES on a
@@ -216,7 +220,8 @@ typedef enum {
     GEMM_DIVISION_WHOLE = 1,
     GEMM_DIVISION_SPLIT = 2,
     GEMM_DIVISION_EARLY_SPLIT = 3,
-    GEMM_DIVISION_HALVES = 4
+    GEMM_DIVISION_HALVES = 4,
+    GEMM_DIVISION_STREAM_K = 5
 } gemm_division_t;
 
 gemm_status_t gemm_plan_force_division(gemm_plan_t plan, gemm_division_t division, int splits);

@@ -209,9 +209,10 @@ Choice choose(const gemm_plan* plan, int64_t M, int64_t N, int64_t K, gemm_dtype
     double best_cost = -1.0;
     bool any = false;
     auto consider = [&](double cost, int kind, int splits, int64_t dp, bool halves, int64_t tiles, int64_t units,
-                        bool early = false) {
+                        bool early = false, bool stream_k = false) {
         // a pinned division (gemm_plan_force_division) admits only its own kind of candidate
-        const int division = halves ? GEMM_DIVISION_HALVES
+        const int division = halves     ? GEMM_DIVISION_HALVES
+                             : stream_k ? GEMM_DIVISION_STREAM_K
                              : splits > 1 ? (early ? GEMM_DIVISION_EARLY_SPLIT : GEMM_DIVISION_SPLIT)
                                           : GEMM_DIVISION_WHOLE;
         if (plan->forced_division != GEMM_DIVISION_AUTO &&
@@ -225,6 +226,7 @@ Choice choose(const gemm_plan* plan, int64_t M, int64_t N, int64_t K, gemm_dtype
         c.dp_tiles = dp;
         c.n_halves = halves;
         c.early = early;
+        c.stream_k = stream_k;
         c.swap = swap;
         c.tiles = tiles;
         c.units = static_cast<int>(units);
@@ -288,6 +290,27 @@ Choice choose(const gemm_plan* plan, int64_t M, int64_t N, int64_t K, gemm_dtype
                 consider(cost, kind, static_cast<int>(s), dp, false, tiles, units, true);
             }
         }
+        // stream-K: after dp - units whole tiles, the last units + rest tiles
+        // shared out as equal K ranges over all units, cut tiles joined through
+        // early partials (at least two waves, so every unit runs a whole tile
+        // before its range; a range is then at least one tile long).  Measured
+        // slower than the other divisions on every shape the autotuner was run
+        // on (2-15 %: two more items per unit, and an owner that follows an
+        // early split can only be seeded after that split's own partial is
+        // written), so the model offers it only when it is pinned or when the
+        // autotuner times every candidate.
+        const bool offer_stream_k = all != nullptr || plan->forced_division == GEMM_DIVISION_STREAM_K;
+        if (offer_stream_k && rest > 0 && dp >= 2 * units && !pinned && plan->d_flags && acc != GEMM_F16 &&
+            kCfgTileN[kind] >= 128 && kind != kCfgSingle16 && kind != kCfgSingle64 &&
+            (units + 1) * 2 * kCfgCtas[kind] <= kNumCounters &&
+            static_cast<int64_t>(units + 1) * 2 * tile_bytes <= static_cast<int64_t>(plan->ws_bytes)) {
+            const int64_t sk_tiles = units + rest;
+            const int64_t per_unit = (sk_tiles * kb + units - 1) / units;
+            const double cost = static_cast<double>(dp / units - 1) * full_item +
+                                static_cast<double>(per_unit) * full_step + 2.0 * fc.item + fc.early +
+                                fc.per_partial + 2.0;
+            consider(cost, kind, 2, tiles - sk_tiles, false, tiles, units, true, true);
+        }
         // two half-width items per tile of the partial wave
         if (kCfgHalves[kind] && rest > 0 && !pinned) {
             const double item = static_cast<double>(kb) * step_cost(kind, bmn, true) + fc.half_item + 2.0;
@@ -338,7 +361,8 @@ std::string config_name(const Choice& ch, gemm_dtype_t acc, gemm_dtype_t out) {
     std::string s = "tc" + std::to_string(kCfgCtas[ch.kind]) + "cta_" + std::to_string(kCfgTileM[ch.kind]) + "x" +
                     std::to_string(kCfgTileN[ch.kind]) + "_" + outs[out_slot(acc, out)];
     if (ch.swap) s += "_swapAB";
-    if (ch.splits > 1) s += (ch.early ? "_esplitk" : "_splitk") + std::to_string(ch.splits);
+    if (ch.stream_k) s += "_streamk";
+    else if (ch.splits > 1) s += (ch.early ? "_esplitk" : "_splitk") + std::to_string(ch.splits);
     if (ch.n_halves) s += "_nhalves";
     return s;
 }
@@ -542,13 +566,14 @@ gemm_status_t gemm_plan_autotune(gemm_plan_t plan, const void* A, const void* B,
     plan->forced_division = GEMM_DIVISION_AUTO;
     plan->forced_division_splits = 0;
     std::vector<Candidate> cands;
-    bool valid = true;
-    const Choice model = choose(plan, M, N, K, accum_dtype, layoutB == GEMM_ROW_MAJOR, &valid, &cands, true);
+    bool valid = true, valid_all = true;
+    const Choice model = choose(plan, M, N, K, accum_dtype, layoutB == GEMM_ROW_MAJOR, &valid);   // the model's pick
+    choose(plan, M, N, K, accum_dtype, layoutB == GEMM_ROW_MAJOR, &valid_all, &cands, true);     // every candidate
     plan->forced_kind = saved_kind;
     plan->forced_splits = saved_splits;
     plan->forced_division = saved_div;
     plan->forced_division_splits = saved_div_splits;
-    if (!valid || cands.empty()) return GEMM_ERR_UNSUPPORTED;
+    if (!valid || !valid_all || cands.empty()) return GEMM_ERR_UNSUPPORTED;
     cudaEvent_t e0 = nullptr, e1 = nullptr;
     if (cudaEventCreate(&e0) != cudaSuccess || cudaEventCreate(&e1) != cudaSuccess) {
         if (e0) cudaEventDestroy(e0);
@@ -593,7 +618,8 @@ gemm_status_t gemm_plan_autotune(gemm_plan_t plan, const void* A, const void* B,
     for (size_t c = 0; c < cands.size(); ++c) {
         const Choice& ch = cands[c].choice;
         const bool is_model = ch.kind == model.kind && ch.splits == model.splits && ch.n_halves == model.n_halves &&
-                              ch.early == model.early && ch.dp_tiles == model.dp_tiles;
+                              ch.early == model.early && ch.stream_k == model.stream_k &&
+                              ch.dp_tiles == model.dp_tiles;
         char line[160];
         std::snprintf(line, sizeof(line), "%s%s model_cost=%.1f us=%.2f%s\n", c == best ? "* " : "  ",
                       config_name(ch, accum_dtype, out_dtype).c_str(), cands[c].cost, med[c],
@@ -656,7 +682,7 @@ gemm_status_t gemm_plan_force_config(gemm_plan_t plan, gemm_config_t config, int
 
 gemm_status_t gemm_plan_force_division(gemm_plan_t plan, gemm_division_t division, int splits) {
     if (!plan) return GEMM_ERR_INVALID_ARG;
-    if (static_cast<int>(division) < GEMM_DIVISION_AUTO || static_cast<int>(division) > GEMM_DIVISION_HALVES)
+    if (static_cast<int>(division) < GEMM_DIVISION_AUTO || static_cast<int>(division) > GEMM_DIVISION_STREAM_K)
         return GEMM_ERR_INVALID_ARG;
     if (splits < 0 || splits > kMaxSplits) return GEMM_ERR_INVALID_ARG;
     plan->forced_division = static_cast<int>(division);

@@ -23,7 +23,7 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
 // Split-K scratch owned by a plan: fp32 partial tiles and arrival counters.
-constexpr size_t kWorkspaceBytes = size_t(32) << 20;
+constexpr size_t kWorkspaceBytes = size_t(64) << 20;
 constexpr int kNumCounters = 8192;
 constexpr int kMaxSplits = 16;
 
@@ -138,6 +138,7 @@ struct Choice {
     int64_t dp_tiles = 0;      // whole tiles before the divided ones (see KernelParams)
     bool n_halves = false;     // divided tiles run as two half-width items (splits == 1)
     bool early = false;        // divided tiles split with early partials (splits > 1)
+    bool stream_k = false;     // the last dp_tiles..tiles shared out as equal K ranges (see unit_item)
     bool swap = false;
     int64_t tiles = 0;
     int units = 0;
@@ -332,6 +333,7 @@ gemm_status_t launch_tc(gemm_plan* plan, const Choice& ch, const Problem& pr, co
     p.ws = plan->d_ws;
     p.counters = plan->d_counters;
     p.early = (ch.early && ch.splits > 1 && plan->d_flags && Cfg::W == 32) ? 1 : 0;
+    p.stream_k = (p.early && ch.stream_k) ? 1 : 0;
     {
         const uint32_t e = static_cast<uint32_t>(plan->launches + 1);
         p.epoch = e == 0u ? 1u : e;

@@ -89,6 +89,8 @@ struct KernelParams {
     float* ws;                // split partials, [split tile][split][cta][128][BN] fp32
     int* counters;            // [split tile][cta] split arrivals; zero on entry, left zero
     int32_t early;            // 1: divided tiles use early partials (see unit_item)
+    int32_t stream_k;         // 1: tiles [dp_tiles, num_tiles) are shared out as equal K
+                              //    ranges over all units (early partials at the cuts)
     uint32_t epoch;           // this launch's nonzero tag for partial-ready flags
     unsigned* flags;          // [split tile][split][cta] partial-ready flags (earlier launches' tags)
     int* status;              // [0] status code, [1] site
@@ -238,7 +240,32 @@ __device__ __forceinline__ WorkItem work_item(const KernelParams& p, int w) {
 // item and leaves its fp32 partial in the workspace; split 0 (the owner) is
 // its unit's last item, whose accumulator starts from the partials, written
 // a whole-tile time or more earlier, so nothing waits on them in practice.
+// Stream-K (stream_k): after its whole tiles (dp_tiles / units of them), unit
+// u takes the K blocks [s, e) of the remaining tiles' K blocks laid end to
+// end, s = floor(u W / units), e = floor((u + 1) W / units).  There are at
+// least `units` such tiles, so a range is at least one tile long and a tile
+// is cut at most once: the piece after a cut is the next unit's first range
+// item (an early split that leaves its fp32 partial), the piece before it is
+// this unit's last item (the owner, seeded with that partial).  The owner
+// starts after at least as much work as the early piece takes, so it does
+// not wait in practice.  The cut at the start of unit u's range is split
+// tile u (split 1 early, split 0 owner).
+struct StreamRange {
+    int64_t s, e;   // K blocks of the unit's range, counted from tile dp_tiles
+};
+
+__device__ __forceinline__ StreamRange stream_range(const KernelParams& p, int unit, int units) {
+    const int64_t w = static_cast<int64_t>(p.num_tiles - p.dp_tiles) * p.num_k_blocks;
+    return {w * unit / units, w * (unit + 1) / units};
+}
+
 __device__ __forceinline__ int unit_items(const KernelParams& p, int unit, int units) {
+    if (p.stream_k) {
+        const StreamRange r = stream_range(p, unit, units);
+        const int kb = p.num_k_blocks;
+        const int pieces = r.e > r.s ? static_cast<int>((r.e - 1) / kb - r.s / kb + 1) : 0;
+        return p.dp_tiles / units + pieces;
+    }
     if (!p.early) {
         const int n = num_work_items(p);
         return unit < n ? (n - unit + units - 1) / units : 0;
@@ -248,6 +275,35 @@ __device__ __forceinline__ int unit_items(const KernelParams& p, int unit, int u
 }
 
 __device__ __forceinline__ WorkItem unit_item(const KernelParams& p, int unit, int units, int i) {
+    if (p.stream_k) {
+        const int whole = p.dp_tiles / units;
+        if (i < whole) return work_item(p, unit + i * units);
+        const StreamRange r = stream_range(p, unit, units);
+        const int kb = p.num_k_blocks;
+        const int64_t t = r.s / kb + (i - whole);   // tile index within the stream-K tiles
+        const int64_t base = t * kb;
+        WorkItem x;
+        x.half = -1;
+        x.tile = p.dp_tiles + static_cast<int>(t);
+        x.kb0 = static_cast<int>(r.s > base ? r.s - base : 0);
+        x.kb1 = static_cast<int>(r.e - base < kb ? r.e - base : kb);
+        x.nsplit = 2;
+        if (x.kb0 > 0) {            // the piece after the cut at the start of the range
+            x.role = kRoleEarly;
+            x.stile = unit;
+            x.split = 1;
+        } else if (x.kb1 < kb) {    // the piece before the cut at its end
+            x.role = kRoleOwner;
+            x.stile = unit + 1;
+            x.split = 0;
+        } else {
+            x.role = kRoleWhole;
+            x.stile = -1;
+            x.split = 0;
+            x.nsplit = 1;
+        }
+        return x;
+    }
     if (!p.early) return work_item(p, unit + i * units);
     const int whole = p.dp_tiles / units;
     const bool split = unit < (p.num_tiles - p.dp_tiles) * p.splits;
@@ -1236,13 +1292,34 @@ gemm_sm103_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             // warm L2 with this thread's C row while the main loop runs
             if (p.beta != 0.0f && !p.trans_out && m0 + row_local < p.M)
                 prefetch_c_row<Cfg>(p, m0 + row_local, n0, nchunks * W);
+            // Seed an owner item's accumulator with the sum of the early splits'
+            // partials, in split order.  Normally the next item's (the TMEM buffer
+            // this item does not use, drained by the previous iteration) while this
+            // item's MMAs run.  An owner right after an early split (stream-K) is
+            // seeded here at the start of its own iteration instead, once the early
+            // split has written its own partial: the partial the owner waits for is
+            // computed on another unit meanwhile, and other units' owners wait for
+            // this unit's.
             if constexpr (W == 32) {
-                if (p.early && iter + 1 < num_items) {
-                    const WorkItem y = unit_item(p, unit, num_units, iter + 1);
-                    if (y.role == kRoleOwner) {
-                        // While this item's MMAs run, seed the next item's accumulator
-                        // (the other TMEM buffer, drained by the previous iteration)
-                        // with the sum of the early splits' partials, in split order.
+                WorkItem y{};
+                uint32_t seed_buf = 0;
+                bool seed = false;
+                if (p.early) {
+                    if (iter + 1 < num_items && !(p.stream_k && x.role == kRoleEarly)) {
+                        y = unit_item(p, unit, num_units, iter + 1);
+                        seed = y.role == kRoleOwner;
+                        seed_buf = static_cast<uint32_t>(buf ^ 1);
+                    }
+                    if (!seed && p.stream_k && x.role == kRoleOwner && iter > 0 &&
+                        unit_item(p, unit, num_units, iter - 1).role == kRoleEarly) {
+                        y = x;
+                        seed = true;
+                        seed_buf = static_cast<uint32_t>(buf);
+                    }
+                }
+                bool seed_failed = false;
+                if (seed) {
+                    do {
                         const int S = y.nsplit;
                         if (threadIdx.x == 64) {
                             const unsigned* f = p.flags + static_cast<int64_t>(y.stile) * S * CG + rank;
@@ -1252,14 +1329,14 @@ gemm_sm103_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                             epi_last_flag[iter & 1] = got ? 1 : 0;
                         }
                         named_bar_sync(1, 32 * Cfg::NUM_EPI_WARPS);
-                        if (!epi_last_flag[iter & 1]) break;
+                        if (!epi_last_flag[iter & 1]) { seed_failed = true; break; }
                         // Each warp brings its 32 rows of the partials in by TMA, two
                         // 32 x 32 fp32 boxes at a time, through its two staging buffers
                         // (128-byte swizzle, as the stores use them).  Plain loads of the
                         // partials here slowed the concurrent main loop by half.
                         const uint32_t sbar = seed_bar(warp - 2);
                         const uint32_t t_next =
-                            tmem_base + (static_cast<uint32_t>(32 * quad) << 16) + (buf ^ 1) * Cfg::ACC_COLS;
+                            tmem_base + (static_cast<uint32_t>(32 * quad) << 16) + seed_buf * Cfg::ACC_COLS;
                         constexpr int NCH = Cfg::BN / W;
                         bool seeded_ok = true;
                         if (lane == 0) fence_proxy_async_global();
@@ -1308,7 +1385,7 @@ gemm_sm103_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                                 }
                             }
                         }
-                        if (!seeded_ok) break;
+                        if (!seeded_ok) { seed_failed = true; break; }
                         tmem_st_wait();
                         tc_fence_before_sync();
                         __syncwarp();
@@ -1316,8 +1393,9 @@ gemm_sm103_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                             if constexpr (CG == 1) mbar_arrive(accinit_bar);
                             else mbar_arrive_cluster(map_to_cta(accinit_bar, 0));   // the leader's barrier
                         }
-                    }
+                    } while (false);
                 }
+                if (seed_failed) break;
             }
             if (threadIdx.x == 64)
                 epi_ok_flag[iter & 1] = wait_phase(accf_bar(buf), acc_phase, wctx, kSiteEpilogueAccFull) ? 1 : 0;

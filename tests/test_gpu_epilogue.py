@@ -121,6 +121,7 @@ PATHS = {
                          "swapAB_splitk"),
     "early_split": (W("early", 2300, 2290, 800, alpha=0.5, beta=1.0), "early_split", "esplitk"),
     "half_width": (W("halves", 1024, 1024, 1024, dt="bf16", out="bf16"), "halves", "nhalves"),
+    "stream_k": (W("streamk", 3300, 3000, 256, alpha=0.5, beta=1.0), "stream_k", "streamk"),
     "fp16_accumulate": (W("acc16", 270, 530, 256, lb="col", acc="f16", out="f16"), None, None),
 }
 KINDS = ["bias", "scale", "bias_relu", "scale_bias_gelu"]

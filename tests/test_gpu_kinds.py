@@ -78,15 +78,17 @@ def test_kind_every_config(plans, kind, config, splits):
 
 
 @pytest.mark.parametrize("kind", KINDS)
-@pytest.mark.parametrize("division", ["split", "early_split", "halves"])
+@pytest.mark.parametrize("division", ["split", "early_split", "halves", "stream_k"])
 def test_kind_tail_divisions(plans, kind, division):
-    w = W(kind, 2300, 2290, 800, out="f32", alpha=0.5, beta=1.0)
+    shape = (3300, 3000, 256) if division == "stream_k" else (2300, 2290, 800)
+    w = W(kind, *shape, out="f32", alpha=0.5, beta=1.0)
     h = inputs(w, integer=True)
     plan = plans[kind]
     plan.force_division(division)
     try:
         desc = plan.describe(w.M, w.N, w.K, "row", "col", "f32", "f32")
-        assert {"split": "_splitk", "early_split": "_esplitk", "halves": "_nhalves"}[division] in desc, desc
+        assert {"split": "_splitk", "early_split": "_esplitk", "halves": "_nhalves",
+                "stream_k": "_streamk"}[division] in desc, desc
         D = run_gpu(plan, w, h)
         torch.cuda.synchronize()
     finally:

@@ -252,3 +252,67 @@ def test_pinned_division_that_does_not_fit(plans):
     with pytest.raises(tc.GemmError) as e:
         plan.force_division(7)
     assert e.value.status == 1
+
+
+# Stream-K: one wave fewer runs whole and the remaining tiles' K blocks are cut
+# into one equal range per unit; a tile cut between two units is joined
+# through an early partial.  Needs at least two whole waves.
+STREAM_K_SHAPES = [(4096, 4096, 1024, "pair_256x256"), (3000, 5000, 2000, "pair_256x256"),
+                   (4100, 4000, 1000, "pair_256x256"), (3300, 3000, 256, "pair_256x256"),
+                   (4096, 4096, 512, "single_128x256")]
+
+
+@pytest.mark.parametrize("shape", STREAM_K_SHAPES, ids=lambda s: "x".join(map(str, s[:3])) + "_" + s[3])
+@pytest.mark.parametrize("out", ["f32", "bf16"])
+def test_stream_k_integer_twin(plans, shape, out):
+    from gpu_util import check_sampled
+    M, N, K, config = shape
+    w = W(M, N, K, "row", "col", out=out, alpha=0.5, beta=1.0)
+    plan = plans["f16"]
+    plan.force_config(config, 0)
+    plan.force_division("stream_k")
+    try:
+        desc = plan.describe(w.M, w.N, w.K, w.layoutA, w.layoutB, "f32", out)
+        assert "_streamk" in desc, desc
+        lda, ldb = padded(w)
+        h = wl.make_inputs(w, integer=True, lda=lda, ldb=ldb)
+        D = run_gpu(plan, w, h)
+        torch.cuda.synchronize()
+    finally:
+        plan.force_division("auto")
+        plan.force_config("auto")
+    if w.M * w.N * w.K <= 4e9:
+        check_full(w, h, D, integer=True)
+    else:
+        check_sampled(w, h, D, integer=True, n_random=8192)
+
+
+def test_stream_k_random_repeats_bitwise(plans):
+    w = W(3300, 3000, 256, "row", "row", out="f32")
+    plan = plans["f16"]
+    plan.force_division("stream_k")
+    try:
+        assert "_streamk" in plan.describe(w.M, w.N, w.K, w.layoutA, w.layoutB, "f32", "f32")
+        lda, ldb = padded(w)
+        h = wl.make_inputs(w, lda=lda, ldb=ldb)
+        D0 = run_gpu(plan, w, h)
+        torch.cuda.synchronize()
+        check_full(w, h, D0, integer=False)
+        for _ in range(5):
+            D1 = run_gpu(plan, w, h)
+            torch.cuda.synchronize()
+            assert torch.equal(D0, D1)
+    finally:
+        plan.force_division("auto")
+
+
+def test_stream_k_needs_two_waves(plans):
+    import tensor_core_dense_tma_gb300 as tc
+    plan = plans["f16"]
+    plan.force_division("stream_k")
+    try:
+        with pytest.raises(tc.GemmError) as e:
+            plan.describe(2300, 2290, 800)     # 81 tiles: one wave
+        assert e.value.status == 2
+    finally:
+        plan.force_division("auto")
