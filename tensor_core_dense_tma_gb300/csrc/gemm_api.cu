@@ -301,7 +301,7 @@ Choice choose(const gemm_plan* plan, int64_t M, int64_t N, int64_t K, gemm_dtype
         // autotuner times every candidate.
         const bool offer_stream_k = all != nullptr || plan->forced_division == GEMM_DIVISION_STREAM_K;
         if (offer_stream_k && rest > 0 && dp >= 2 * units && !pinned && plan->d_flags && acc != GEMM_F16 &&
-            kCfgTileN[kind] >= 128 && kind != kCfgSingle16 && kind != kCfgSingle64 &&
+            kCfgTileN[kind] == 256 &&
             (units + 1) * 2 * kCfgCtas[kind] <= kNumCounters &&
             static_cast<int64_t>(units + 1) * 2 * tile_bytes <= static_cast<int64_t>(plan->ws_bytes)) {
             const int64_t sk_tiles = units + rest;
