@@ -297,6 +297,16 @@ gemm_status_t gemm_plan_describe(gemm_plan_t plan, int64_t M, int64_t N, int64_t
                                  gemm_dtype_t accum_dtype, gemm_dtype_t out_dtype,
                                  char *buf, int64_t len);
 
+/* The configuration the cost model would pick on a device with `sm_count`
+ * SMs (all co-resident, early partials available), described as
+ * gemm_plan_describe does, without touching any device: for tests and for
+ * planning on a host without a GPU.  GEMM_ERR_INVALID_ARG for sm_count
+ * outside 2..4096 or an input type a plan cannot take. */
+gemm_status_t gemm_describe_model(int sm_count, gemm_dtype_t in_dtype, int64_t M, int64_t N, int64_t K,
+                                  gemm_layout_t layoutA, gemm_layout_t layoutB,
+                                  gemm_dtype_t accum_dtype, gemm_dtype_t out_dtype,
+                                  char *buf, int64_t len);
+
 /* gemm_run for callers that cannot allocate device memory.  The paper has no
  * counterpart to this entry point: its kernels need no workspace at all.
  *

@@ -33,7 +33,7 @@ __all__ = [
     "gemm_plan_sm_count", "gemm_plan_describe", "gemm_plan_destroy", "gemm_status_string",
     "gemm_plan_force_config", "CONFIG", "gemm_run_static_scratch", "gemm_plan_autotune",
     "gemm_plan_clear_tuning", "gemm_plan_tuned_count", "gemm_plan_force_division", "DIVISION",
-    "gemm_run_prior_art", "PRIOR_ART", "gemm_mma_fragment_map", "run_prior_art",
+    "gemm_run_prior_art", "PRIOR_ART", "gemm_mma_fragment_map", "run_prior_art", "gemm_describe_model",
 ]
 
 STATUS = {
@@ -94,6 +94,8 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.gemm_plan_autotune.argtypes = [p, p, p, p, p, i64, i64, i64, i64, i64, i64, i32, i32, i32, i32, f32, f32,
                                        i32, p, ctypes.c_char_p, i64]
     lib.gemm_plan_autotune.restype = i32
+    lib.gemm_describe_model.argtypes = [i32, i32, i64, i64, i64, i32, i32, i32, i32, ctypes.c_char_p, i64]
+    lib.gemm_describe_model.restype = i32
     lib.gemm_run_host.argtypes = [p, p, p, p, p, i64, i64, i64, i64, i64, i64, i32, i32, i32, i32, f32, f32,
                                   ctypes.POINTER(Epilogue), p]
     lib.gemm_run_host.restype = i32
@@ -263,6 +265,18 @@ def gemm_plan_describe(plan, M, N, K, layoutA="row", layoutB="row", accum_dtype=
                                    DTYPE[out_dtype], buf, 256)
     if st != 0:
         raise GemmError(st, "gemm_plan_describe")
+    return buf.value.decode()
+
+
+def gemm_describe_model(sm_count: int, in_dtype: str, M, N, K, layoutA="row", layoutB="row",
+                        accum_dtype="f32", out_dtype="f32") -> str:
+    """The cost model's configuration for a device with `sm_count` SMs (no GPU
+    needed)."""
+    buf = ctypes.create_string_buffer(256)
+    st = load().gemm_describe_model(sm_count, DTYPE[in_dtype], M, N, K, LAYOUT[layoutA], LAYOUT[layoutB],
+                                    DTYPE[accum_dtype], DTYPE[out_dtype], buf, 256)
+    if st != 0:
+        raise GemmError(st, "gemm_describe_model")
     return buf.value.decode()
 
 

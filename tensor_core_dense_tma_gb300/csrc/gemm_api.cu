@@ -279,7 +279,7 @@ Choice choose(const gemm_plan* plan, int64_t M, int64_t N, int64_t K, gemm_dtype
         // the partial wave's tiles split along K with early partials: at most
         // one split per unit, the early splits first and the owners last, after
         // at least one whole wave (so an owner never waits for its partials)
-        if (rest > 0 && dp >= units && !pinned && plan->d_flags && acc != GEMM_F16 && kCfgTileN[kind] >= 128) {
+        if (rest > 0 && dp >= units && !pinned && plan->flags_ready && acc != GEMM_F16 && kCfgTileN[kind] >= 128) {
             for (int64_t s = 2; s <= 4; ++s) {
                 if (rest * s > units || s > kb || rest * s * tile_bytes > static_cast<int64_t>(plan->ws_bytes) ||
                     rest * s * kCfgCtas[kind] > kNumCounters)
@@ -300,7 +300,7 @@ Choice choose(const gemm_plan* plan, int64_t M, int64_t N, int64_t K, gemm_dtype
         // written), so the model offers it only when it is pinned or when the
         // autotuner times every candidate.
         const bool offer_stream_k = all != nullptr || plan->forced_division == GEMM_DIVISION_STREAM_K;
-        if (offer_stream_k && rest > 0 && dp >= 2 * units && !pinned && plan->d_flags && acc != GEMM_F16 &&
+        if (offer_stream_k && rest > 0 && dp >= 2 * units && !pinned && plan->flags_ready && acc != GEMM_F16 &&
             kCfgTileN[kind] == 256 &&
             (units + 1) * 2 * kCfgCtas[kind] <= kNumCounters &&
             static_cast<int64_t>(units + 1) * 2 * tile_bytes <= static_cast<int64_t>(plan->ws_bytes)) {
@@ -404,6 +404,10 @@ Choice select_choice(const gemm_plan* plan, int64_t M, int64_t N, int64_t K, gem
     return choose(plan, M, N, K, acc, lb == GEMM_ROW_MAJOR, valid);
 }
 
+gemm_status_t describe_impl(const gemm_plan* plan, int64_t M, int64_t N, int64_t K, gemm_layout_t layoutA,
+                            gemm_layout_t layoutB, gemm_dtype_t accum_dtype, gemm_dtype_t out_dtype, char* buf,
+                            int64_t len);
+
 // Launch one chosen configuration (arguments already validated, M, N, K > 0).
 gemm_status_t run_choice(gemm_plan* plan, const Choice& ch, const void* A, const void* B, const void* C, void* D,
                          int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
@@ -492,6 +496,7 @@ gemm_status_t gemm_plan_create(gemm_plan_t* out, int device, gemm_dtype_t in_dty
               cudaMalloc(&plan->d_flags, kNumCounters * sizeof(unsigned)) == cudaSuccess &&
               cudaMemset(plan->d_flags, 0, kNumCounters * sizeof(unsigned)) == cudaSuccess &&
               prepare_all(plan) == GEMM_OK;
+    plan->flags_ready = ok;
     if (!ok) {
         cudaGetLastError();
         if (plan->d_status) cudaFree(plan->d_status);
@@ -707,7 +712,30 @@ int gemm_plan_sm_count(gemm_plan_t plan) { return plan ? plan->sm_count : 0; }
 gemm_status_t gemm_plan_describe(gemm_plan_t plan, int64_t M, int64_t N, int64_t K, gemm_layout_t layoutA,
                                  gemm_layout_t layoutB, gemm_dtype_t accum_dtype, gemm_dtype_t out_dtype,
                                  char* buf, int64_t len) {
-    if (!plan || !buf || len <= 0) return GEMM_ERR_INVALID_ARG;
+    if (!plan) return GEMM_ERR_INVALID_ARG;
+    return describe_impl(plan, M, N, K, layoutA, layoutB, accum_dtype, out_dtype, buf, len);
+}
+
+gemm_status_t gemm_describe_model(int sm_count, gemm_dtype_t in_dtype, int64_t M, int64_t N, int64_t K,
+                                  gemm_layout_t layoutA, gemm_layout_t layoutB, gemm_dtype_t accum_dtype,
+                                  gemm_dtype_t out_dtype, char* buf, int64_t len) {
+    if (sm_count < 2 || sm_count > 4096 || !valid_dtype(in_dtype) || in_dtype == GEMM_F32) return GEMM_ERR_INVALID_ARG;
+    gemm_plan model;   // never touches a device: the cost model reads only these fields
+    model.sm_count = sm_count;
+    model.in_dtype = in_dtype;
+    model.ws_bytes = kWorkspaceBytes;
+    model.flags_ready = true;
+    return describe_impl(&model, M, N, K, layoutA, layoutB, accum_dtype, out_dtype, buf, len);
+}
+
+}  // extern "C"
+
+namespace {
+
+gemm_status_t describe_impl(const gemm_plan* plan, int64_t M, int64_t N, int64_t K, gemm_layout_t layoutA,
+                            gemm_layout_t layoutB, gemm_dtype_t accum_dtype, gemm_dtype_t out_dtype, char* buf,
+                            int64_t len) {
+    if (!buf || len <= 0) return GEMM_ERR_INVALID_ARG;
     const int64_t lda = layoutA == GEMM_ROW_MAJOR ? K : M, ldb = layoutB == GEMM_ROW_MAJOR ? N : K;
     const int64_t pad = 16 / dtype_bytes(plan->in_dtype);   // leading dimensions taken as 16-byte multiples
     gemm_status_t st = validate(plan->in_dtype, nullptr, nullptr, nullptr, nullptr, M, N, K,
@@ -738,6 +766,10 @@ gemm_status_t gemm_plan_describe(gemm_plan_t plan, int64_t M, int64_t N, int64_t
                   static_cast<long long>(units * kCfgCtas[ch.kind]), plan->sm_count, source);
     return GEMM_OK;
 }
+
+}  // namespace
+
+extern "C" {
 
 gemm_status_t gemm_plan_destroy(gemm_plan_t plan) {
     if (!plan) return GEMM_OK;

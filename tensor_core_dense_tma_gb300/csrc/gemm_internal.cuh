@@ -99,6 +99,7 @@ struct gemm_plan {
     float* d_ws = nullptr;        // split-K partials
     int* d_counters = nullptr;    // split-K arrival counters (kept zero between launches)
     unsigned* d_flags = nullptr;  // early-partial ready flags, kNumCounters (null: none)
+    bool flags_ready = false;     // d_flags allocated: early partials and stream-K are available
     uint64_t timeout_ns = 2000000000ull;
     uint64_t launches = 0;
     tcdt_host::EncodeTiledFn encode = nullptr;
