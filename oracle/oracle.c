@@ -41,7 +41,7 @@
  *    rounding mode; binary16/bfloat16 by the encoder below).  This holds for
  *    the fp16-accumulate mode too: the oracle's value there is the exact
  *    result rounded once to binary16, and the fp16 accumulation of the
- *    device path is judged against it with the looser fp16 tolerance.
+ *    device path is compared with it under the looser fp16 tolerance.
  *  - Alongside D it can return the unrounded value V and the error scale
  *    S[i,j] = |alpha| * sum_k |A[i,k] B[k,j]| + |beta * C[i,j]|.
  *
