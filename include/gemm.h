@@ -24,6 +24,8 @@
  * Supported (input, accumulator, output) combinations:
  *   fp16: (f32 acc -> f32, f16 or bf16 out), (f16 acc -> f16 out)
  *   bf16: (f32 acc -> f32 or bf16 out)
+ *   E4M3, E5M2, TF32: (f32 acc -> f32, f16 or bf16 out), K-major operands
+ *   (see gemm_dtype_t)
  * fp32 accumulation is the standard ("深入CUDA Tensor Core与WMMA", sections
  * 6.2 and 7.1); fp16 accumulation is the f16.f16.f16.f16 form of
  * "hgemm_mma_m16n8k16_naive_kernel详解", section 1.1.  alpha and beta are
@@ -35,13 +37,14 @@
  * never frees or retains them after a call returns.  gemm_run is
  * asynchronous on `stream` (a cudaStream_t; NULL = the legacy default
  * stream) and synchronises nothing; results are visible after the caller
- * synchronises the stream.  A plan holds device state (a status word) and
- * must not be used from two streams at once.
+ * synchronises the stream.  A plan holds device state (a status word,
+ * split-K partials and counters, early-partial flags) and must not be used
+ * from two streams at once, nor from two host threads at once.
  *
  * Alignment ("CUDA算子优化(5)：WMMA矩阵乘法", load_matrix_sync: ldm a
  * multiple of 16 bytes): A and B must start on 16-byte boundaries and
- * lda*2, ldb*2 must be multiples of 16 bytes (A and B are read by the
- * tensor-memory accelerator).  C and D need only element alignment; any
+ * lda and ldb times the element size must be multiples of 16 bytes (A and B
+ * are read by the tensor-memory accelerator).  C and D need only element alignment; any
  * ldc >= N is accepted (unaligned rows take a scalar store path).
  *
  * Errors.  Every entry point returns a gemm_status_t and leaves its
