@@ -15,21 +15,26 @@
 // How it maps onto sm_103a (the pages' WMMA / mma.sync kernels are prior art
 // for older GPUs; this is a Blackwell design):
 //   * persistent CTAs (or CTA pairs) walk work items in a grouped raster; a
-//     work item is an output tile, or one of `splits` contiguous K ranges of
-//     a tile when there are too few tiles to fill the GPU;
-//   * warp 0, one thread: TMA loads of 128-byte-swizzled A and B slices into a
+//     work item is an output tile, or -- for the last, partial wave of tiles
+//     -- a K range of a tile (split with a last-arriver reduction, or with
+//     early partials; or stream-K ranges joined the same way) or a
+//     half-width tile (see unit_item);
+//   * warp 0: TMA loads of 128-byte-swizzled A and B slices (one 128-byte row
+//     of each operand row per K block, whatever the operand kind) into a
 //     STAGES-deep shared-memory ring, each stage guarded by a "full" and an
-//     "empty" mbarrier;
+//     "empty" mbarrier; one elected lane issues, the warp runs the loop;
 //   * warp 1: allocates tensor memory (two 128 x BN fp32 accumulators per
-//     CTA); one thread of the pair's leader issues tcgen05.mma (kind::f16)
-//     for every 16-deep K step, and tcgen05.commit frees the stage / publishes
-//     the finished accumulator;
+//     CTA); one elected lane of the pair's leader issues tcgen05.mma
+//     (kind::f16, kind::f8f6f4 or kind::tf32) for every 32 bytes of K, and
+//     tcgen05.commit frees the stage / publishes the finished accumulator;
 //   * warps 2..5: epilogue -- tcgen05.ld of the accumulator, alpha/beta*C in
-//     fp32, RNE cast, 16-byte stores for the aligned part of each row segment
-//     and element stores for the unaligned head/tail and the masked edges.
-//     Split K: every split writes its fp32 partial to a workspace; the last
-//     split to arrive adds all partials in split order (a fixed order, so the
-//     result does not depend on which split finishes last) and stores.
+//     fp32 (with the fused scales, bias and activation in the EP variant),
+//     RNE cast, TMA stores through swizzled staging for aligned tiles and
+//     coalesced row-block stores otherwise; early splits write fp32 partials
+//     and a ready flag, and the epilogue warps seed an owner's accumulator
+//     from them (tcgen05.st) while the previous tile's MMAs run; the
+//     last-arriver split adds all partials in split order (a fixed order, so
+//     the result does not depend on which split finishes last) and stores.
 //   * `trans_out`: the kernel computes the transposed product (used for
 //     D^T = B^T A^T when M is small) and stores element (r, c) at D[c*ldc + r].
 // Every mbarrier wait is bounded: when a wait exceeds the plan's limit the
