@@ -252,7 +252,9 @@ int gemm_plan_sm_count(gemm_plan_t plan);
  * back: synchronise it before reading D.  Calls on one plan are ordered
  * through their streams; the host buffers must stay valid until then.
  * Returns gemm_run's statuses; growing the staging buffers synchronises
- * `stream`. */
+ * `stream`.  Arguments are checked before anything is queued; if a CUDA call
+ * fails part way, the internal streams are drained and rows of D already
+ * copied back stay written. */
 gemm_status_t gemm_run_host(gemm_plan_t plan, const void *A, const void *B, const void *C, void *D,
                             int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
                             gemm_layout_t layoutA, gemm_layout_t layoutB,
