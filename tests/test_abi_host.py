@@ -125,3 +125,42 @@ def test_validate_rejects(lib, kw, code):
 ])
 def test_validate_accepts(lib, kw):
     assert v(**kw) == OK
+
+
+C_CALLER = r"""
+#include <stdio.h>
+#include <string.h>
+#include "gemm.h"
+
+int main(void) {
+    char buf[256];
+    /* argument checks need no device */
+    if (gemm_validate(GEMM_F16, (void *)16, (void *)16, NULL, (void *)16, 64, 64, 64, 64, 64, 64,
+                      GEMM_ROW_MAJOR, GEMM_ROW_MAJOR, GEMM_F32, GEMM_F32, 0.0f) != GEMM_OK) return 1;
+    if (gemm_validate(GEMM_F16, (void *)16, (void *)16, NULL, (void *)16, 64, 64, 64, 60, 64, 64,
+                      GEMM_ROW_MAJOR, GEMM_ROW_MAJOR, GEMM_F32, GEMM_F32, 0.0f) != GEMM_ERR_INVALID_ARG) return 2;
+    /* the cost model without a device */
+    if (gemm_describe_model(152, GEMM_F16, 4096, 4096, 4096, GEMM_ROW_MAJOR, GEMM_ROW_MAJOR, GEMM_F32,
+                            GEMM_F32, buf, (int64_t)sizeof(buf)) != GEMM_OK) return 3;
+    if (strncmp(buf, "tc2cta_256x256", 14) != 0) return 4;
+    if (strcmp(gemm_status_string(GEMM_ERR_TIMEOUT), "GEMM_ERR_TIMEOUT") != 0) return 5;
+    printf("%s\n", buf);
+    return 0;
+}
+"""
+
+
+def test_plain_c_caller(lib, tmp_path):
+    """The header compiles as C99 and a C program links the library and
+    calls it (host-only entry points)."""
+    src = tmp_path / "caller.c"
+    src.write_text(C_CALLER)
+    exe = tmp_path / "caller"
+    lib_dir = os.path.dirname(tcbuild.LIB_PATH)
+    r = subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"), str(src),
+                        "-L", lib_dir, "-l:" + os.path.basename(tcbuild.LIB_PATH), "-Wl,-rpath," + lib_dir,
+                        "-o", str(exe)], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    run = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert run.returncode == 0, (run.returncode, run.stderr)
+    assert run.stdout.startswith("tc2cta_256x256_acc32_out32_esplitk2")
