@@ -955,21 +955,18 @@ __device__ __forceinline__ void stage_row_and_store(const void* tmap, const uint
     sbuf ^= 1;
 }
 
-// Epilogue values of one segment -> D through the staging buffer.
+// Epilogue values of one segment -> D through the staging buffer.  `ec`:
+// the segment's epilogue vectors (EP), loaded a segment ahead by the caller.
 template <class Cfg, bool EP>
 __device__ __forceinline__ void stage_and_store(const KernelParams& p, const void* tmap, float (&v)[32], int row,
                                                 int col0, int row0w, int lane, uint32_t stg, int& sbuf,
-                                                bool row_ok) {
+                                                bool row_ok, const EpLane& ec) {
     constexpr int ESZ = Vec<Cfg::OUT>::ESZ;
     float acc[32];
 #pragma unroll
     for (int i = 0; i < 32; ++i) acc[i] = v[i];
-    EpLane ec{};
     if constexpr (EP) {
-        if (p.ep) {
-            ec = ep_lane<32>(p, row, col0, lane);
-            ep_scale_w<32>(p, ec, acc);
-        }
+        if (p.ep) ep_scale_w<32>(p, ec, acc);
     }
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] = p.alpha * acc[i];
@@ -1456,10 +1453,20 @@ gemm_sm103_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                                   (static_cast<uint64_t>(x.kb1 - x.kb0) * static_cast<uint64_t>(2 * nchunks));
                         }
                         t_prev_acc = t_acc;
+                        // the epilogue vectors of each segment are loaded one segment
+                        // ahead, so their latency overlaps the previous segment's work
+                        EpLane ec_next{};
+                        if constexpr (EP) {
+                            if (p.ep) ec_next = ep_lane<32>(p, row, n0, lane);
+                        }
 #pragma unroll 1
                         for (int c = 0; c < nchunks; ++c) {
                             const int col0 = n0 + W * c;
                             if (col0 >= p.N) break;   // warp-uniform
+                            const EpLane ec = ec_next;
+                            if constexpr (EP) {
+                                if (p.ep && c + 1 < nchunks) ec_next = ep_lane<32>(p, row, col0 + W, lane);
+                            }
                             if (gap) {
                                 const uint64_t until = t_acc + static_cast<uint64_t>(c) * gap;
 #pragma unroll 1
@@ -1473,7 +1480,7 @@ gemm_sm103_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                             float v[W];
 #pragma unroll
                             for (int i = 0; i < W; ++i) v[i] = acc_value<Cfg::ACC_F16>(r[i]);
-                            stage_and_store<Cfg, EP>(p, &tmD, v, row, col0, row0w, lane, stg, sbuf, row_ok);
+                            stage_and_store<Cfg, EP>(p, &tmD, v, row, col0, row0w, lane, stg, sbuf, row_ok, ec);
                         }
                     }
                 }
