@@ -73,3 +73,30 @@ def test_storage_and_logical_views():
     LB = wl.logical(t.B, w.K, w.N, "col")
     assert LB.shape == (5, 6)
     assert LB[3, 4] == t.B[4, 3]
+
+
+def test_narrow_operand_inputs():
+    """E4M3 / E5M2 inputs are the 8-bit torch types (RNE of the fp32 draw);
+    TF32 inputs are fp32 values with the 13 low fraction bits cleared (the
+    tensor cores then read them exactly); bytes per element follow the type."""
+    for name, dt, esz in (("e4m3_8192", torch.float8_e4m3fn, 1), ("e5m2_8192", torch.float8_e5m2, 1),
+                          ("tf32_4096", torch.float32, 4)):
+        w = wl.WORKLOADS[name]
+        small = w.with_shape(64, 48, 96)
+        h = wl.make_inputs(small)
+        assert h.A.dtype == dt and h.B.dtype == dt
+        assert (small.layoutA, small.layoutB) == ("row", "col")
+        assert wl.ELEMENT_BYTES[w.in_dtype] == esz
+        if name.startswith("tf32"):
+            assert int((h.A.view(torch.int32) & 8191).abs().sum()) == 0
+            assert int((h.B.view(torch.int32) & 8191).abs().sum()) == 0
+        else:
+            bits = wl.bits(h.A)
+            assert bits.dtype == np.uint8 and bits.shape == tuple(h.A.shape)
+        out_b = wl.ELEMENT_BYTES[w.out_dtype]
+        assert w.algorithmic_bytes() == (w.M * w.K + w.K * w.N) * esz + w.M * w.N * out_b
+    # integer twins stay exact in every narrow type
+    for name in ("e4m3_8192", "e5m2_8192", "tf32_4096"):
+        h = wl.make_inputs(wl.WORKLOADS[name].with_shape(16, 16, 32), integer=True)
+        vals = h.A.to(torch.float32)
+        assert set(np.unique(vals.numpy()).tolist()) <= {-2.0, -1.0, 0.0, 1.0, 2.0}
