@@ -287,6 +287,22 @@ gemm_status_t gemm_plan_autotune(gemm_plan_t plan, const void *A, const void *B,
                                  float alpha, float beta, int reps, void *stream,
                                  char *report, int64_t report_len);
 
+/* The plan's autotuned choices as text, one line per shape:
+ *   "M N K layoutA layoutB accum_dtype out_dtype config\n"
+ * (enum values as integers; config named as gemm_plan_describe names it),
+ * NUL-terminated into buf (at most `len` bytes).  `needed` (optional)
+ * receives the size the text needs, NUL included; len == 0 only reports it.
+ * GEMM_ERR_INVALID_ARG if buf is too small (nothing written then). */
+gemm_status_t gemm_plan_tuning_export(gemm_plan_t plan, char *buf, int64_t len, int64_t *needed);
+
+/* Load choices written by gemm_plan_tuning_export (on this run or another,
+ * for a plan of the same input type).  Every line must name a configuration
+ * the plan's cost model offers for that shape (the autotuner's candidates);
+ * the first line that does not, or that does not parse, makes the call
+ * return GEMM_ERR_INVALID_ARG with nothing loaded.  Loaded entries replace
+ * existing ones for the same shape. */
+gemm_status_t gemm_plan_tuning_import(gemm_plan_t plan, const char *text);
+
 /* Forget every autotuned choice of the plan (the cost model decides again). */
 gemm_status_t gemm_plan_clear_tuning(gemm_plan_t plan);
 

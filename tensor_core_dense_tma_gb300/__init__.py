@@ -105,6 +105,10 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.gemm_mma_fragment_map.restype = i32
     lib.gemm_plan_force_division.argtypes = [p, i32, i32]
     lib.gemm_plan_force_division.restype = i32
+    lib.gemm_plan_tuning_export.argtypes = [p, ctypes.c_char_p, i64, ctypes.POINTER(i64)]
+    lib.gemm_plan_tuning_export.restype = i32
+    lib.gemm_plan_tuning_import.argtypes = [p, ctypes.c_char_p]
+    lib.gemm_plan_tuning_import.restype = i32
     lib.gemm_plan_clear_tuning.argtypes = [p]
     lib.gemm_plan_clear_tuning.restype = i32
     lib.gemm_plan_tuned_count.argtypes = [p]
@@ -511,6 +515,24 @@ class Plan:
             rows.append({"config": parts[0], "model_cost": float(kv["model_cost"]), "us": float(kv["us"]),
                          "chosen": chosen, "model": "(model)" in line})
         return D, rows
+
+    def export_tuning(self) -> str:
+        """The autotuned choices as text (gemm_plan_tuning_export)."""
+        need = ctypes.c_int64(0)
+        st = load().gemm_plan_tuning_export(self.handle, None, 0, ctypes.byref(need))
+        if st != 0:
+            raise GemmError(st, "gemm_plan_tuning_export")
+        buf = ctypes.create_string_buffer(max(1, need.value))
+        st = load().gemm_plan_tuning_export(self.handle, buf, need.value, None)
+        if st != 0:
+            raise GemmError(st, "gemm_plan_tuning_export")
+        return buf.value.decode()
+
+    def import_tuning(self, text: str):
+        """Load choices written by export_tuning (gemm_plan_tuning_import)."""
+        st = load().gemm_plan_tuning_import(self.handle, text.encode())
+        if st != 0:
+            raise GemmError(st, "gemm_plan_tuning_import")
 
     def clear_tuning(self):
         st = gemm_plan_clear_tuning(self.handle)

@@ -647,6 +647,97 @@ int64_t gemm_plan_tuned_count(gemm_plan_t plan) {
     return plan && plan->tuned ? static_cast<int64_t>(plan->tuned->best.size()) : 0;
 }
 
+gemm_status_t gemm_plan_tuning_export(gemm_plan_t plan, char* buf, int64_t len, int64_t* needed) {
+    if (!plan || (len > 0 && !buf) || len < 0) return GEMM_ERR_INVALID_ARG;
+    std::string text;
+    if (plan->tuned) {
+        for (const auto& kv : plan->tuned->best) {
+            const TuneKey& k = kv.first;
+            char line[256];
+            std::snprintf(line, sizeof(line), "%lld %lld %lld %lld %lld %lld %lld %s\n",
+                          static_cast<long long>(k[0]), static_cast<long long>(k[1]), static_cast<long long>(k[2]),
+                          static_cast<long long>(k[3]), static_cast<long long>(k[4]), static_cast<long long>(k[5]),
+                          static_cast<long long>(k[6]),
+                          config_name(kv.second, static_cast<gemm_dtype_t>(k[5]), static_cast<gemm_dtype_t>(k[6]))
+                              .c_str());
+            text += line;
+        }
+    }
+    if (needed) *needed = static_cast<int64_t>(text.size()) + 1;
+    if (len == 0) return GEMM_OK;
+    if (static_cast<int64_t>(text.size()) + 1 > len) return GEMM_ERR_INVALID_ARG;
+    std::memcpy(buf, text.c_str(), text.size() + 1);
+    return GEMM_OK;
+}
+
+gemm_status_t gemm_plan_tuning_import(gemm_plan_t plan, const char* text) {
+    if (!plan || !text) return GEMM_ERR_INVALID_ARG;
+    // every line is checked and resolved to one of the model's own candidates
+    // for its shape before anything is stored, so an entry can only name a
+    // choice the plan could have made itself
+    std::vector<std::pair<TuneKey, Choice>> entries;
+    const int saved_kind = plan->forced_kind, saved_splits = plan->forced_splits;
+    const int saved_div = plan->forced_division, saved_div_splits = plan->forced_division_splits;
+    plan->forced_kind = -1;
+    plan->forced_splits = 0;
+    plan->forced_division = GEMM_DIVISION_AUTO;
+    plan->forced_division_splits = 0;
+    gemm_status_t st = GEMM_OK;
+    const char* p = text;
+    while (*p && st == GEMM_OK) {
+        const char* eol = std::strchr(p, '\n');
+        const std::string line(p, eol ? static_cast<size_t>(eol - p) : std::strlen(p));
+        p = eol ? eol + 1 : p + line.size();
+        if (line.find_first_not_of(" \t\r") == std::string::npos) continue;
+        long long v[7];
+        char name[128];
+        if (std::sscanf(line.c_str(), "%lld %lld %lld %lld %lld %lld %lld %127s", &v[0], &v[1], &v[2], &v[3], &v[4],
+                        &v[5], &v[6], name) != 8) {
+            st = GEMM_ERR_INVALID_ARG;
+            break;
+        }
+        const int64_t M = v[0], N = v[1], K = v[2];
+        if (!valid_layout(static_cast<int>(v[3])) || !valid_layout(static_cast<int>(v[4])) ||
+            !valid_dtype(static_cast<int>(v[5])) || !valid_dtype(static_cast<int>(v[6])) || M <= 0 || N <= 0 ||
+            K <= 0) {
+            st = GEMM_ERR_INVALID_ARG;
+            break;
+        }
+        const gemm_layout_t la = static_cast<gemm_layout_t>(v[3]), lb = static_cast<gemm_layout_t>(v[4]);
+        const gemm_dtype_t acc = static_cast<gemm_dtype_t>(v[5]), out = static_cast<gemm_dtype_t>(v[6]);
+        const int64_t pad = 16 / dtype_bytes(plan->in_dtype);
+        const int64_t lda = la == GEMM_ROW_MAJOR ? K : M, ldb = lb == GEMM_ROW_MAJOR ? N : K;
+        st = validate(plan->in_dtype, nullptr, nullptr, nullptr, nullptr, M, N, K, (lda + pad - 1) / pad * pad,
+                      (ldb + pad - 1) / pad * pad, N, la, lb, acc, out, 0.0f, false);
+        if (st != GEMM_OK) break;
+        std::vector<Candidate> cands;
+        bool valid = true;
+        choose(plan, M, N, K, acc, lb == GEMM_ROW_MAJOR, &valid, &cands, true);
+        const Candidate* hit = nullptr;
+        for (const Candidate& c : cands)
+            if (config_name(c.choice, acc, out) == name) {
+                hit = &c;
+                break;
+            }
+        if (!valid || !hit) {
+            st = GEMM_ERR_INVALID_ARG;
+            break;
+        }
+        entries.push_back({tune_key(M, N, K, la, lb, acc, out), hit->choice});
+    }
+    plan->forced_kind = saved_kind;
+    plan->forced_splits = saved_splits;
+    plan->forced_division = saved_div;
+    plan->forced_division_splits = saved_div_splits;
+    if (st != GEMM_OK) return st;
+    if (!plan->tuned) {
+        plan->tuned = new (std::nothrow) TunedTable();
+        if (!plan->tuned) return GEMM_ERR_CUDA;
+    }
+    for (const auto& e : entries) plan->tuned->best[e.first] = e.second;
+    return GEMM_OK;
+}
+
 gemm_status_t gemm_plan_device_status(gemm_plan_t plan, int clear) {
     if (!plan) return GEMM_ERR_INVALID_ARG;
     DeviceGuard guard(plan->device);

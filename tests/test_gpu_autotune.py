@@ -117,3 +117,37 @@ def test_autotune_rejects_bad_reps(plans):
     with pytest.raises(tc.GemmError) as e:
         plans["f16"].autotune(A, B, C, D[:, :w.N], reps=0)
     assert e.value.status == 1
+
+
+def test_tuning_export_import(plans):
+    """Tuned choices move between plans as text; a line naming a
+    configuration the model does not offer for its shape is rejected whole."""
+    import tensor_core_dense_tma_gb300 as tc
+    w = SHAPES["few_tiles"]
+    src = plans["bf16"]
+    src.clear_tuning()
+    h = _inputs(w)
+    A, B, C, D = _tensors(w, h)
+    _, rows = src.autotune(A, B, C, D[:, :w.N], reps=1, alpha=w.alpha, beta=w.beta, accum_dtype=w.accum_dtype,
+                           out_dtype=w.out_dtype)
+    chosen = next(r["config"] for r in rows if r["chosen"])
+    text = src.export_tuning()
+    assert text.count("\n") == 1 and text.split()[:3] == ["1024", "1024", "4096"] and text.split()[7] == chosen
+    with tc.Plan("bf16", 0) as dst:
+        dst.import_tuning(text)
+        assert dst.tuned_count == 1
+        desc = dst.describe(w.M, w.N, w.K, w.layoutA, w.layoutB, w.accum_dtype, w.out_dtype)
+        assert desc.split()[0] == chosen and desc.endswith("source=tuned")
+        D2 = torch.full_like(D, float("nan"))
+        dst.gemm(A, B, C, D2[:, :w.N], alpha=w.alpha, beta=w.beta, accum_dtype=w.accum_dtype, out_dtype=w.out_dtype)
+        torch.cuda.synchronize()
+        check_full(w, h, D2, integer=True)
+        # a configuration that is not a candidate for the shape, and garbage
+        bad = text.replace(chosen, "tc1cta_128x16_acc32_outbf16_swapAB")
+        for t in (bad, "1 2 3\n", text + "x y z\n"):
+            with pytest.raises(tc.GemmError) as e:
+                dst.import_tuning(t)
+            assert e.value.status == 1
+        assert dst.tuned_count == 1
+        assert dst.export_tuning() == text
+    src.clear_tuning()
