@@ -230,12 +230,16 @@ def encode(values: np.ndarray, dtype: str, lib: ctypes.CDLL | None = None) -> np
 
 
 def ulp(values: np.ndarray, dtype: str) -> np.ndarray:
-    """Spacing of the output format at |values| (for the half-ulp term of the
-    tolerance on 16-bit outputs).  binary16: 10 fraction bits, smallest
+    """Spacing of the output format in the binade of |values| (the half-ulp
+    term of the tolerance on 16-bit outputs): 2^(e - frac) where
+    2^e <= |v| < 2^(e+1), and 2^(emin - frac) below the smallest normal
+    (sub-normals are evenly spaced).  binary16: 10 fraction bits, smallest
     normal 2^-14; bfloat16: 7 fraction bits, smallest normal 2^-126;
-    float32: 23 fraction bits, smallest normal 2^-126."""
+    float32: 23 fraction bits, smallest normal 2^-126.  The exponent comes
+    from frexp (exact), not from a rounded logarithm."""
     frac, emin = {"f16": (10, -14), "bf16": (7, -126), "f32": (23, -126)}[dtype]
     a = np.abs(np.asarray(values, dtype=np.float64))
-    e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
-    e = np.maximum(np.where(a > 0, e, emin), emin)
-    return np.ldexp(1.0, (e - frac).astype(np.int64))
+    _, e2 = np.frexp(a)                       # a = m * 2^e2 with 0.5 <= m < 1
+    e = np.where(a > 0, e2.astype(np.int64) - 1, emin)
+    e = np.maximum(e, emin)
+    return np.ldexp(1.0, e - frac)

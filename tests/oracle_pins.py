@@ -552,4 +552,98 @@ def pin_tf32_real_against_float64_matmul(lib):
     assert np.array_equal(D, V.astype(np.float32))
 
 
+# --------------------------------------------------------------------------
+# The half-ulp term of the 16-bit-output tolerance (oracle.ulp)
+# --------------------------------------------------------------------------
+
+def pin_ulp_f16_against_numpy_spacing(lib):
+    """oracle.ulp for binary16 at every positive finite binary16 value but the
+    largest (whose numpy spacing is the step to infinity) equals numpy's
+    np.spacing of that value: sub-normals, the smallest normal and every
+    binade up to 2^15."""
+    pats = np.arange(0x0001, 0x7BFF, dtype=np.uint16)          # 0x7BFF = 65504 excluded
+    x16 = pats.view(np.float16)
+    want = np.spacing(x16).astype(np.float64)
+    got = oracle.ulp(x16.astype(np.float64), "f16")
+    assert np.array_equal(got, want), "binary16 ulp differs from numpy spacing"
+    # the largest value lies in the binade [2^15, 2^16): spacing 2^5
+    assert oracle.ulp(np.array([65504.0]), "f16")[0] == 32.0
+
+
+def pin_ulp_bf16_against_torch_successor(lib):
+    """oracle.ulp for bfloat16 equals the distance from each positive finite
+    bfloat16 value to its successor, both decoded by torch."""
+    import torch
+    pats = np.arange(0x0001, 0x7F7F, dtype=np.int32)           # 0x7F7F = largest finite
+    here = torch.from_numpy(pats.astype(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+    nxt = torch.from_numpy((pats + 1).astype(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+    got = oracle.ulp(here, "bf16")
+    assert np.array_equal(got, nxt - here), "bfloat16 ulp differs from torch's successor step"
+
+
+def pin_ulp_f32_against_numpy_spacing(lib):
+    """oracle.ulp for binary32 equals numpy's np.spacing over sub-normals,
+    normals and every binade edge."""
+    rng = np.random.default_rng(31)
+    pats = np.concatenate([np.arange(1, 4096, dtype=np.uint32),
+                           rng.integers(1, 0x7F7FFFFF, 200000, dtype=np.uint32),
+                           (np.arange(1, 255, dtype=np.uint32) << 23),
+                           (np.arange(1, 255, dtype=np.uint32) << 23) - 1])
+    x32 = pats.view(np.float32)
+    got = oracle.ulp(x32.astype(np.float64), "f32")
+    assert np.array_equal(got, np.spacing(x32).astype(np.float64)), "binary32 ulp differs from numpy"
+
+
+def pin_ulp_fixed_values(lib):
+    """Values fixed by the formats: bfloat16 has 8 significant bits (ulp(1) =
+    2^-7, ulp(256) = 2), binary16 11 (ulp(1) = 2^-10, ulp(65504) = 32) with
+    sub-normals spaced 2^-24 (also at 0 and at the smallest normal 2^-14);
+    the binade is that of the value itself, also just below a power of two
+    (where a rounded log2 would step into the next binade) and between
+    representable values."""
+    u = oracle.ulp
+    assert u(np.array([1.0, 256.0]), "bf16").tolist() == [2.0 ** -7, 2.0]
+    assert u(np.array([1.0, 65504.0, 2.0 ** -14, 0.0, 2.0 ** -24, 3 * 2.0 ** -24]), "f16").tolist() == \
+        [2.0 ** -10, 32.0, 2.0 ** -24, 2.0 ** -24, 2.0 ** -24, 2.0 ** -24]
+    assert u(np.array([-1.0, -65504.0]), "f16").tolist() == [2.0 ** -10, 32.0]
+    for k in range(-13, 17):
+        below = np.nextafter(2.0 ** k, 0.0)
+        assert u(np.array([below]), "f16")[0] == 2.0 ** (k - 1 - 10), k
+        assert u(np.array([below]), "bf16")[0] == 2.0 ** (k - 1 - 7), k
+        assert u(np.array([2.0 ** k * 1.3]), "f16")[0] == 2.0 ** (k - 10), k
+
+
+# --------------------------------------------------------------------------
+# The thread split of the oracle (rows of D, or sampled entries)
+# --------------------------------------------------------------------------
+
+def pin_threads_split_rows_and_entries(lib):
+    """Threads only divide the work: the full product and the sampled entries
+    with 3, 7 and 64 threads on ragged shapes (fewer rows than threads too)
+    equal the one-thread result bit for bit, every row and entry written."""
+    rng = np.random.default_rng(41)
+    for M, N, K in ((13, 37, 29), (131, 19, 45)):
+        A = _f16_bits(rng.uniform(-1, 1, (M, K)))
+        B = _f16_bits(rng.uniform(-1, 1, (N, K)))            # column-major K x N
+        C = rng.standard_normal((M, N)).astype(np.float32)
+        bias = rng.standard_normal(N).astype(np.float32)
+        kw = dict(lib=lib, want_exact=True, bias=bias, act="gelu")
+        D1, V1, S1 = oracle.gemm("f16", A, B, C, M, N, K, K, K, N, "row", "col", "f32", 0.5, 1.0,
+                                 nthreads=1, **kw)
+        assert np.all(S1 > 0), "a row of the one-thread result was not written"
+        ii = np.concatenate([np.arange(M), rng.integers(0, M, 50)])
+        jj = np.concatenate([np.arange(M) % N, rng.integers(0, N, 50)])
+        _, Ve1, Se1 = oracle.gemm_entries("f16", A, B, C, ii, jj, M, N, K, K, K, N, "row", "col", "f32",
+                                          0.5, 1.0, nthreads=1, lib=lib, bias=bias, act="gelu")
+        assert np.array_equal(Ve1, V1[ii, jj]) and np.array_equal(Se1, S1[ii, jj])
+        for nt in (3, 7, 64):
+            D, V, S = oracle.gemm("f16", A, B, C, M, N, K, K, K, N, "row", "col", "f32", 0.5, 1.0,
+                                  nthreads=nt, **kw)
+            assert np.array_equal(D.view(np.uint32), D1.view(np.uint32)), (M, nt)
+            assert np.array_equal(V, V1) and np.array_equal(S, S1), (M, nt)
+            _, Ve, Se = oracle.gemm_entries("f16", A, B, C, ii, jj, M, N, K, K, K, N, "row", "col", "f32",
+                                            0.5, 1.0, nthreads=nt, lib=lib, bias=bias, act="gelu")
+            assert np.array_equal(Ve, Ve1) and np.array_equal(Se, Se1), (M, nt)
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

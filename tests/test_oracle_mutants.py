@@ -48,6 +48,23 @@ MUTANTS = {
     "e5m2_read_as_e4m3": ("case OR_E5M2: return oracle_e5m2_decode", "case OR_E5M2: return oracle_e4m3_decode"),
     "tf32_low_bits_dropped": ("ldexp((double)(8388608u + f), e - 150)",
                               "ldexp((double)(8388608u + (f & 0x7fe000u)), e - 150)"),
+    # the thread split: a row or entry range that stops one short, or that
+    # skips the first row of every thread after the first
+    "row_end_off_by_one": ("w[t].row_end = M * (t + 1) / nt;", "w[t].row_end = M * (t + 1) / nt - 1;"),
+    "row_begin_skips_one": ("w[t].row_begin = M * t / nt;", "w[t].row_begin = M * t / nt + (t > 0);"),
+    "entry_end_off_by_one": ("w[t].e_end = n_entries * (t + 1) / nt;",
+                             "w[t].e_end = n_entries * (t + 1) / nt - (t + 1 < nt);"),
+}
+
+# Mistakes in the Python side of the oracle (oracle/__init__.py): the
+# tolerance's half-ulp term.
+PY_SRC = oracle.__file__
+PY_MUTANTS = {
+    "ulp_f16_frac_off_by_one": ('"f16": (10, -14)', '"f16": (9, -14)'),
+    "ulp_bf16_frac_off_by_one": ('"bf16": (7, -126)', '"bf16": (8, -126)'),
+    "ulp_f16_emin_off_by_one": ('"f16": (10, -14)', '"f16": (10, -15)'),
+    "ulp_exponent_from_log2": ("e = np.where(a > 0, e2.astype(np.int64) - 1, emin)",
+                               "e = np.where(a > 0, np.floor(np.log2(np.where(a > 0, a, 1.0))).astype(np.int64), emin)"),
 }
 
 
@@ -70,6 +87,28 @@ def test_mutant_is_caught(tmp_path, name):
     so = str(tmp_path / "liboracle_mut.so")
     oracle.build(str(mutated), so, force=True)
     lib = oracle.load_library(so)
+    failed = []
+    for pin in oracle_pins.ALL_PINS:
+        try:
+            pin(lib)
+        except AssertionError:
+            failed.append(pin.__name__)
+            break
+    assert failed, f"no pin caught the planted mistake {name}"
+
+
+@pytest.mark.parametrize("name", sorted(PY_MUTANTS))
+def test_python_mutant_is_caught(monkeypatch, name):
+    """A planted mistake in oracle.ulp (run from a mutated copy of the
+    module's source) must fail at least one pin."""
+    old, new = PY_MUTANTS[name]
+    with open(PY_SRC) as f:
+        src = f.read()
+    assert src.count(old) == 1, f"mutation site of {name} not found"
+    ns = {"__name__": "oracle_mutant", "__file__": PY_SRC}
+    exec(compile(src.replace(old, new), PY_SRC, "exec"), ns)
+    monkeypatch.setattr(oracle, "ulp", ns["ulp"])
+    lib = oracle.load_library()
     failed = []
     for pin in oracle_pins.ALL_PINS:
         try:
