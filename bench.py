@@ -15,6 +15,12 @@ whole is bracketed by a barrier and torch.cuda.synchronize().  With N > 1
 the same workload (a single GEMM of this size does not need to be sharded);
 value = the flops of all ranks / the slowest rank's time.
 
+The roofline object is that of the step's one kernel: the longer of the
+tensor-pipe bound (2*M*N*K at the measured dense peak) and the HBM bound
+(|A| + |B| (+ |C|) + |D| at the measured copy bandwidth) is `bound` (the
+skinny and ragged shapes are reported in GB/s, the square ones in
+TFLOP/s), the other one follows as `other_bound`.
+
 Prints one JSON line (rank 0).
 """
 from __future__ import annotations
@@ -254,6 +260,41 @@ def traffic_from_profiles(workload: str, kernel_tag: str):
     return float(val) if val else None
 
 
+def rooflines(w, avg_s: float, tensor_peak: float, hbm_peak: float, traffic, peak_src: str,
+              ratio: float) -> dict:
+    """The roofline of the step's one kernel.  Two bounds apply to a GEMM:
+    the tensor pipe (2*M*N*K flop at the measured dense peak) and HBM (the
+    algorithmic bytes |A| + |B| (+ |C|) + |D|, each moved once, at the
+    measured copy bandwidth).  The one that takes longer is the roofline
+    reported (`bound`); the other follows under `other_bound`, so shapes
+    below the ridge (skinny, ragged) are reported in GB/s and the square
+    ones in TFLOP/s."""
+    flops = float(w.flops)
+    nbytes = float(w.algorithmic_bytes())
+    t_flop = flops / (tensor_peak * 1e12)
+    t_byte = nbytes / (hbm_peak * 1e9)
+    src = "measured" if peak_src == "measured" else "fallback"
+    tensor = {"bound": "tensor", "achieved": flops / avg_s / 1e12, "peak": tensor_peak, "unit": "TFLOP/s",
+              "frac": t_flop / avg_s, "traffic": traffic,
+              "peak_source": (f"{src} bf16 dense GEMM burst (MEASURED_PEAKS.json)" if src == "measured"
+                              else "fallback 1.9 PFLOP/s bf16 burst")
+                             + (", fp16:bf16 = 1:1" if ratio == 1.0 else
+                                f", x {ratio:.3g} = the datasheet ratio of {w.in_dtype} to bf16 dense rates"),
+              "algorithmic": f"2*M*N*K = {flops:.4g} flop per launch"}
+    hbm = {"bound": "hbm", "achieved": nbytes / avg_s / 1e9, "peak": hbm_peak, "unit": "GB/s",
+           "frac": t_byte / avg_s, "traffic": traffic,
+           "peak_source": (f"{src} HBM copy bandwidth (MEASURED_PEAKS.json, read + write bytes)"
+                           if src == "measured" else "fallback 6.8 TB/s copy"),
+           "pct_of_nominal_7900_gbs": 100.0 * nbytes / avg_s / 7.9e12,
+           "algorithmic": f"|A|+|B|{'+|C|' if w.beta != 0.0 else ''}+|D| = {nbytes:.6g} bytes per launch"}
+    primary, other = (hbm, tensor) if t_byte > t_flop else (tensor, hbm)
+    primary["other_bound"] = other
+    primary["arithmetic_intensity_flop_per_byte"] = flops / nbytes
+    primary["ridge_flop_per_byte"] = tensor_peak * 1e12 / (hbm_peak * 1e9)
+    primary["bound_us"] = max(t_flop, t_byte) * 1e6
+    return primary
+
+
 def run_reference(args):
     """The CPU oracle on the host cores, each step a bounded sample."""
     rank = int(os.environ.get("RANK", "0"))
@@ -450,14 +491,9 @@ def main():
     kernel_tag = ("prior_art_" + args.prior_art if args.prior_art else
                   plan.describe(w.M, w.N, w.K, w.layoutA, w.layoutB, w.accum_dtype, w.out_dtype).split()[0])
     traffic = traffic_from_profiles(w.name, kernel_tag)
-    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak, "traffic": traffic,
-                "peak_source": (f"{peak_src} bf16 dense GEMM burst (MEASURED_PEAKS.json)"
-                                if peak_src == "measured" else "fallback 1.9 PFLOP/s bf16 burst")
-                               + (", fp16:bf16 = 1:1" if ratio == 1.0 else
-                                  f", x {ratio:.3g} = the datasheet ratio of {w.in_dtype} to bf16 dense rates"),
-                "kernel": kernel_tag,
-                "algorithmic": f"2*M*N*K = {w.flops:.4g} flop per launch"}
+    hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
+    roofline = rooflines(w, avg_s, peak, hbm_peak, traffic, peak_src, ratio)
+    roofline["kernel"] = kernel_tag
     try:
         # tensor-core rate probe (no memory traffic): cycles per 256x256x16 MMA and the peak
         # it implies at the clock measured meanwhile; outside the timed region

@@ -100,3 +100,30 @@ def test_narrow_operand_inputs():
         h = wl.make_inputs(wl.WORKLOADS[name].with_shape(16, 16, 32), integer=True)
         vals = h.A.to(torch.float32)
         assert set(np.unique(vals.numpy()).tolist()) <= {-2.0, -1.0, 0.0, 1.0, 2.0}
+
+
+def test_bench_roofline_picks_the_longer_bound():
+    """bench.py's roofline: skinny (16 x 8192 x 8192 bf16) is bound by HBM and
+    reported in GB/s, the square shapes by the tensor pipe in TFLOP/s, and
+    ragged (below the ridge) by HBM with the tensor bound beside it; the
+    figures are the algorithmic bytes / flops over the step time."""
+    import bench
+    tp, hp = 1954.3, 6655.6
+    sk = wl.WORKLOADS["skinny"]
+    r = bench.rooflines(sk, 33.384e-6, tp, hp, None, "measured", 1.0)
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s"
+    nbytes = 16 * 8192 * 2 + 8192 * 8192 * 2 + 16 * 8192 * 2
+    assert r["achieved"] == pytest.approx(nbytes / 33.384e-6 / 1e9)
+    assert r["frac"] == pytest.approx(nbytes / 33.384e-6 / 1e9 / hp)
+    assert r["other_bound"]["bound"] == "tensor"
+    assert r["other_bound"]["achieved"] == pytest.approx(2 * 16 * 8192 * 8192 / 33.384e-6 / 1e12)
+    sq = wl.WORKLOADS["sq4096"]
+    r = bench.rooflines(sq, 83.4e-6, tp, hp, 137374976.0, "measured", 1.0)
+    assert r["bound"] == "tensor" and r["unit"] == "TFLOP/s" and r["traffic"] == 137374976.0
+    assert r["achieved"] == pytest.approx(2 * 4096 ** 3 / 83.4e-6 / 1e12)
+    assert r["other_bound"]["bound"] == "hbm"
+    rg = wl.WORKLOADS["ragged"]
+    r = bench.rooflines(rg, 40e-6, tp, hp, None, "measured", 1.0)
+    assert r["bound"] == "hbm"                      # 211 flop/B, below the ridge of ~294
+    assert r["arithmetic_intensity_flop_per_byte"] == pytest.approx(rg.flops / rg.algorithmic_bytes())
+    assert r["bound_us"] == pytest.approx(rg.algorithmic_bytes() / (hp * 1e9) * 1e6)
