@@ -161,10 +161,30 @@ gemm_status_t gemm_validate(gemm_dtype_t in_dtype, const void *A, const void *B,
 
 /* Read the plan's device status word: GEMM_OK, or the first device-side
  * error (GEMM_ERR_TIMEOUT) recorded by any launch since the plan was
- * created or the word last cleared.  Synchronises nothing itself (the copy
- * is a blocking read of one word: call it after synchronising the stream).
- * `clear` != 0 resets the word to GEMM_OK afterwards. */
+ * created or the word last cleared.  The word is copied on a stream the
+ * plan owns (non-blocking) and the call waits for that copy alone: it
+ * synchronises no stream of the caller and not the device, so call it once
+ * the work to be checked is known to be finished (after synchronising its
+ * stream).  `clear` != 0 resets the word to GEMM_OK afterwards, together
+ * with the split-K arrival counters an aborted launch can leave behind.
+ * Returns GEMM_ERR_INVALID_ARG for a null plan, GEMM_ERR_CUDA if the copy
+ * fails. */
 gemm_status_t gemm_plan_device_status(gemm_plan_t plan, int clear);
+
+/* Stream-ordered form: enqueue on `stream` (a cudaStream_t, NULL = the
+ * legacy default stream) a copy of the status word -- host_status[0] the
+ * status, host_status[1] the site code -- into `host_status` (2 ints, owned
+ * by the caller; pinned memory for an asynchronous copy).  The values are
+ * there once `stream` has reached the copy; nothing is waited for here.
+ * GEMM_ERR_INVALID_ARG for a null plan or host_status. */
+gemm_status_t gemm_plan_device_status_async(gemm_plan_t plan, int *host_status, void *stream);
+
+/* How often this plan's calls found their TMA tensor maps already encoded:
+ * the plan keeps the 16 most recently used maps (keyed by address, extents,
+ * row stride, box, element type and swizzle) and reuses one when a call
+ * asks for the same map again, instead of encoding it anew.  Either output
+ * may be NULL. */
+gemm_status_t gemm_plan_tensor_map_stats(gemm_plan_t plan, uint64_t *hits, uint64_t *misses);
 
 /* Where the last recorded device error happened (a role/wait code), 0 if none. */
 int gemm_plan_device_error_site(gemm_plan_t plan);
@@ -346,28 +366,40 @@ gemm_status_t gemm_describe_model(int sm_count, gemm_dtype_t in_dtype, int64_t M
  * or GEMM_BF16) and `splits` (1..16): the number of K ranges each output
  * tile is split into, with the kernel configuration gemm_run would pick.
  * Split partials take tiles x splits x (128 x tile-width x 4 bytes) per CTA
- * of a tile; when that exceeds the array's 4,177,664 bytes for partials, or
- * the tiles exceed its 4096 split counters, the call returns
- * GEMM_ERR_UNSUPPORTED and launches nothing (example: M = 16, N = K = 8192
- * uses 64 tiles of 128 x 16, i.e. 1 MiB at splits = 2; 1024^3 with splits
- * = 2 needs 8 MiB and is rejected).  splits > 1 with fp16 accumulation, or
- * more splits than 64-deep K blocks, also returns GEMM_ERR_UNSUPPORTED.
+ * of a tile; when that exceeds the array's 4,193,024 bytes for partials the
+ * call returns GEMM_ERR_UNSUPPORTED and launches nothing (example: M = 16,
+ * N = K = 8192 uses 64 tiles of 128 x 16, i.e. 1 MiB at splits = 2; 1024^3
+ * with splits = 2 needs 8 MiB and is rejected).  splits > 1 with fp16
+ * accumulation, or more splits than 64-deep K blocks, also returns
+ * GEMM_ERR_UNSUPPORTED.
  *
  * The first call on a device sets that device up (it finds the array's
- * device address and prepares the kernels); make that first call before
- * any stream capture.  Every call on a device shares the array, which
- * keeps the previous call's contents: each call first clears the status
- * word and the split counters on `stream`.  Calls whose kernels overlap on
- * the GPU (other streams, other threads) race on the array and must be
- * serialised by the caller.  A device-side timeout is recorded in the
- * array's status word, which this entry point does not report; results of
- * a call are valid once `stream` has been synchronised. */
+ * device address, zeroes the array's status word and counters and prepares
+ * the kernels; it synchronises the device once); make that first call before
+ * any stream capture.  Every call on a device shares the array, which keeps
+ * the previous call's contents: a call with splits > 1 first clears, on
+ * `stream`, the split counters it uses.  Calls whose kernels overlap on the
+ * GPU (other streams) race on the array and must be serialised by the
+ * caller; calls from several host threads are serialised by the library.
+ * A device-side timeout is recorded in the array's status word, which keeps
+ * the first error until gemm_static_scratch_device_status clears it; results
+ * of a call are valid once `stream` has been synchronised. */
 gemm_status_t gemm_run_static_scratch(int device, gemm_dtype_t in_dtype, const void *A, const void *B,
                                       const void *C, void *D, int64_t M, int64_t N, int64_t K,
                                       int64_t lda, int64_t ldb, int64_t ldc, gemm_layout_t layoutA,
                                       gemm_layout_t layoutB, gemm_dtype_t accum_dtype,
                                       gemm_dtype_t out_dtype, float alpha, float beta, int splits,
                                       void *stream);
+
+/* The status word of gemm_run_static_scratch on `device` (like that entry
+ * point, this has no counterpart on the pages): GEMM_OK, or the
+ * first device-side error (GEMM_ERR_TIMEOUT) of its calls since the device
+ * was set up or the word last cleared.  The word is copied on `stream` (a
+ * cudaStream_t; NULL = the legacy default stream) and the call waits for
+ * `stream`; `clear` != 0 then resets the word and the split counters.
+ * Allocates nothing.  GEMM_OK if the entry point has not run on `device`;
+ * GEMM_ERR_INVALID_ARG for a bad ordinal, GEMM_ERR_CUDA if the copy fails. */
+gemm_status_t gemm_static_scratch_device_status(int device, int clear, void *stream);
 
 /* Tensor-core rate probe (no memory traffic): the median number of SM
  * cycles one tcgen05.mma with M = 256 (a CTA pair), N = `n` columns

@@ -34,6 +34,7 @@ __all__ = [
     "gemm_plan_force_config", "CONFIG", "gemm_run_static_scratch", "gemm_plan_autotune",
     "gemm_plan_clear_tuning", "gemm_plan_tuned_count", "gemm_plan_force_division", "DIVISION",
     "gemm_run_prior_art", "PRIOR_ART", "gemm_mma_fragment_map", "run_prior_art", "gemm_describe_model",
+    "gemm_plan_device_status_async", "gemm_plan_tensor_map_stats", "gemm_static_scratch_device_status",
 ]
 
 STATUS = {
@@ -79,6 +80,12 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.gemm_plan_device_status.restype = i32
     lib.gemm_plan_device_error_site.argtypes = [p]
     lib.gemm_plan_device_error_site.restype = i32
+    lib.gemm_plan_device_status_async.argtypes = [p, p, p]
+    lib.gemm_plan_device_status_async.restype = i32
+    lib.gemm_plan_tensor_map_stats.argtypes = [p, ctypes.POINTER(ctypes.c_uint64), ctypes.POINTER(ctypes.c_uint64)]
+    lib.gemm_plan_tensor_map_stats.restype = i32
+    lib.gemm_static_scratch_device_status.argtypes = [i32, i32, p]
+    lib.gemm_static_scratch_device_status.restype = i32
     lib.gemm_plan_set_timeout_ns.argtypes = [p, u64]
     lib.gemm_plan_set_timeout_ns.restype = i32
     lib.gemm_plan_force_config.argtypes = [p, i32, i32]
@@ -188,6 +195,26 @@ def gemm_plan_device_status(plan, clear: bool = False) -> int:
 
 def gemm_plan_device_error_site(plan) -> int:
     return load().gemm_plan_device_error_site(plan)
+
+
+def gemm_plan_device_status_async(plan, host_status_ptr: int, stream=None) -> int:
+    """Enqueue a copy of the status word (2 ints) to host memory at
+    host_status_ptr on `stream`."""
+    return load().gemm_plan_device_status_async(plan, host_status_ptr, stream)
+
+
+def gemm_plan_tensor_map_stats(plan) -> tuple[int, int]:
+    """(hits, misses) of the plan's cache of encoded tensor maps."""
+    hits, misses = ctypes.c_uint64(), ctypes.c_uint64()
+    st = load().gemm_plan_tensor_map_stats(plan, ctypes.byref(hits), ctypes.byref(misses))
+    if st != 0:
+        raise GemmError(st, "gemm_plan_tensor_map_stats")
+    return hits.value, misses.value
+
+
+def gemm_static_scratch_device_status(device: int, clear: bool = False, stream=None) -> int:
+    """Status word of gemm_run_static_scratch on `device` (waits for `stream`)."""
+    return load().gemm_static_scratch_device_status(device, 1 if clear else 0, stream)
 
 
 def gemm_plan_set_timeout_ns(plan, ns: int) -> int:
@@ -413,6 +440,9 @@ class Plan:
 
     def device_status(self, clear: bool = False) -> int:
         return gemm_plan_device_status(self.handle, clear)
+
+    def tensor_map_stats(self) -> tuple[int, int]:
+        return gemm_plan_tensor_map_stats(self.handle)
 
     def set_timeout_ns(self, ns: int):
         st = gemm_plan_set_timeout_ns(self.handle, ns)

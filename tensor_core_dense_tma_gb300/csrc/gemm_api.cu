@@ -487,7 +487,8 @@ gemm_status_t gemm_plan_create(gemm_plan_t* out, int device, gemm_dtype_t in_dty
         return GEMM_ERR_CUDA;
     }
     plan->encode = reinterpret_cast<EncodeTiledFn>(fn);
-    bool ok = cudaMalloc(&plan->d_status, 2 * sizeof(int)) == cudaSuccess &&
+    bool ok = cudaStreamCreateWithFlags(&plan->status_stream, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaMalloc(&plan->d_status, 2 * sizeof(int)) == cudaSuccess &&
               cudaMemset(plan->d_status, 0, 2 * sizeof(int)) == cudaSuccess &&
               cudaMalloc(&plan->d_ws, kWorkspaceBytes) == cudaSuccess &&
               (plan->ws_bytes = kWorkspaceBytes) > 0 &&
@@ -503,6 +504,7 @@ gemm_status_t gemm_plan_create(gemm_plan_t* out, int device, gemm_dtype_t in_dty
         if (plan->d_ws) cudaFree(plan->d_ws);
         if (plan->d_counters) cudaFree(plan->d_counters);
         if (plan->d_flags) cudaFree(plan->d_flags);
+        if (plan->status_stream) cudaStreamDestroy(plan->status_stream);
         delete plan;
         return GEMM_ERR_CUDA;
     }
@@ -738,26 +740,60 @@ gemm_status_t gemm_plan_tuning_import(gemm_plan_t plan, const char* text) {
     return GEMM_OK;
 }
 
+}  // extern "C"
+
+namespace {
+// The status word of a plan, read by a copy on the plan's own non-blocking
+// stream (it waits for that copy only: no other stream, no device-wide
+// synchronisation); with `clear`, the word and the split counters (which an
+// aborted launch can leave behind) are reset after the read, on that stream.
+gemm_status_t read_plan_status(gemm_plan* plan, int (&h)[2], int clear) {
+    DeviceGuard guard(plan->device);
+    if (!guard.ok) return GEMM_ERR_CUDA;
+    cudaStream_t s = plan->status_stream;
+    bool ok = cudaMemcpyAsync(h, plan->d_status, 2 * sizeof(int), cudaMemcpyDeviceToHost, s) == cudaSuccess;
+    if (ok && clear)
+        ok = cudaMemsetAsync(plan->d_status, 0, 2 * sizeof(int), s) == cudaSuccess &&
+             cudaMemsetAsync(plan->d_counters, 0, kNumCounters * sizeof(int), s) == cudaSuccess;
+    ok = ok && cudaStreamSynchronize(s) == cudaSuccess;
+    if (!ok) cudaGetLastError();
+    return ok ? GEMM_OK : GEMM_ERR_CUDA;
+}
+}  // namespace
+
+extern "C" {
+
 gemm_status_t gemm_plan_device_status(gemm_plan_t plan, int clear) {
     if (!plan) return GEMM_ERR_INVALID_ARG;
-    DeviceGuard guard(plan->device);
     int h[2] = {0, 0};
-    if (cudaMemcpy(h, plan->d_status, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return GEMM_ERR_CUDA;
-    if (clear) {
-        // an aborted launch can leave split-K counters behind: clear them too
-        if (cudaMemset(plan->d_status, 0, sizeof(h)) != cudaSuccess ||
-            cudaMemset(plan->d_counters, 0, kNumCounters * sizeof(int)) != cudaSuccess)
-            return GEMM_ERR_CUDA;
-    }
+    if (read_plan_status(plan, h, clear) != GEMM_OK) return GEMM_ERR_CUDA;
     return static_cast<gemm_status_t>(h[0]);
+}
+
+gemm_status_t gemm_plan_device_status_async(gemm_plan_t plan, int* host_status, void* stream) {
+    if (!plan || !host_status) return GEMM_ERR_INVALID_ARG;
+    DeviceGuard guard(plan->device);
+    if (!guard.ok) return GEMM_ERR_CUDA;
+    if (cudaMemcpyAsync(host_status, plan->d_status, 2 * sizeof(int), cudaMemcpyDeviceToHost,
+                        static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
+    return GEMM_OK;
 }
 
 int gemm_plan_device_error_site(gemm_plan_t plan) {
     if (!plan) return -1;
-    DeviceGuard guard(plan->device);
     int h[2] = {0, 0};
-    if (cudaMemcpy(h, plan->d_status, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return -1;
+    if (read_plan_status(plan, h, 0) != GEMM_OK) return -1;
     return h[1];
+}
+
+gemm_status_t gemm_plan_tensor_map_stats(gemm_plan_t plan, uint64_t* hits, uint64_t* misses) {
+    if (!plan) return GEMM_ERR_INVALID_ARG;
+    if (hits) *hits = plan->tmap_hits;
+    if (misses) *misses = plan->tmap_misses;
+    return GEMM_OK;
 }
 
 gemm_status_t gemm_plan_set_timeout_ns(gemm_plan_t plan, uint64_t ns) {
@@ -870,6 +906,7 @@ gemm_status_t gemm_plan_destroy(gemm_plan_t plan) {
         if (plan->d_ws) cudaFree(plan->d_ws);
         if (plan->d_counters) cudaFree(plan->d_counters);
         if (plan->d_flags) cudaFree(plan->d_flags);
+        if (plan->status_stream) cudaStreamDestroy(plan->status_stream);
         destroy_host_pipeline(plan->host_pipe);
     }
     delete plan->tuned;
@@ -903,10 +940,15 @@ namespace {
 constexpr size_t kStaticScratchBytes = size_t(4) << 20;          // 4 MiB in all
 constexpr size_t kStaticStatusOffset = 0;                         // 2 ints
 constexpr size_t kStaticCountersOffset = 256;                     // kStaticCounters ints
-constexpr int kStaticCounters = 4096;
+constexpr int kStaticCounters = 256;
 constexpr size_t kStaticPartialsOffset = kStaticCountersOffset + kStaticCounters * sizeof(int);
 constexpr size_t kStaticPartialsBytes = kStaticScratchBytes - kStaticPartialsOffset;
 static_assert(kStaticPartialsOffset % 256 == 0, "partials start on a 256-byte boundary");
+// A split tile uses one counter per CTA and at least 2 splits x 128 x 16 fp32
+// partials per counter (the narrowest tiles, 128 x 16); whatever fits the
+// partials therefore fits the counters.
+static_assert(static_cast<size_t>(kStaticCounters) * 2 * 128 * 16 * 4 >= kStaticPartialsBytes,
+              "the partials limit implies the counter limit");
 
 static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
 
@@ -949,6 +991,12 @@ gemm_status_t static_setup(int device, StaticDeviceState& st) {
         q != cudaDriverEntryPointSuccess || !fn)
         return GEMM_ERR_CUDA;
     st.scratch = static_cast<unsigned char*>(ptr);
+    // the status word and the split counters start at zero (the array's
+    // initial contents are not relied on)
+    if (cudaMemset(st.scratch, 0, kStaticPartialsOffset) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
     for (int t = 0; t < 2; ++t) {
         gemm_plan& pl = st.plan[t];
         pl.device = device;
@@ -984,12 +1032,12 @@ extern "C" gemm_status_t gemm_run_static_scratch(int device, gemm_dtype_t in_dty
     DeviceGuard guard(device);
     if (!guard.ok) return GEMM_ERR_CUDA;
     StaticDeviceState& ds = g_static_state[device];
-    {
-        std::lock_guard<std::mutex> lock(g_static_mutex);
-        if (!ds.ready) {
-            st = static_setup(device, ds);
-            if (st != GEMM_OK) return st;
-        }
+    // one call at a time on the host: the device's plans (their lazily set
+    // kernel attributes, launch count and tensor-map cache) are shared
+    std::lock_guard<std::mutex> lock(g_static_mutex);
+    if (!ds.ready) {
+        st = static_setup(device, ds);
+        if (st != GEMM_OK) return st;
     }
     gemm_plan* plan = &ds.plan[in_dtype == GEMM_F16 ? 0 : 1];
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -1004,19 +1052,21 @@ extern "C" gemm_status_t gemm_run_static_scratch(int device, gemm_dtype_t in_dty
     ch.splits = splits;
     ch.n_halves = false;
     ch.dp_tiles = 0;   // every tile is split `splits` ways
-    // the size limit: split partials and counters must fit the fixed array
     if (splits > 1) {
+        // the size limit: split partials must fit the fixed array (the
+        // counters then fit too, see kStaticCounters)
         const int64_t ctas = kCfgCtas[ch.kind];
         const int64_t partial_bytes = ch.tiles * splits * ctas * 128 * kCfgTileN[ch.kind] * 4;
         if (ch.tiles * ctas > kStaticCounters || partial_bytes > static_cast<int64_t>(kStaticPartialsBytes))
             return GEMM_ERR_UNSUPPORTED;
-    }
-    // the array keeps the previous call's contents: start from a clear
-    // status word and zero split counters (stream-ordered, no allocation)
-    if (cudaMemsetAsync(plan->d_status, 0, 2 * sizeof(int), s) != cudaSuccess ||
-        cudaMemsetAsync(plan->d_counters, 0, kStaticCounters * sizeof(int), s) != cudaSuccess) {
-        cudaGetLastError();
-        return GEMM_ERR_CUDA;
+        // the array keeps the previous call's contents: the counters this call
+        // uses start from zero (a completed launch leaves them zero, an aborted
+        // one may not); stream-ordered, no allocation
+        if (cudaMemsetAsync(plan->d_counters, 0, static_cast<size_t>(ch.tiles * ctas) * sizeof(int), s) !=
+            cudaSuccess) {
+            cudaGetLastError();
+            return GEMM_ERR_CUDA;
+        }
     }
     const Problem pr = make_problem(ch.swap, A, B, M, N, K, lda, ldb, layoutA, layoutB);
     const int slot = out_slot(accum_dtype, out_dtype);
@@ -1028,3 +1078,47 @@ extern "C" gemm_status_t gemm_run_static_scratch(int device, gemm_dtype_t in_dty
         default: return launch_pair256(plan, slot, ch, pr, C, D, ldc, alpha, beta, s);
     }
 }
+
+extern "C" gemm_status_t gemm_static_scratch_device_status(int device, int clear, void* stream) {
+    if (device < 0 || device >= kMaxStaticDevices) return GEMM_ERR_INVALID_ARG;
+    StaticDeviceState& ds = g_static_state[device];
+    std::lock_guard<std::mutex> lock(g_static_mutex);
+    if (!ds.ready) return GEMM_OK;   // nothing has run on this device
+    DeviceGuard guard(device);
+    if (!guard.ok) return GEMM_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int h[2] = {0, 0};
+    bool ok = cudaMemcpyAsync(h, ds.scratch + kStaticStatusOffset, sizeof(h), cudaMemcpyDeviceToHost, s) ==
+              cudaSuccess;
+    if (ok && clear)
+        ok = cudaMemsetAsync(ds.scratch + kStaticStatusOffset, 0, kStaticPartialsOffset - kStaticStatusOffset, s) ==
+             cudaSuccess;
+    ok = ok && cudaStreamSynchronize(s) == cudaSuccess;
+    if (!ok) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
+    return static_cast<gemm_status_t>(h[0]);
+}
+
+#ifdef TCDT_FAULT_INJECTION
+// Test builds only (not part of the product library or of include/gemm.h):
+// the pipeline-wait limit and the skipped TMA issue of the entry point's
+// plans on `device` (set up first if needed).
+extern "C" gemm_status_t gemm_test_static_configure(int device, uint64_t timeout_ns, int64_t skip_load) {
+    if (device < 0 || device >= kMaxStaticDevices || timeout_ns == 0) return GEMM_ERR_INVALID_ARG;
+    DeviceGuard guard(device);
+    if (!guard.ok) return GEMM_ERR_CUDA;
+    StaticDeviceState& ds = g_static_state[device];
+    std::lock_guard<std::mutex> lock(g_static_mutex);
+    if (!ds.ready) {
+        const gemm_status_t st = static_setup(device, ds);
+        if (st != GEMM_OK) return st;
+    }
+    for (gemm_plan& pl : ds.plan) {
+        pl.timeout_ns = timeout_ns;
+        pl.fi_skip_load = skip_load;
+    }
+    return GEMM_OK;
+}
+#endif

@@ -86,6 +86,28 @@ inline int out_slot(gemm_dtype_t acc, gemm_dtype_t out) {
 }  // namespace tcdt_host
 
 namespace tcdt_host {
+// A plan's cache of encoded tensor maps.  A map encodes an address, the
+// matrix extents and row stride, the box, the element type and the swizzle;
+// a request equal in all of these reuses the encoded map instead of calling
+// cuTensorMapEncodeTiled again (a map holds no other state, so a cached map
+// stays right for any later allocation at the same address and geometry).
+// The least recently used of kTmapCacheSize entries is replaced on a miss.
+constexpr int kTmapCacheSize = 16;
+struct TmapKey {
+    const void* ptr;
+    uint64_t inner, outer, ld;
+    uint32_t box_inner, box_outer;
+    int dtype, swizzle;
+    bool operator==(const TmapKey& o) const {
+        return ptr == o.ptr && inner == o.inner && outer == o.outer && ld == o.ld && box_inner == o.box_inner &&
+               box_outer == o.box_outer && dtype == o.dtype && swizzle == o.swizzle;
+    }
+};
+struct TmapEntry {
+    TmapKey key;
+    CUtensorMap map;
+    uint64_t last_use = 0;   // 0: empty
+};
 struct TunedTable;     // gemm_plan_autotune's results, keyed by problem shape (gemm_api.cu)
 struct HostPipeline;   // gemm_run_host's streams, events and staging buffers (gemm_host.cu)
 void destroy_host_pipeline(HostPipeline* hp);
@@ -96,6 +118,7 @@ struct gemm_plan {
     int sm_count = 0;
     gemm_dtype_t in_dtype = GEMM_F16;
     int* d_status = nullptr;      // [0] status, [1] site
+    cudaStream_t status_stream = nullptr;   // owned, non-blocking: reads of the status word
     float* d_ws = nullptr;        // split-K partials
     int* d_counters = nullptr;    // split-K arrival counters (kept zero between launches)
     unsigned* d_flags = nullptr;  // early-partial ready flags, kNumCounters (null: none)
@@ -115,6 +138,8 @@ struct gemm_plan {
     int forced_division_splits = 0;
     tcdt_host::TunedTable* tuned = nullptr;   // owned; null until the first gemm_plan_autotune
     tcdt_host::HostPipeline* host_pipe = nullptr;   // owned; null until the first gemm_run_host
+    tcdt_host::TmapEntry tmap_cache[tcdt_host::kTmapCacheSize];   // encoded tensor maps (encode_map)
+    uint64_t tmap_clock = 0, tmap_hits = 0, tmap_misses = 0;
 };
 
 namespace tcdt_host {
@@ -181,9 +206,23 @@ TCDT_DECLARE_KIND_IN(pair256, tf32)
 
 // 2-D tensor map over a matrix whose contiguous dimension has `inner`
 // elements (rows of `ld` elements), 128-byte swizzle, zero fill outside.
-inline gemm_status_t encode_map(const gemm_plan* plan, CUtensorMap* map, const void* ptr, uint64_t inner,
+// Served from the plan's cache of encoded maps when the same request was
+// encoded before.
+inline gemm_status_t encode_map(gemm_plan* plan, CUtensorMap* map, const void* ptr, uint64_t inner,
                                 uint64_t outer, uint64_t ld, uint32_t box_inner, uint32_t box_outer,
                                 gemm_dtype_t dtype, CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
+    const TmapKey key{ptr, inner, outer, ld, box_inner, box_outer, static_cast<int>(dtype), static_cast<int>(swizzle)};
+    TmapEntry* victim = &plan->tmap_cache[0];
+    for (TmapEntry& e : plan->tmap_cache) {
+        if (e.last_use != 0 && e.key == key) {
+            e.last_use = ++plan->tmap_clock;
+            ++plan->tmap_hits;
+            std::memcpy(map, &e.map, sizeof(CUtensorMap));
+            return GEMM_OK;
+        }
+        if (e.last_use < victim->last_use) victim = &e;
+    }
+    ++plan->tmap_misses;
     const uint64_t esz = static_cast<uint64_t>(dtype_bytes(dtype));
     const cuuint64_t dims[2] = {inner, outer};
     const cuuint64_t strides[1] = {ld * esz};
@@ -197,7 +236,11 @@ inline gemm_status_t encode_map(const gemm_plan* plan, CUtensorMap* map, const v
     CUresult r = plan->encode(map, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr,
                               CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_CUDA;
+    if (r != CUDA_SUCCESS) return GEMM_ERR_CUDA;
+    victim->key = key;
+    std::memcpy(&victim->map, map, sizeof(CUtensorMap));
+    victim->last_use = ++plan->tmap_clock;
+    return GEMM_OK;
 }
 
 // tcgen05 instruction descriptor (kind::f16, kind::tf32, kind::f8f6f4):

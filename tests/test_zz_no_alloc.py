@@ -4,11 +4,14 @@ Some callers cannot obtain device memory of their own -- code hosted by a
 framework that owns the whole device memory and gives kernels only their
 inputs and outputs, or code that must keep cudaMalloc's device-wide
 synchronisation off its path.  This entry point takes no plan; its split-K
-scratch is a fixed array inside the library.  The test calls it through the
-C ABI and compares it, element by element, with gemm_run on the same
-inputs (same configuration and split count), on two calls in a row with
-different data: the array keeps the previous call's contents, so the
-second call shows that nothing stale leaks into it.
+scratch is a fixed array inside the library.  The tests call it through the
+C ABI, on two calls in a row with different data (the array keeps the
+previous call's contents, so the second call shows that nothing stale leaks
+into it), and compare each result element by element with gemm_run on the
+same inputs (same configuration and split count) and with the CPU oracle:
+random data within the fp32-accumulate tolerance, and integer twins
+(entries in {-2..2}, every partial sum exact) bit for bit.  The array's
+status word is read with gemm_static_scratch_device_status.
 
 This file is named so that pytest collects it last.
 """
@@ -63,6 +66,28 @@ CASES = [
 ]
 
 
+def _oracle_check(w, h, D, integer):
+    """D against the oracle: bit for bit on an integer twin, within the
+    parity tolerance otherwise."""
+    import oracle
+    A, B = wl.bits(h.A), wl.bits(h.B)
+    C = None if h.C is None else wl.bits(h.C)
+    ref, V, S = oracle.gemm(w.in_dtype, A, B, C, w.M, w.N, w.K, h.lda, h.ldb, h.ldc, w.layoutA, w.layoutB,
+                            w.out_dtype, w.alpha, w.beta, nthreads=16, want_exact=True)
+    got = D.cpu()
+    if integer:
+        gb = got.view(torch.int32 if w.out_dtype == "f32" else torch.int16).numpy()
+        rb = ref.view(np.int32 if w.out_dtype == "f32" else np.int16)
+        assert np.array_equal(gb, rb), f"{int(np.count_nonzero(gb != rb))} elements differ from the oracle"
+        return
+    g = got.float().double().numpy()
+    tol = 2e-3 * S + 1e-6
+    if w.out_dtype != "f32":
+        tol = tol + 0.5 * oracle.ulp(V, w.out_dtype)
+    bad = np.argwhere(~(np.abs(g - V) <= tol))
+    assert bad.size == 0, f"{len(bad)} elements outside the tolerance, first at {tuple(bad[0])}"
+
+
 @pytest.mark.parametrize("w,splits", CASES, ids=[c[0].name for c in CASES])
 def test_matches_gemm_run_twice(tc, w, splits):
     plan = tc.Plan(w.in_dtype, 0)
@@ -92,7 +117,9 @@ def test_matches_gemm_run_twice(tc, w, splits):
             if h.C is not None:
                 S = S + abs(w.beta) * h.C.double().abs().numpy()
             _compare(w, D_static, D_plan, S)
+            _oracle_check(w, h, D_static, integer=False)
         assert plan.device_status() == 0
+        assert tc.gemm_static_scratch_device_status(0, False, torch.cuda.current_stream().cuda_stream) == 0
     finally:
         plan.close()
 
@@ -106,3 +133,45 @@ def test_too_large_is_rejected(tc):
     st = tc.gemm_run_static_scratch(0, "bf16", A.data_ptr(), B.data_ptr(), None, D.data_ptr(), M, N, K, K, N, N,
                                     "row", "row", "f32", "bf16", 1.0, 0.0, 2, None)
     assert st == 2, tc.gemm_status_string(st)
+
+
+TWINS = [
+    # skinny (transposed 128 x 16 tiles), one, two and three K splits
+    (wl.Workload("noalloc_skinny_twin", 24, 16, 4096, 4096, "bf16", "row", "row", "f32", "bf16", 1.0, 0.0, "u1"), 1),
+    (wl.Workload("noalloc_skinny_twin2", 24, 16, 4096, 4096, "bf16", "row", "row", "f32", "bf16", 1.0, 0.0, "u1"), 2),
+    (wl.Workload("noalloc_skinny_twin3", 24, 16, 4096, 4096, "bf16", "row", "row", "f32", "bf16", 1.0, 0.0, "u1"), 3),
+    # ragged with alpha 0.5, beta 1 and an integer C, two and three K splits
+    (wl.Workload("noalloc_ragged_twin2", 25, 300, 264, 2000, "f16", "row", "col", "f32", "f32", 0.5, 1.0, "n01"), 2),
+    (wl.Workload("noalloc_ragged_twin3", 25, 300, 264, 2000, "f16", "row", "col", "f32", "f32", 0.5, 1.0, "n01"), 3),
+    # the full ragged shape, whole tiles (its split partials would not fit the array)
+    (wl.WORKLOADS["ragged"], 1),
+]
+
+
+@pytest.mark.parametrize("w,splits", TWINS, ids=[f"{c[0].name}-s{c[1]}" for c in TWINS])
+def test_integer_twins_bit_exact(tc, w, splits):
+    """Integer twins, two calls in a row: each result equals the oracle bit
+    for bit (the split partials are summed in split order, so the rounding
+    to the output type sees the exact sum)."""
+    for call in range(2):
+        h = wl.make_inputs(w, integer=True, seed_offset=100 * call)
+        A, B = h.A.cuda(), h.B.cuda()
+        C = None if h.C is None else h.C.cuda()
+        D = torch.full((w.M, w.N), float("nan"), dtype=wl.DTYPES[w.out_dtype], device="cuda")
+        _run_static(tc, w, A, B, C, D, splits)
+        torch.cuda.synchronize()
+        _oracle_check(w, h, D, integer=True)
+    assert tc.gemm_static_scratch_device_status(0, False, torch.cuda.current_stream().cuda_stream) == 0
+
+
+def test_bad_arguments_are_rejected(tc):
+    """Sizes and arguments outside the entry point's limits: an error, no launch."""
+    A = torch.zeros((16, 64), dtype=torch.bfloat16, device="cuda")
+    B = torch.zeros((64, 256), dtype=torch.bfloat16, device="cuda")
+    D = torch.zeros((16, 256), dtype=torch.bfloat16, device="cuda")
+    args = (A.data_ptr(), B.data_ptr(), None, D.data_ptr(), 16, 256, 64, 64, 256, 256, "row", "row", "f32", "bf16",
+            1.0, 0.0)
+    assert tc.gemm_run_static_scratch(0, "bf16", *args, 2, None) == 2     # 2 splits of a single 64-deep K block
+    assert tc.gemm_run_static_scratch(0, "bf16", *args, 0, None) == 1     # splits < 1
+    assert tc.gemm_run_static_scratch(0, "bf16", *args, 17, None) == 1    # splits > 16
+    assert tc.gemm_run_static_scratch(-1, "bf16", *args, 1, None) == 1    # bad device ordinal
