@@ -75,7 +75,8 @@ def parse():
     ap.add_argument("--prior-art", choices=["wmma_naive", "wmma_shared", "mma_sync"],
                     help="time one of the pages' own warp-level kernels instead (fp16 row-major A and B; "
                          "comparison only)")
-    ap.add_argument("--division", choices=["auto", "whole", "split", "early_split", "halves", "stream_k"],
+    ap.add_argument("--division", choices=["auto", "whole", "split", "early_split", "halves", "stream_k",
+                                           "pair_split"],
                     default="auto", help="pin how the last wave's tiles are divided (gemm_plan_force_division)")
     ap.add_argument("--autotune", action="store_true",
                     help="time every candidate configuration first (gemm_plan_autotune) and run the fastest")

@@ -232,7 +232,15 @@ gemm_status_t gemm_plan_force_config(gemm_plan_t plan, gemm_config_t config, int
  *   STREAM_K     after at least two whole waves: one wave fewer runs whole,
  *                and the remaining tiles' K blocks, laid end to end, are
  *                cut into one equal range per unit; a tile cut between two
- *                units is joined through an early partial ("Stream-K").
+ *                units is joined through an early partial ("Stream-K");
+ *   PAIR_SPLIT   the transposed product (M <= 64, tiles of 128 x 16 or
+ *                128 x 64), when its tiles fit one wave of CTA pairs: each
+ *                tile runs on a cluster of two CTAs, each taking half the K
+ *                blocks; the second CTA writes its fp32 partial into the
+ *                first's shared memory, which adds it to its own accumulator
+ *                (split 0 + split 1, the order SPLIT adds them in) and
+ *                stores the tile.  fp32 accumulation, K of two 64-deep
+ *                blocks or more.
  * `splits` (0: any) pins the split count of SPLIT and EARLY_SPLIT.  A call
  * whose problem admits no candidate of the pinned division (EARLY_SPLIT
  * with less than one whole wave or fp16 accumulation, HALVES on a
@@ -244,7 +252,8 @@ typedef enum {
     GEMM_DIVISION_SPLIT = 2,
     GEMM_DIVISION_EARLY_SPLIT = 3,
     GEMM_DIVISION_HALVES = 4,
-    GEMM_DIVISION_STREAM_K = 5
+    GEMM_DIVISION_STREAM_K = 5,
+    GEMM_DIVISION_PAIR_SPLIT = 6
 } gemm_division_t;
 
 gemm_status_t gemm_plan_force_division(gemm_plan_t plan, gemm_division_t division, int splits);

@@ -273,7 +273,8 @@ def gemm_mma_fragment_map(device: int = 0):
     return out
 
 
-DIVISION = {"auto": 0, "whole": 1, "split": 2, "early_split": 3, "halves": 4, "stream_k": 5}
+DIVISION = {"auto": 0, "whole": 1, "split": 2, "early_split": 3, "halves": 4, "stream_k": 5,
+            "pair_split": 6}
 
 
 def gemm_plan_force_division(plan, division: str | int = "auto", splits: int = 0) -> int:

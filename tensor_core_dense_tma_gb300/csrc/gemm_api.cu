@@ -209,9 +209,10 @@ Choice choose(const gemm_plan* plan, int64_t M, int64_t N, int64_t K, gemm_dtype
     double best_cost = -1.0;
     bool any = false;
     auto consider = [&](double cost, int kind, int splits, int64_t dp, bool halves, int64_t tiles, int64_t units,
-                        bool early = false, bool stream_k = false) {
+                        bool early = false, bool stream_k = false, bool pair = false) {
         // a pinned division (gemm_plan_force_division) admits only its own kind of candidate
-        const int division = halves     ? GEMM_DIVISION_HALVES
+        const int division = pair       ? GEMM_DIVISION_PAIR_SPLIT
+                             : halves   ? GEMM_DIVISION_HALVES
                              : stream_k ? GEMM_DIVISION_STREAM_K
                              : splits > 1 ? (early ? GEMM_DIVISION_EARLY_SPLIT : GEMM_DIVISION_SPLIT)
                                           : GEMM_DIVISION_WHOLE;
@@ -227,6 +228,7 @@ Choice choose(const gemm_plan* plan, int64_t M, int64_t N, int64_t K, gemm_dtype
         c.n_halves = halves;
         c.early = early;
         c.stream_k = stream_k;
+        c.pair_split = pair;
         c.swap = swap;
         c.tiles = tiles;
         c.units = static_cast<int>(units);
@@ -275,6 +277,15 @@ Choice choose(const gemm_plan* plan, int64_t M, int64_t N, int64_t K, gemm_dtype
                                     static_cast<double>((split_tiles * s + units - 1) / units) * item;
                 consider(cost, kind, static_cast<int>(s), dp_split, false, tiles, units);
             }
+        }
+        // transposed tiles on CTA pairs: each CTA of a pair takes half the K
+        // blocks and the second hands its partial to the first through shared
+        // memory (no workspace round trip, no arrival counter); offered when the
+        // tiles fit one wave of pairs
+        if (swap && kCfgCtas[kind] == 1 && kCfgTileN[kind] <= 64 && acc != GEMM_F16 && kb >= 2 && !pinned &&
+            tiles <= units / 2) {
+            const double item = static_cast<double>((kb + 1) / 2) * full_step + fc.item + 1.0;
+            consider(item, kind, 2, 0, false, tiles, units / 2, false, false, true);
         }
         // the partial wave's tiles split along K with early partials: at most
         // one split per unit, the early splits first and the owners last, after
@@ -361,7 +372,8 @@ std::string config_name(const Choice& ch, gemm_dtype_t acc, gemm_dtype_t out) {
     std::string s = "tc" + std::to_string(kCfgCtas[ch.kind]) + "cta_" + std::to_string(kCfgTileM[ch.kind]) + "x" +
                     std::to_string(kCfgTileN[ch.kind]) + "_" + outs[out_slot(acc, out)];
     if (ch.swap) s += "_swapAB";
-    if (ch.stream_k) s += "_streamk";
+    if (ch.pair_split) s += "_pairsplitk2";
+    else if (ch.stream_k) s += "_streamk";
     else if (ch.splits > 1) s += (ch.early ? "_esplitk" : "_splitk") + std::to_string(ch.splits);
     if (ch.n_halves) s += "_nhalves";
     return s;
@@ -626,6 +638,7 @@ gemm_status_t gemm_plan_autotune(gemm_plan_t plan, const void* A, const void* B,
         const Choice& ch = cands[c].choice;
         const bool is_model = ch.kind == model.kind && ch.splits == model.splits && ch.n_halves == model.n_halves &&
                               ch.early == model.early && ch.stream_k == model.stream_k &&
+                              ch.pair_split == model.pair_split &&
                               ch.dp_tiles == model.dp_tiles;
         char line[160];
         std::snprintf(line, sizeof(line), "%s%s model_cost=%.1f us=%.2f%s\n", c == best ? "* " : "  ",
@@ -814,7 +827,7 @@ gemm_status_t gemm_plan_force_config(gemm_plan_t plan, gemm_config_t config, int
 
 gemm_status_t gemm_plan_force_division(gemm_plan_t plan, gemm_division_t division, int splits) {
     if (!plan) return GEMM_ERR_INVALID_ARG;
-    if (static_cast<int>(division) < GEMM_DIVISION_AUTO || static_cast<int>(division) > GEMM_DIVISION_STREAM_K)
+    if (static_cast<int>(division) < GEMM_DIVISION_AUTO || static_cast<int>(division) > GEMM_DIVISION_PAIR_SPLIT)
         return GEMM_ERR_INVALID_ARG;
     if (splits < 0 || splits > kMaxSplits) return GEMM_ERR_INVALID_ARG;
     plan->forced_division = static_cast<int>(division);
@@ -885,7 +898,8 @@ gemm_status_t describe_impl(const gemm_plan* plan, int64_t M, int64_t N, int64_t
     const int64_t work = ch.n_halves      ? ch.dp_tiles + (ch.tiles - ch.dp_tiles) * 2
                          : ch.splits > 1 ? ch.dp_tiles + (ch.tiles - ch.dp_tiles) * ch.splits
                                          : ch.tiles;
-    const int64_t units = work < ch.units ? work : ch.units;
+    // a pair split launches two CTAs per tile
+    const int64_t units = ch.pair_split ? 2 * ch.tiles : work < ch.units ? work : ch.units;
     std::snprintf(buf, static_cast<size_t>(len),
                   "%s tiles=%lld divided_tiles=%lld splits=%d ctas=%lld sms=%d source=%s",
                   config_name(ch, accum_dtype, out_dtype).c_str(), static_cast<long long>(ch.tiles),
@@ -1051,6 +1065,9 @@ extern "C" gemm_status_t gemm_run_static_scratch(int device, gemm_dtype_t in_dty
     if (splits > kb || (accum_dtype == GEMM_F16 && splits > 1)) return GEMM_ERR_UNSUPPORTED;
     ch.splits = splits;
     ch.n_halves = false;
+    ch.pair_split = false;
+    ch.early = false;
+    ch.stream_k = false;
     ch.dp_tiles = 0;   // every tile is split `splits` ways
     if (splits > 1) {
         // the size limit: split partials must fit the fixed array (the

@@ -165,6 +165,7 @@ struct Choice {
     bool n_halves = false;     // divided tiles run as two half-width items (splits == 1)
     bool early = false;        // divided tiles split with early partials (splits > 1)
     bool stream_k = false;     // the last dp_tiles..tiles shared out as equal K ranges (see unit_item)
+    bool pair_split = false;   // transposed tiles: a CTA pair per tile, K halved (see pair_item)
     bool swap = false;
     int64_t tiles = 0;
     int units = 0;
@@ -336,7 +337,9 @@ gemm_status_t launch_tc(gemm_plan* plan, const Choice& ch, const Problem& pr, co
                         out_esz == 4 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
         if (st != GEMM_OK) return st;
     }
-    if (ch.splits > 1 && Cfg::W == 32) {
+    const bool pair = ch.pair_split && Cfg::CG == 1 && Cfg::BN <= 64;
+    if (ch.pair_split && !pair) return GEMM_ERR_UNSUPPORTED;
+    if (ch.splits > 1 && Cfg::W == 32 && !pair) {
         // the workspace as a [rows][BN] fp32 matrix; a split's partial is 128 rows of it
         const uint64_t ws_rows = plan->ws_bytes / (static_cast<uint64_t>(Cfg::BN) * 4);
         st = encode_map(plan, &tmW, plan->d_ws, Cfg::BN, ws_rows, Cfg::BN, 32, 32, GEMM_F32);
@@ -381,6 +384,11 @@ gemm_status_t launch_tc(gemm_plan* plan, const Choice& ch, const Problem& pr, co
     p.counters = plan->d_counters;
     p.early = (ch.early && ch.splits > 1 && plan->d_flags && Cfg::W == 32) ? 1 : 0;
     p.stream_k = (p.early && ch.stream_k) ? 1 : 0;
+    p.pair_split = pair ? 1 : 0;
+    if (pair) {
+        p.splits = 2;
+        p.dp_tiles = 0;
+    }
     {
         const uint32_t e = static_cast<uint32_t>(plan->launches + 1);
         p.epoch = e == 0u ? 1u : e;
@@ -398,6 +406,16 @@ gemm_status_t launch_tc(gemm_plan* plan, const Choice& ch, const Problem& pr, co
     const int64_t work = p.dp_tiles + static_cast<int64_t>(p.num_tiles - p.dp_tiles) * (n_halves ? 2 : p.splits);
     const int units = work < ch.units ? static_cast<int>(work) : ch.units;
     cfg.gridDim = dim3(Cfg::CG * units, 1, 1);
+    if (pair) {
+        // one cluster of two CTAs per tile (the plan offers this only when the
+        // tiles fit one wave of pairs)
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.numAttrs = 1;
+        cfg.gridDim = dim3(2 * p.num_tiles, 1, 1);
+    }
     if (cudaLaunchKernelEx(&cfg, tcdt::gemm_sm103_kernel<Cfg, EP>, tmA, tmB, tmBh, tmD, tmW, p) != cudaSuccess) {
         cudaGetLastError();
         return GEMM_ERR_CUDA;

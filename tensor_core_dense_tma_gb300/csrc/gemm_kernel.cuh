@@ -99,6 +99,9 @@ struct KernelParams {
     uint32_t epoch;           // this launch's nonzero tag for partial-ready flags
     unsigned* flags;          // [split tile][split][cta] partial-ready flags (earlier launches' tags)
     int* status;              // [0] status code, [1] site
+    int32_t pair_split;       // 1: (one-CTA transposed tiles) a cluster of two CTAs per tile, each
+                              //    taking half the K blocks; the second hands its partial to the
+                              //    first through the first's shared memory (see pair_item)
     uint64_t timeout_ns;
 #ifdef TCDT_FAULT_INJECTION
     int64_t fi_skip_load;     // test builds only: this producer issue (counted per CTA) loads nothing
@@ -190,6 +193,7 @@ enum ItemRole : int {
     kRoleSplit = 1,    // one K range of a split tile; the last split to arrive reduces
     kRoleEarly = 2,    // an early-partial split: writes its fp32 partial and a ready flag
     kRoleOwner = 3,    // the owner split: its accumulator starts as the sum of the partials
+    kRolePair = 4,     // one half of a tile split across a CTA pair (pair_split)
 };
 
 struct WorkItem {
@@ -323,6 +327,24 @@ __device__ __forceinline__ WorkItem unit_item(const KernelParams& p, int unit, i
     if (k >= 0) return work_item(p, unit + k * units);
     WorkItem x = work_item(p, p.dp_tiles + unit);   // split (unit / S, unit % S) of the divided tiles
     x.role = s == 0 ? kRoleOwner : kRoleEarly;
+    return x;
+}
+
+// pair_split: cluster u (a pair of CTAs) computes tile u; CTA `prank` of the
+// pair takes K blocks [prank * kb / 2, (prank + 1) * kb / 2).  There are at
+// most as many tiles as pairs, so a pair has one item (or none).
+__device__ __forceinline__ int pair_items(const KernelParams& p, int unit) { return unit < p.num_tiles ? 1 : 0; }
+
+__device__ __forceinline__ WorkItem pair_item(const KernelParams& p, int unit, int prank) {
+    WorkItem x;
+    x.tile = unit;
+    x.stile = -1;
+    x.split = prank;
+    x.nsplit = 2;
+    x.kb0 = p.num_k_blocks * prank / 2;
+    x.kb1 = p.num_k_blocks * (prank + 1) / 2;
+    x.half = -1;
+    x.role = kRolePair;
     return x;
 }
 
@@ -1040,10 +1062,22 @@ gemm_sm103_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     const int lane = threadIdx.x % 32;
     // position of this CTA in its pair, and of the pair in the grid
     const uint32_t rank = CG == 1 ? 0u : cluster_ctarank();
-    const int unit = CG == 1 ? static_cast<int>(blockIdx.x) : static_cast<int>(cluster_id_x());
-    const int num_units = CG == 1 ? static_cast<int>(gridDim.x) : static_cast<int>(num_clusters_x());
+    // pair_split is built into the one-CTA transposed-tile kernels only
+    constexpr bool kPairOK = CG == 1 && Cfg::BN <= 64;
+    const bool psplit = kPairOK && p.pair_split != 0;
+    const int prank = psplit ? static_cast<int>(cluster_ctarank()) : 0;
+    const int unit = psplit ? static_cast<int>(cluster_id_x())
+                     : CG == 1 ? static_cast<int>(blockIdx.x) : static_cast<int>(cluster_id_x());
+    const int num_units = psplit ? static_cast<int>(num_clusters_x())
+                          : CG == 1 ? static_cast<int>(gridDim.x) : static_cast<int>(num_clusters_x());
     const bool leader = rank == 0;
-    const int num_items = unit_items(p, unit, num_units);
+    const int num_items = psplit ? pair_items(p, unit) : unit_items(p, unit, num_units);
+    auto item_at = [&](int i) -> WorkItem {
+        if constexpr (kPairOK) {
+            if (psplit) return pair_item(p, unit, prank);
+        }
+        return unit_item(p, unit, num_units, i);
+    };
     const bool a_mn = Cfg::MN_OK && p.a_mn_major;   // A is M-contiguous
     const bool b_mn = Cfg::MN_OK && p.b_mn_major;   // B is N-contiguous
 
@@ -1076,8 +1110,12 @@ gemm_sm103_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         tmem_relinquish_alloc_permit<CG>();
     }
     tc_fence_before_sync();
-    if constexpr (CG == 1) __syncthreads();
-    else cluster_sync_all();              // peer barriers initialised before any remote use
+    if constexpr (CG == 1) {
+        if (psplit) cluster_sync_all();   // the peer's barriers initialised before its partial arrives
+        else __syncthreads();
+    } else {
+        cluster_sync_all();               // peer barriers initialised before any remote use
+    }
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
     const WaitCtx wctx{p.status, p.timeout_ns, abort_flag};
@@ -1097,7 +1135,7 @@ gemm_sm103_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             const uint32_t b_tx_half = b_mn ? static_cast<uint32_t>(Cfg::B_CHUNKS_HALF * 64 * 128)
                                             : static_cast<uint32_t>(Cfg::BN_CTA_HALF * 128);
             for (int it = 0; ok && it < num_items; ++it) {
-                const WorkItem x = unit_item(p, unit, num_units, it);
+                const WorkItem x = item_at(it);
                 int mb, nb;
                 tile_coords(p, x.tile, mb, nb);
                 const bool half = Cfg::HALVES_OK && x.half >= 0;
@@ -1205,7 +1243,7 @@ gemm_sm103_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             const uint32_t b_kstep = b_mn ? 16u * 128u : 32u;
             uint32_t init_phase = 0;
             for (int it = 0; ok && it < num_items; ++it) {
-                const WorkItem x = unit_item(p, unit, num_units, it);
+                const WorkItem x = item_at(it);
                 bool got;
                 if constexpr (CG == 1) got = warp_wait_phase(acce_bar(buf), acc_phase ^ 1u, wctx, kSiteMmaAccEmpty);
                 else got = warp_wait_phase<true>(acce_bar(buf), acc_phase ^ 1u, wctx, kSiteMmaAccEmpty);
@@ -1284,7 +1322,7 @@ gemm_sm103_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         uint32_t acc_phase = 0;
         int iter = 0;
         for (; iter < num_items; ++iter) {
-            const WorkItem x = unit_item(p, unit, num_units, iter);
+            const WorkItem x = item_at(iter);
             int mb, nb;
             tile_coords(p, x.tile, mb, nb);
             const int m0 = mb * Cfg::UMMA_M + Cfg::BM * static_cast<int>(rank);
@@ -1407,7 +1445,58 @@ gemm_sm103_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             const int row = m0 + row_local;
             const bool row_ok = row < p.M;
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(32 * quad) << 16) + buf * Cfg::ACC_COLS;
-            if (x.role == kRoleEarly) {
+            if constexpr (kPairOK) {
+                if (x.role == kRolePair) {
+                    // The tile's two K halves meet in the first CTA of the pair: each
+                    // epilogue warp of the second writes its 32 accumulator rows
+                    // (fp32, row lane at lane * BN * 4 bytes) into the same warp's
+                    // staging buffer of the first and arrives on that warp's barrier
+                    // there; the first adds them to its own accumulator -- split 0 +
+                    // split 1, the order of the last-arriver reduction -- and stores.
+                    const uint32_t row_off = static_cast<uint32_t>(lane) * (Cfg::BN * 4u);
+                    if (prank == 1) {
+#pragma unroll 1
+                        for (int c = 0; c < nchunks; ++c) {
+                            __syncwarp();
+                            uint32_t r[W];
+                            tmem_ld_row<W>(t_row + W * c, r);
+                            tmem_ld_wait();
+                            const uint32_t dst = map_to_cta(stg + row_off + static_cast<uint32_t>(W * c) * 4u, 0);
+#pragma unroll
+                            for (int i = 0; i < W; i += 4) st_cluster_v4(dst + 4u * i, r[i], r[i + 1], r[i + 2], r[i + 3]);
+                        }
+                        fence_acq_rel_cluster();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive_cluster(map_to_cta(seed_bar(warp - 2), 0));
+                    } else if (warp_wait_phase<true>(seed_bar(warp - 2), 0, wctx, kSitePartialReady)) {
+#pragma unroll 1
+                        for (int c = 0; c < nchunks; ++c) {
+                            const int col0 = n0 + W * c;
+                            if (col0 >= p.N) break;   // warp-uniform
+                            __syncwarp();
+                            uint32_t r[W];
+                            tmem_ld_row<W>(t_row + W * c, r);
+                            tmem_ld_wait();
+                            if constexpr (!EP) {
+                                if (!row_ok) continue;
+                            }
+                            float acc[W];
+#pragma unroll
+                            for (int i = 0; i < W; i += 4) {
+                                const float4 q = ld_shared_v4f(stg + row_off + static_cast<uint32_t>(W * c + i) * 4u);
+                                acc[i] = __uint_as_float(r[i]) + q.x;
+                                acc[i + 1] = __uint_as_float(r[i + 1]) + q.y;
+                                acc[i + 2] = __uint_as_float(r[i + 2]) + q.z;
+                                acc[i + 3] = __uint_as_float(r[i + 3]) + q.w;
+                            }
+                            epilogue_chunk<Cfg, EP>(p, acc, row, col0, row_ok, lane);
+                        }
+                    }
+                }
+            }
+            if (kPairOK && x.role == kRolePair) {
+                // handled above
+            } else if (x.role == kRoleEarly) {
                 // an early split: its fp32 partial -> workspace, then the ready flag
                 if constexpr (W == 32) {
                     const int ws_row0 = static_cast<int>(
@@ -1666,8 +1755,14 @@ gemm_sm103_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     }
 
     tc_fence_before_sync();
-    if constexpr (CG == 1) __syncthreads();
-    else cluster_sync_all();              // the leader's MMAs into the peer's TMEM are finished
+    if constexpr (CG == 1) {
+        // pair_split: the first CTA of the pair stays until the second has
+        // written its partial into the first's shared memory
+        if (psplit) cluster_sync_all();
+        else __syncthreads();
+    } else {
+        cluster_sync_all();               // the leader's MMAs into the peer's TMEM are finished
+    }
     if (warp == 1) {
         __syncwarp();
         tc_fence_after_sync();

@@ -119,6 +119,8 @@ PATHS = {
     "coalesced_unaligned": (W("coal_u", 257, 263, 200, lb="col"), None, None),
     "transposed_split": (W("skinny", 16, 1104, 4096, dt="bf16", out="bf16", alpha=0.5, beta=1.0), "split",
                          "swapAB_splitk"),
+    "transposed_pair_split": (W("skinny_pair", 16, 1104, 4096, dt="bf16", out="bf16", alpha=0.5, beta=1.0),
+                              "pair_split", "swapAB_pairsplitk2"),
     "early_split": (W("early", 2300, 2290, 800, alpha=0.5, beta=1.0), "early_split", "esplitk"),
     "half_width": (W("halves", 1024, 1024, 1024, dt="bf16", out="bf16"), "halves", "nhalves"),
     "stream_k": (W("streamk", 3300, 3000, 256, alpha=0.5, beta=1.0), "stream_k", "streamk"),

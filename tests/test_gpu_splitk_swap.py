@@ -316,3 +316,79 @@ def test_stream_k_needs_two_waves(plans):
         assert e.value.status == 2
     finally:
         plan.force_division("auto")
+
+
+# CTA-pair split of the transposed product: each tile on a cluster of two
+# CTAs, each taking half the K blocks; the second hands its fp32 partial to
+# the first through shared memory and the first adds split 0 + split 1.
+PAIR_SHAPES = [(16, 1104, 520), (1, 2048, 256), (7, 600, 1000), (33, 712, 1000), (64, 512, 2048),
+               (64, 72, 640), (16, 9728, 136), (16, 8192, 8192)]
+
+
+@pytest.mark.parametrize("shape", PAIR_SHAPES, ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("layouts", LAYOUTS, ids=lambda l: "".join(x[0] for x in l))
+@pytest.mark.parametrize("out", ["f32", "bf16"])
+def test_pair_split_integer_twin(plans, shape, layouts, out):
+    from gpu_util import check_sampled
+    w = W(*shape, *layouts, dt="bf16", out=out, alpha=0.5, beta=1.0)
+    plan = plans["bf16"]
+    plan.force_division("pair_split")
+    try:
+        desc = plan.describe(w.M, w.N, w.K, w.layoutA, w.layoutB, "f32", out)
+        assert "_pairsplitk2" in desc, desc
+        lda, ldb = padded(w)
+        h = wl.make_inputs(w, integer=True, lda=lda, ldb=ldb)
+        D = run_gpu(plan, w, h)
+        torch.cuda.synchronize()
+    finally:
+        plan.force_division("auto")
+    if w.M * w.N * w.K <= 2e8:
+        check_full(w, h, D, integer=True)
+    else:
+        check_sampled(w, h, D, integer=True, n_random=8192)
+
+
+@pytest.mark.parametrize("shape", [(16, 4096, 4096), (48, 1024, 4096), (3, 1000, 1064)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_pair_split_equals_last_arriver_split(plans, shape):
+    """Random data: the pair split adds the same two fp32 partials in the
+    same order as the two-way last-arriver split, so the results are equal
+    bit for bit (and within the oracle's tolerance), call after call."""
+    w = W(*shape, "row", "row", dt="bf16", out="f32", alpha=0.5, beta=1.0)
+    plan = plans["bf16"]
+    h = wl.make_inputs(w)
+    try:
+        plan.force_division("split", 2)
+        assert "_swapAB_splitk2" in plan.describe(w.M, w.N, w.K, "row", "row", "f32", "f32")
+        D_split = run_gpu(plan, w, h)
+        plan.force_division("pair_split")
+        assert "_pairsplitk2" in plan.describe(w.M, w.N, w.K, "row", "row", "f32", "f32")
+        D_pair = run_gpu(plan, w, h)
+        torch.cuda.synchronize()
+        assert torch.equal(D_split, D_pair)
+        check_full(w, h, D_pair, integer=False)
+        for _ in range(5):
+            assert torch.equal(run_gpu(plan, w, h), D_pair)
+    finally:
+        plan.force_division("auto")
+
+
+def test_pair_split_limits(plans):
+    """The pair split is offered only where it applies: the transposed product
+    with fp32 accumulation, at least two K blocks, tiles within one wave of
+    pairs."""
+    import tensor_core_dense_tma_gb300 as tc
+    plan = plans["f16"]
+    plan.force_division("pair_split")
+    try:
+        for args in ((16, 4096, 64),                               # one 64-deep K block
+                     (16, 128 * 80, 1024),                         # 80 tiles: more than 76 pairs
+                     (512, 512, 1024),                             # not a transposed product
+                     (16, 4096, 1024, "row", "row", "f16", "f16")):   # fp16 accumulation
+            with pytest.raises(tc.GemmError) as e:
+                plan.describe(*args)
+            assert e.value.status == 2, args
+    finally:
+        plan.force_division("auto")
+    # the model's own choice for the skinny workload
+    assert "_pairsplitk2" in plans["bf16"].describe(16, 8192, 8192, "row", "row", "f32", "bf16")

@@ -24,9 +24,14 @@ def test_benchmark_workloads():
     assert d.startswith("tc2cta_256x256_acc32_out32_esplitk2 ") and "divided_tiles=28" in d
     # fp16 accumulate, column-major B: 256 x 224 tiles fill whole waves (16 x 19 = 4 x 76)
     assert model("f16", 4096, 4096, 4096, "row", "col", "f16", "f16").startswith("tc2cta_256x224_acc16_out16 ")
-    # M = 16: the transposed product with the narrow tile, split along K
+    # M = 16: the transposed product with the narrow tile, its 64 tiles split
+    # along K across CTA pairs (one wave of pairs)
     d = model("bf16", 16, 8192, 8192, "row", "row", "f32", "bf16")
-    assert d.startswith("tc1cta_128x16_acc32_outbf16_swapAB_splitk")
+    assert d.startswith("tc1cta_128x16_acc32_outbf16_swapAB_pairsplitk2 ")
+    assert "ctas=128 " in d
+    # more tiles than pairs (128 tiles): no pair split
+    d = model("bf16", 16, 16384, 8192, "row", "row", "f32", "bf16")
+    assert "pairsplit" not in d.split()[0]
     # fp8 8192^3 -> bf16 uses the same pipeline and division as bf16
     assert model("e4m3", 8192, 8192, 8192, "row", "col", "f32", "bf16").startswith(
         "tc2cta_256x256_acc32_outbf16_esplitk2 ")
