@@ -410,6 +410,23 @@ gemm_status_t gemm_run_static_scratch(int device, gemm_dtype_t in_dtype, const v
  * GEMM_ERR_INVALID_ARG for a bad ordinal, GEMM_ERR_CUDA if the copy fails. */
 gemm_status_t gemm_static_scratch_device_status(int device, int clear, void *stream);
 
+/* Timeline of gemm_run_host (diagnostics; the pages have no counterpart).
+ * With `enable` != 0, later gemm_run_host calls on this plan record a timing
+ * event after each copy in (A's rows of a row block, with C's; B's columns of
+ * a column block), after each block of D is computed and after it is copied
+ * back; gemm_plan_host_trace_read returns the last call's events once its
+ * stream has been synchronised.  Off by default (no timing events then). */
+gemm_status_t gemm_plan_host_trace(gemm_plan_t plan, int enable);
+
+/* The last traced gemm_run_host call's timeline: up to `max` entries, each a
+ * kind (0: A rows of row block `rows` copied in; 1: B columns of column block
+ * `cols` copied in; 2: block (rows, cols) of D computed; 3: that block copied
+ * back; cols = -1 means all columns), and the time in milliseconds since the
+ * call's first copy could start.  `count` receives the number of entries
+ * (0 when tracing is off).  Any of kinds, rows, cols, ms may be NULL. */
+gemm_status_t gemm_plan_host_trace_read(gemm_plan_t plan, int *kinds, int *rows, int *cols, float *ms, int max,
+                                        int *count);
+
 /* Tensor-core rate probe (no memory traffic): the median number of SM
  * cycles one tcgen05.mma with M = 256 (a CTA pair), N = `n` columns
  * (16..256, a multiple of 16) and 32 bytes of K (K = 16 for GEMM_F16 /

@@ -35,6 +35,7 @@ __all__ = [
     "gemm_plan_clear_tuning", "gemm_plan_tuned_count", "gemm_plan_force_division", "DIVISION",
     "gemm_run_prior_art", "PRIOR_ART", "gemm_mma_fragment_map", "run_prior_art", "gemm_describe_model",
     "gemm_plan_device_status_async", "gemm_plan_tensor_map_stats", "gemm_static_scratch_device_status",
+    "gemm_plan_host_trace", "gemm_plan_host_trace_read",
 ]
 
 STATUS = {
@@ -86,6 +87,11 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.gemm_plan_tensor_map_stats.restype = i32
     lib.gemm_static_scratch_device_status.argtypes = [i32, i32, p]
     lib.gemm_static_scratch_device_status.restype = i32
+    lib.gemm_plan_host_trace.argtypes = [p, i32]
+    lib.gemm_plan_host_trace.restype = i32
+    pi = ctypes.POINTER(ctypes.c_int)
+    lib.gemm_plan_host_trace_read.argtypes = [p, pi, pi, pi, ctypes.POINTER(ctypes.c_float), i32, pi]
+    lib.gemm_plan_host_trace_read.restype = i32
     lib.gemm_plan_set_timeout_ns.argtypes = [p, u64]
     lib.gemm_plan_set_timeout_ns.restype = i32
     lib.gemm_plan_force_config.argtypes = [p, i32, i32]
@@ -210,6 +216,27 @@ def gemm_plan_tensor_map_stats(plan) -> tuple[int, int]:
     if st != 0:
         raise GemmError(st, "gemm_plan_tensor_map_stats")
     return hits.value, misses.value
+
+
+def gemm_plan_host_trace(plan, enable: bool = True) -> int:
+    return load().gemm_plan_host_trace(plan, 1 if enable else 0)
+
+
+HOST_TRACE_KINDS = {0: "a_in", 1: "b_in", 2: "computed", 3: "d_back"}
+
+
+def gemm_plan_host_trace_read(plan, max_entries: int = 256) -> list[dict]:
+    """The last traced gemm_run_host call: [{kind, rows, cols, ms}, ...]."""
+    kinds = (ctypes.c_int * max_entries)()
+    rows = (ctypes.c_int * max_entries)()
+    cols = (ctypes.c_int * max_entries)()
+    ms = (ctypes.c_float * max_entries)()
+    n = ctypes.c_int()
+    st = load().gemm_plan_host_trace_read(plan, kinds, rows, cols, ms, max_entries, ctypes.byref(n))
+    if st != 0:
+        raise GemmError(st, "gemm_plan_host_trace_read")
+    return [{"kind": HOST_TRACE_KINDS[kinds[k]], "rows": rows[k], "cols": cols[k], "ms": ms[k]}
+            for k in range(n.value)]
 
 
 def gemm_static_scratch_device_status(device: int, clear: bool = False, stream=None) -> int:
@@ -444,6 +471,14 @@ class Plan:
 
     def tensor_map_stats(self) -> tuple[int, int]:
         return gemm_plan_tensor_map_stats(self.handle)
+
+    def host_trace(self, enable: bool = True):
+        st = gemm_plan_host_trace(self.handle, enable)
+        if st != 0:
+            raise GemmError(st, "gemm_plan_host_trace")
+
+    def host_trace_read(self) -> list[dict]:
+        return gemm_plan_host_trace_read(self.handle)
 
     def set_timeout_ns(self, ns: int):
         st = gemm_plan_set_timeout_ns(self.handle, ns)

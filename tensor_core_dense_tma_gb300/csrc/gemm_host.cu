@@ -36,6 +36,14 @@ struct HostPipeline {
     cudaEvent_t a_ready[kMaxSplit] = {}, b_ready[kMaxSplit] = {}, d_ready[kMaxSplit * kMaxSplit] = {};
     void* buf[4] = {nullptr, nullptr, nullptr, nullptr};   // A, B, C, D
     size_t cap[4] = {0, 0, 0, 0};
+    // timeline (gemm_plan_host_trace): timing events after each copy in, each
+    // block's compute and each copy back, created when tracing is turned on
+    static constexpr int kMaxTrace = 2 * kMaxSplit + 2 * kMaxSplit * kMaxSplit;
+    bool trace = false;
+    cudaEvent_t t_start = nullptr;
+    cudaEvent_t t_ev[kMaxTrace] = {};
+    int t_kind[kMaxTrace] = {}, t_i[kMaxTrace] = {}, t_j[kMaxTrace] = {};
+    int t_count = 0;
 };
 
 void destroy_host_pipeline(HostPipeline* hp) {
@@ -48,6 +56,9 @@ void destroy_host_pipeline(HostPipeline* hp) {
     }
     for (int i = 0; i < HostPipeline::kMaxSplit * HostPipeline::kMaxSplit; ++i)
         if (hp->d_ready[i]) cudaEventDestroy(hp->d_ready[i]);
+    if (hp->t_start) cudaEventDestroy(hp->t_start);
+    for (int i = 0; i < HostPipeline::kMaxTrace; ++i)
+        if (hp->t_ev[i]) cudaEventDestroy(hp->t_ev[i]);
     if (hp->start) cudaEventDestroy(hp->start);
     if (hp->done) cudaEventDestroy(hp->done);
     if (hp->h2d) cudaStreamDestroy(hp->h2d);
@@ -98,6 +109,16 @@ gemm_status_t staging(HostPipeline* hp, int i, size_t bytes, void** ptr) {
     }
     *ptr = hp->buf[i];
     return GEMM_OK;
+}
+
+// With tracing on, record a timing event of the given kind on stream s.
+bool trace_mark(HostPipeline* hp, int kind, int i, int j, cudaStream_t s) {
+    if (!hp->trace || hp->t_count >= HostPipeline::kMaxTrace) return true;
+    const int n = hp->t_count++;
+    hp->t_kind[n] = kind;
+    hp->t_i[n] = i;
+    hp->t_j[n] = j;
+    return cudaEventRecord(hp->t_ev[n], s) == cudaSuccess;
 }
 
 // Copy a rows x cols block of elements (row pitch `ld` elements on both sides).
@@ -168,6 +189,8 @@ extern "C" gemm_status_t gemm_run_host(gemm_plan_t plan, const void* A, const vo
     auto cols_of = [&](int j) { return (j + 1) * cols_per <= N ? cols_per : N - j * cols_per; };
 
     bool ok = cudaEventRecord(hp->start, user) == cudaSuccess && cudaStreamWaitEvent(hp->h2d, hp->start, 0) == cudaSuccess;
+    hp->t_count = 0;
+    if (hp->trace) ok = ok && cudaEventRecord(hp->t_start, hp->h2d) == cudaSuccess;
     // rows [r0, r0 + rows) of A: a row block (row-major) or the same rows of every column
     auto copy_a = [&](int i) {
         const int64_t r0 = i * rows_per, rows = rows_of(i);
@@ -182,7 +205,7 @@ extern "C" gemm_status_t gemm_run_host(gemm_plan_t plan, const void* A, const vo
         if (good && use_c)
             good = copy2d(static_cast<char*>(dC) + r0 * ldc * out_esz, static_cast<const char*>(C) + r0 * ldc * out_esz,
                           ldc, rows, N, out_esz, cudaMemcpyHostToDevice, hp->h2d);
-        return good && cudaEventRecord(hp->a_ready[i], hp->h2d) == cudaSuccess;
+        return good && cudaEventRecord(hp->a_ready[i], hp->h2d) == cudaSuccess && trace_mark(hp, 0, i, -1, hp->h2d);
     };
     // columns [c0, c0 + cols) of B: the same columns of every row (row-major) or a block of rows
     auto copy_b = [&](int j) {
@@ -195,7 +218,7 @@ extern "C" gemm_status_t gemm_run_host(gemm_plan_t plan, const void* A, const vo
                                   static_cast<const char*>(B) + c0 * ldb * in_esz, ldb, cols, K, in_esz,
                                   cudaMemcpyHostToDevice, hp->h2d);
         }
-        return good && cudaEventRecord(hp->b_ready[j], hp->h2d) == cudaSuccess;
+        return good && cudaEventRecord(hp->b_ready[j], hp->h2d) == cudaSuccess && trace_mark(hp, 1, -1, j, hp->h2d);
     };
     ok = ok && copy_a(0);
     for (int j = 0; ok && j < ncb; ++j) ok = copy_b(j);
@@ -229,10 +252,11 @@ extern "C" gemm_status_t gemm_run_host(gemm_plan_t plan, const void* A, const vo
                                         accum_dtype, out_dtype, alpha, beta, epp, hp->compute);
         if (bst != GEMM_OK) return bst;
         cudaEvent_t ev = hp->d_ready[i * HostPipeline::kMaxSplit + (j < 0 ? 0 : j)];
-        const bool good = cudaEventRecord(ev, hp->compute) == cudaSuccess &&
+        const bool good = trace_mark(hp, 2, i, j, hp->compute) && cudaEventRecord(ev, hp->compute) == cudaSuccess &&
                           cudaStreamWaitEvent(hp->d2h, ev, 0) == cudaSuccess &&
                           copy2d(static_cast<char*>(D) + doff, Db, ldc, rows, cols, out_esz, cudaMemcpyDeviceToHost,
-                                 hp->d2h);
+                                 hp->d2h) &&
+                          trace_mark(hp, 3, i, j, hp->d2h);
         return good ? GEMM_OK : GEMM_ERR_CUDA;
     };
     if (!ok) st = GEMM_ERR_CUDA;
@@ -248,6 +272,50 @@ extern "C" gemm_status_t gemm_run_host(gemm_plan_t plan, const void* A, const vo
     if (!ok) {
         cudaGetLastError();
         return GEMM_ERR_CUDA;
+    }
+    return GEMM_OK;
+}
+
+extern "C" gemm_status_t gemm_plan_host_trace(gemm_plan_t plan, int enable) {
+    if (!plan) return GEMM_ERR_INVALID_ARG;
+    int prev = -1;
+    if (cudaGetDevice(&prev) != cudaSuccess || cudaSetDevice(plan->device) != cudaSuccess) return GEMM_ERR_CUDA;
+    gemm_status_t st = GEMM_OK;
+    if (!plan->host_pipe) st = make_pipeline(&plan->host_pipe);
+    HostPipeline* hp = plan->host_pipe;
+    if (st == GEMM_OK && enable && !hp->t_start) {
+        bool ok = cudaEventCreate(&hp->t_start) == cudaSuccess;
+        for (int i = 0; ok && i < HostPipeline::kMaxTrace; ++i) ok = cudaEventCreate(&hp->t_ev[i]) == cudaSuccess;
+        if (!ok) {
+            cudaGetLastError();
+            st = GEMM_ERR_CUDA;
+        }
+    }
+    if (st == GEMM_OK) {
+        hp->trace = enable != 0;
+        hp->t_count = 0;
+    }
+    cudaSetDevice(prev);
+    return st;
+}
+
+extern "C" gemm_status_t gemm_plan_host_trace_read(gemm_plan_t plan, int* kinds, int* rows, int* cols, float* ms,
+                                                   int max, int* count) {
+    if (!plan || !count) return GEMM_ERR_INVALID_ARG;
+    *count = 0;
+    HostPipeline* hp = plan->host_pipe;
+    if (!hp || !hp->trace) return GEMM_OK;
+    for (int n = 0; n < hp->t_count && n < max; ++n) {
+        float t = 0.0f;
+        if (cudaEventElapsedTime(&t, hp->t_start, hp->t_ev[n]) != cudaSuccess) {
+            cudaGetLastError();
+            return GEMM_ERR_CUDA;
+        }
+        if (kinds) kinds[n] = hp->t_kind[n];
+        if (rows) rows[n] = hp->t_i[n];
+        if (cols) cols[n] = hp->t_j[n];
+        if (ms) ms[n] = t;
+        *count = n + 1;
     }
     return GEMM_OK;
 }

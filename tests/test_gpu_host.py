@@ -101,3 +101,37 @@ def test_host_rejects_device_tensors(plans):
     A = torch.zeros((64, 64), dtype=torch.float16, device="cuda")
     with pytest.raises(ValueError):
         plans["f16"].gemm_host(A, A)
+
+
+def test_host_trace_timeline(plans):
+    """The opt-in timeline of gemm_run_host: every copy in, every computed
+    block and every copy back is recorded once, in an order the pipeline's
+    dependencies allow (a block after its A rows and B columns are in, its
+    copy back after it is computed); the product is unchanged."""
+    w = W(3000, 5000, 320, out="bf16")
+    plan = plans["f16"]
+    h = wl.make_inputs(w, integer=True)
+    plan.host_trace(True)
+    try:
+        D = host_run(plan, w, h)
+        ev = plan.host_trace_read()
+    finally:
+        plan.host_trace(False)
+    check_full(w, h, D, integer=True)
+    a_in = {e["rows"]: e["ms"] for e in ev if e["kind"] == "a_in"}
+    b_in = {e["cols"]: e["ms"] for e in ev if e["kind"] == "b_in"}
+    comp = {(e["rows"], e["cols"]): e["ms"] for e in ev if e["kind"] == "computed"}
+    back = {(e["rows"], e["cols"]): e["ms"] for e in ev if e["kind"] == "d_back"}
+    # row blocks of 512 rows (6 of them), the first one in column blocks of 1024 (5)
+    nrb, ncb = len(a_in), len(b_in)
+    assert (nrb, ncb) == (6, 5)
+    assert sorted(a_in) == list(range(nrb)) and sorted(b_in) == list(range(ncb))
+    blocks = sorted([(0, j) for j in range(ncb)] + [(i, -1) for i in range(1, nrb)])
+    assert sorted(comp) == sorted(back) == blocks
+    for (i, j), t in comp.items():
+        assert t >= a_in[i] and t >= b_in[j if j >= 0 else max(b_in)]
+        assert back[(i, j)] >= t
+    assert all(e["ms"] >= 0 for e in ev)
+    # off again: nothing recorded
+    host_run(plan, w, h)
+    assert plan.host_trace_read() == []
