@@ -111,7 +111,8 @@ gemm_status_t gemm_plan_create(gemm_plan_t *out, int device, gemm_dtype_t in_dty
 
 /* Launch D = alpha*A*B + beta*C on `stream`.  Layout and pointers as in the
  * header comment.  M == 0 or N == 0 launches nothing and returns GEMM_OK;
- * K == 0 gives D = beta*C (zero when beta == 0).  One persistent kernel per
+ * K == 0 gives D = alpha*(+0) + beta*C: the empty sum is +0, so with
+ * beta == 0 D is a zero with the sign of alpha.  One persistent kernel per
  * call on the tensor-core path. */
 gemm_status_t gemm_run(gemm_plan_t plan, const void *A, const void *B, const void *C, void *D,
                        int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
@@ -133,8 +134,9 @@ gemm_status_t gemm_run(gemm_plan_t plan, const void *A, const void *B, const voi
  * N entries (NULL: 1 and 0).  act: GEMM_ACT_NONE (identity), GEMM_ACT_RELU
  * (max(u, 0)) or GEMM_ACT_GELU (u * Phi(u) = u/2 * (1 + erf(u / sqrt 2)),
  * the exact form; erfc is evaluated in fp32 by Abramowitz & Stegun 7.1.26,
- * so GELU is within about 1e-7 |u| + 1 ulp of the exact value).  With K == 0,
- * D = act(beta * C + bias). */
+ * so GELU is within about 1e-7 |u| + 1 ulp of the exact value).  With K == 0
+ * the sum is +0 and the same formula applies: D = act(alpha * row_scale[i] *
+ * col_scale[j] * (+0) + beta * C + bias). */
 typedef enum { GEMM_ACT_NONE = 0, GEMM_ACT_RELU = 1, GEMM_ACT_GELU = 2 } gemm_activation_t;
 
 typedef struct {

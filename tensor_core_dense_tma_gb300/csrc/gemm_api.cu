@@ -349,19 +349,23 @@ gemm_status_t prepare_all(gemm_plan* plan) {
 }
 
 gemm_status_t launch_scale(gemm_plan* plan, const void* C, void* D, int64_t M, int64_t N, int64_t ldc,
-                           gemm_dtype_t out, float beta, cudaStream_t stream, const gemm_epilogue_t* ep = nullptr) {
+                           gemm_dtype_t out, float alpha, float beta, cudaStream_t stream,
+                           const gemm_epilogue_t* ep = nullptr) {
     const int64_t total = M * N;
     int64_t blocks = (total + 255) / 256;
     if (blocks > 4LL * plan->sm_count) blocks = 4LL * plan->sm_count;
     const int32_t m = static_cast<int32_t>(M), n = static_cast<int32_t>(N);
+    const float* rs = ep ? ep->row_scale : nullptr;
+    const float* cs = ep ? ep->col_scale : nullptr;
     const float* bias = ep ? ep->bias : nullptr;
     const uint32_t act = ep ? static_cast<uint32_t>(ep->act) : 0u;
     if (out == GEMM_F32)
-        tcdt::scale_c_kernel<tcdt::kOutF32><<<blocks, 256, 0, stream>>>(m, n, C, D, ldc, beta, bias, act);
+        tcdt::scale_c_kernel<tcdt::kOutF32><<<blocks, 256, 0, stream>>>(m, n, C, D, ldc, alpha, beta, rs, cs, bias, act);
     else if (out == GEMM_F16)
-        tcdt::scale_c_kernel<tcdt::kOutF16><<<blocks, 256, 0, stream>>>(m, n, C, D, ldc, beta, bias, act);
+        tcdt::scale_c_kernel<tcdt::kOutF16><<<blocks, 256, 0, stream>>>(m, n, C, D, ldc, alpha, beta, rs, cs, bias, act);
     else
-        tcdt::scale_c_kernel<tcdt::kOutBF16><<<blocks, 256, 0, stream>>>(m, n, C, D, ldc, beta, bias, act);
+        tcdt::scale_c_kernel<tcdt::kOutBF16><<<blocks, 256, 0, stream>>>(m, n, C, D, ldc, alpha, beta, rs, cs, bias,
+                                                                         act);
     if (cudaGetLastError() != cudaSuccess) return GEMM_ERR_CUDA;
     ++plan->launches;
     return GEMM_OK;
@@ -554,7 +558,7 @@ gemm_status_t gemm_run_ep(gemm_plan_t plan, const void* A, const void* B, const 
     DeviceGuard guard(plan->device);
     if (!guard.ok) return GEMM_ERR_CUDA;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (K == 0) return launch_scale(plan, C, D, M, N, ldc, out_dtype, beta, s, ep);
+    if (K == 0) return launch_scale(plan, C, D, M, N, ldc, out_dtype, alpha, beta, s, ep);
     bool valid = true;
     const Choice ch = select_choice(plan, M, N, K, layoutA, layoutB, accum_dtype, out_dtype, &valid, nullptr);
     if (!valid) return GEMM_ERR_UNSUPPORTED;
@@ -1055,7 +1059,7 @@ extern "C" gemm_status_t gemm_run_static_scratch(int device, gemm_dtype_t in_dty
     }
     gemm_plan* plan = &ds.plan[in_dtype == GEMM_F16 ? 0 : 1];
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (K == 0) return launch_scale(plan, C, D, M, N, ldc, out_dtype, beta, s);
+    if (K == 0) return launch_scale(plan, C, D, M, N, ldc, out_dtype, alpha, beta, s);
 
     // the configuration gemm_run would pick, with the caller's split count
     bool valid = true;

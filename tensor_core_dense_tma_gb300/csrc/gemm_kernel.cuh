@@ -1770,16 +1770,22 @@ gemm_sm103_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     }
 }
 
-// D = act(beta * C + bias) (or act(bias), or 0) when K == 0: no product to accumulate.
+// K == 0: no product to accumulate.  The empty sum is +0 and goes through the
+// epilogue as an accumulator would -- scaled by row_scale[i] * col_scale[j],
+// then D = alpha * that (+ beta * C) (+ bias), activated -- so where nothing
+// else is added D keeps the sign of alpha * scale * 0, as the GEMM's own
+// epilogue gives it for a sum that comes to zero.
 template <int OUT>
-__global__ void scale_c_kernel(int32_t M, int32_t N, const void* C, void* D, int64_t ldc, float beta,
-                               const float* bias, uint32_t act) {
+__global__ void scale_c_kernel(int32_t M, int32_t N, const void* C, void* D, int64_t ldc, float alpha, float beta,
+                               const float* row_scale, const float* col_scale, const float* bias, uint32_t act) {
     const int64_t total = static_cast<int64_t>(M) * N;
     for (int64_t e = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; e < total;
          e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
         const int64_t i = e / N, j = e % N;
         const int64_t off = i * ldc + j;
-        float v = beta != 0.0f ? beta * load_elem<OUT>(C, off) : 0.0f;
+        const float s = (row_scale ? row_scale[i] : 1.0f) * (col_scale ? col_scale[j] : 1.0f);
+        const float a0 = 0.0f * s;
+        float v = beta != 0.0f ? fmaf(alpha, a0, beta * load_elem<OUT>(C, off)) : alpha * a0;
         if (bias) v += bias[j];
         float a[1] = {v};
         ep_act_w<1>(act, a);

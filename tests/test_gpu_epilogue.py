@@ -195,6 +195,22 @@ def test_epilogue_k_zero(plans, act):
     compare(w, ep, True, out_bits(D[:, :w.N]), Dref, V, S, "k0")
 
 
+@pytest.mark.parametrize("out", ["f32", "bf16"])
+@pytest.mark.parametrize("kind", ["plain", "scale", "scale_bias_relu"])
+@pytest.mark.parametrize("alpha,beta", [(-1.0, 0.0), (2.0, 0.0), (-1.0, 0.5), (0.5, 1.0)])
+def test_epilogue_k_zero_signs(plans, out, kind, alpha, beta):
+    """K = 0 with every epilogue term: the empty sum is +0, and alpha and the
+    (signed) scales act on it as on any accumulator, so where nothing else is
+    added D carries the sign of alpha * row_scale * col_scale * 0."""
+    w = W(f"k0_{kind}", 37, 70, 0, dt="bf16", out=out, alpha=alpha, beta=beta)
+    h = wl.make_inputs(w, integer=True)
+    ep = make_ep(w, kind, integer=True, seed=11)
+    D = run_ep(plans["bf16"], w, h, ep)
+    torch.cuda.synchronize()
+    Dref, V, S = oracle_ep(w, h, ep)
+    compare(w, ep, True, out_bits(D[:, :w.N]), Dref, V, S, "k0 signs")
+
+
 def test_epilogue_bad_activation(plans):
     import tensor_core_dense_tma_gb300 as tc
     A = torch.zeros((64, 64), dtype=torch.float16, device="cuda")
