@@ -78,6 +78,9 @@ def parse():
     ap.add_argument("--division", choices=["auto", "whole", "split", "early_split", "halves", "stream_k",
                                            "pair_split"],
                     default="auto", help="pin how the last wave's tiles are divided (gemm_plan_force_division)")
+    ap.add_argument("--config", choices=["auto", "single_128x16", "single_128x64", "single_128x256", "pair_256x256",
+                                         "pair_256x224", "pair_256x256_rowbulk"],
+                    default="auto", help="pin the kernel configuration (gemm_plan_force_config)")
     ap.add_argument("--autotune", action="store_true",
                     help="time every candidate configuration first (gemm_plan_autotune) and run the fastest")
     return ap.parse_args()
@@ -402,6 +405,8 @@ def main():
         plan.gemm(A_l, B_l, C_l, D_l, alpha=w.alpha, beta=w.beta, accum_dtype=w.accum_dtype,
                   out_dtype=w.out_dtype, stream=stream.cuda_stream, **ep)
 
+    if args.config != "auto":
+        plan.force_config(args.config)
     if args.division != "auto":
         plan.force_division(args.division)
     tuning = None

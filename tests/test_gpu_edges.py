@@ -114,6 +114,24 @@ def test_guard_bands_and_padded_ldc(plan, out):
     check_full(w, h, Dfull, integer=True)
 
 
+@pytest.mark.parametrize("out,N,ldc", [("f32", 263, 264), ("f32", 262, 268), ("f16", 301, 304), ("f16", 297, 312)])
+def test_aligned_rows_padding_untouched(plan, out, N, ldc):
+    """16-byte aligned D rows (the TMA-store path) whose N does not end on a
+    16-byte boundary: the padding columns after N must keep their contents."""
+    M, K = 300, 200
+    w = W(M, N, K, "row", "col", out=out, alpha=1.0, beta=0.0)
+    h = wl.make_inputs(w, integer=True, ldc=ldc)
+    A, B = h.A.cuda(), h.B.cuda()
+    dt = wl.DTYPES[out]
+    big = torch.full((M * ldc + 64,), float("nan"), dtype=dt, device="cuda")
+    Dfull = big[:M * ldc].view(M, ldc)
+    plan.gemm(wl.logical(A, M, K, "row"), wl.logical(B, K, N, "col"), None, Dfull[:, :N])
+    torch.cuda.synchronize()
+    assert torch.isnan(Dfull[:, N:].float()).all(), "padding columns were written"
+    assert torch.isnan(big[M * ldc:].float()).all()
+    check_full(w, h, Dfull, integer=True)
+
+
 def test_padded_lda_ldb_not_read(plan):
     """Leading dimensions beyond the extent: the padding holds NaN and must
     not reach the result."""
