@@ -79,7 +79,7 @@ def parse():
                                            "pair_split"],
                     default="auto", help="pin how the last wave's tiles are divided (gemm_plan_force_division)")
     ap.add_argument("--config", choices=["auto", "single_128x16", "single_128x64", "single_128x256", "pair_256x256",
-                                         "pair_256x224", "pair_256x256_rowbulk"],
+                                         "pair_256x224"],
                     default="auto", help="pin the kernel configuration (gemm_plan_force_config)")
     ap.add_argument("--autotune", action="store_true",
                     help="time every candidate configuration first (gemm_plan_autotune) and run the fastest")

@@ -205,12 +205,7 @@ typedef enum {
     GEMM_CONFIG_SINGLE_128x64 = 1,    /* transposed product, at most 64 rows */
     GEMM_CONFIG_SINGLE_128x256 = 2,   /* one CTA per 128 x 256 tile */
     GEMM_CONFIG_PAIR_256x256 = 3,     /* a CTA pair per 256 x 256 tile */
-    GEMM_CONFIG_PAIR_256x224 = 4,     /* a CTA pair per 256 x 224 tile */
-    GEMM_CONFIG_PAIR_256x256_ROWBULK = 5   /* a CTA pair per 256 x 256 tile, fp32 output: each
-                                            * row of C and D moves as one contiguous bulk copy
-                                            * (for an fp32 C, or D rows that are not 16-byte
-                                            * aligned); 16-bit operands, fp32 accumulation, no
-                                            * fused epilogue (other calls: GEMM_ERR_UNSUPPORTED) */
+    GEMM_CONFIG_PAIR_256x224 = 4      /* a CTA pair per 256 x 224 tile */
 } gemm_config_t;
 
 /* Pin the kernel configuration and the number of K splits (1..16) used by

@@ -249,7 +249,7 @@ def gemm_plan_set_timeout_ns(plan, ns: int) -> int:
 
 
 CONFIG = {"auto": -1, "single_128x16": 0, "single_128x64": 1, "single_128x256": 2, "pair_256x256": 3,
-          "pair_256x224": 4, "pair_256x256_rowbulk": 5}
+          "pair_256x224": 4}
 
 
 def gemm_plan_force_config(plan, config: str | int = "auto", splits: int = 0) -> int:

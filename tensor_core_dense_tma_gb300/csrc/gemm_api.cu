@@ -135,8 +135,7 @@ int default_units(const gemm_plan* plan, int kind) {
 // other and with their own splits; they get the same per-step cost.
 double step_cost(int kind, bool b_mn_major, bool half) {
     switch (kind) {
-        case kCfgPair256:
-        case kCfgPair256Rb: return half ? 0.83 : 1.0;
+        case kCfgPair256: return half ? 0.83 : 1.0;
         case kCfgPair224: return b_mn_major ? 1.0 : 0.92;
         case kCfgSingle256: return half ? 1.02 : 1.23;
         default: return 1.0;
@@ -194,8 +193,7 @@ Choice choose(const gemm_plan* plan, int64_t M, int64_t N, int64_t K, gemm_dtype
     if (plan->forced_kind >= 0) {
         const int f = plan->forced_kind;
         const bool f_swap = f == kCfgSingle16 || f == kCfgSingle64;
-        if (f_swap != swap || (f_swap && Nk > kCfgTileN[f]) ||
-            (!f16_kind && (f == kCfgPair224 || f == kCfgPair256Rb)) || (f == kCfgPair256Rb && acc == GEMM_F16)) {
+        if (f_swap != swap || (f_swap && Nk > kCfgTileN[f]) || (!f16_kind && f == kCfgPair224)) {
             *valid = false;
             return best;
         }
@@ -376,8 +374,7 @@ gemm_status_t launch_scale(gemm_plan* plan, const void* C, void* D, int64_t M, i
 std::string config_name(const Choice& ch, gemm_dtype_t acc, gemm_dtype_t out) {
     static const char* outs[4] = {"acc32_out32", "acc32_out16", "acc32_outbf16", "acc16_out16"};
     std::string s = "tc" + std::to_string(kCfgCtas[ch.kind]) + "cta_" + std::to_string(kCfgTileM[ch.kind]) + "x" +
-                    std::to_string(kCfgTileN[ch.kind]) + (ch.kind == kCfgPair256Rb ? "rb" : "") + "_" +
-                    outs[out_slot(acc, out)];
+                    std::to_string(kCfgTileN[ch.kind]) + "_" + outs[out_slot(acc, out)];
     if (ch.swap) s += "_swapAB";
     if (ch.pair_split) s += "_pairsplitk2";
     else if (ch.stream_k) s += "_streamk";
@@ -453,7 +450,6 @@ gemm_status_t run_choice(gemm_plan* plan, const Choice& ch, const void* A, const
     }
     if (ep) {
         switch (ch.kind) {
-            case kCfgPair256Rb: return GEMM_ERR_UNSUPPORTED;
             case kCfgSingle16: return launch_single16_ep(plan, slot, ch, pr, C, D, ldc, alpha, beta, s);
             case kCfgSingle64: return launch_single64_ep(plan, slot, ch, pr, C, D, ldc, alpha, beta, s);
             case kCfgSingle256: return launch_single256_ep(plan, slot, ch, pr, C, D, ldc, alpha, beta, s);
@@ -466,7 +462,6 @@ gemm_status_t run_choice(gemm_plan* plan, const Choice& ch, const void* A, const
         case kCfgSingle64: return launch_single64(plan, slot, ch, pr, C, D, ldc, alpha, beta, s);
         case kCfgSingle256: return launch_single256(plan, slot, ch, pr, C, D, ldc, alpha, beta, s);
         case kCfgPair224: return launch_pair224(plan, slot, ch, pr, C, D, ldc, alpha, beta, s);
-        case kCfgPair256Rb: return launch_pair256rb(plan, slot, ch, pr, C, D, ldc, alpha, beta, s);
         default: return launch_pair256(plan, slot, ch, pr, C, D, ldc, alpha, beta, s);
     }
 }
@@ -1101,7 +1096,6 @@ extern "C" gemm_status_t gemm_run_static_scratch(int device, gemm_dtype_t in_dty
         case kCfgSingle64: return launch_single64(plan, slot, ch, pr, C, D, ldc, alpha, beta, s);
         case kCfgSingle256: return launch_single256(plan, slot, ch, pr, C, D, ldc, alpha, beta, s);
         case kCfgPair224: return launch_pair224(plan, slot, ch, pr, C, D, ldc, alpha, beta, s);
-        case kCfgPair256Rb: return launch_pair256rb(plan, slot, ch, pr, C, D, ldc, alpha, beta, s);
         default: return launch_pair256(plan, slot, ch, pr, C, D, ldc, alpha, beta, s);
     }
 }

@@ -35,12 +35,7 @@ constexpr int kMaxSplits = 16;
 //  single256           : one CTA, 128 x 256, 4 stages of 48 KB;
 //  pair256             : CTA pair (cta_group::2), 256 x 256, 6 stages of 32 KB per CTA;
 //  pair224             : CTA pair, 256 x 224 (fills whole waves where 256 leaves a
-//                        partial one, e.g. N = 4096: 19 column tiles x 16 = 4 x 76 pairs);
-//  pair256rb           : CTA pair, 256 x 256, 4 stages, with the row-residue
-//                        epilogue (fp32 output, 16-bit operands, no fused
-//                        epilogue): C and D move as TMA boxes of the rows with
-//                        the same index mod 4, for an fp32 C or D rows that are
-//                        not 16-byte aligned.
+//                        partial one, e.g. N = 4096: 19 column tiles x 16 = 4 x 76 pairs).
 // IN: the operand kind (tcdt::kInF16, kInF8, kInTF32).
 template <bool ACC16, int OUT, int IN = tcdt::kInF16>
 using CfgSingle16 = tcdt::TileConfig<16, 8, 1, ACC16, OUT, IN>;
@@ -52,7 +47,6 @@ template <bool ACC16, int OUT, int IN = tcdt::kInF16>
 using CfgPair256 = tcdt::TileConfig<256, 6, 2, ACC16, OUT, IN>;
 template <bool ACC16, int OUT, int IN = tcdt::kInF16>
 using CfgPair224 = tcdt::TileConfig<224, 6, 2, ACC16, OUT, IN>;
-using CfgPair256Rb = tcdt::TileConfig<256, 4, 2, false, tcdt::kOutF32, tcdt::kInF16, true>;
 
 // Operand types: the tensor-core kind, the element size, and the format
 // field of the instruction descriptor (kind::f16: f16 0, bf16 1;
@@ -75,15 +69,14 @@ enum ConfigId : int {
     kCfgSingle256 = 2,
     kCfgPair256 = 3,
     kCfgPair224 = 4,
-    kCfgPair256Rb = 5,
-    kNumCfgKinds = 6
+    kNumCfgKinds = 5
 };
-constexpr int kCfgTileM[kNumCfgKinds] = {128, 128, 128, 256, 256, 256};
-constexpr int kCfgTileN[kNumCfgKinds] = {16, 64, 256, 256, 224, 256};
-constexpr int kCfgCtas[kNumCfgKinds] = {1, 1, 1, 2, 2, 2};
+constexpr int kCfgTileM[kNumCfgKinds] = {128, 128, 128, 256, 256};
+constexpr int kCfgTileN[kNumCfgKinds] = {16, 64, 256, 256, 224};
+constexpr int kCfgCtas[kNumCfgKinds] = {1, 1, 1, 2, 2};
 // configurations whose tiles can run as two half-width items (BN/2 a
 // multiple of 32: whole epilogue chunks)
-constexpr bool kCfgHalves[kNumCfgKinds] = {false, true, true, true, false, true};
+constexpr bool kCfgHalves[kNumCfgKinds] = {false, true, true, true, false};
 
 inline int out_slot(gemm_dtype_t acc, gemm_dtype_t out) {
     if (acc == GEMM_F16) return 3;
@@ -194,10 +187,6 @@ TCDT_DECLARE_KIND(single256)
 TCDT_DECLARE_KIND(pair256)
 TCDT_DECLARE_KIND(pair224)
 #undef TCDT_DECLARE_KIND
-// the row-bulk pair kernel exists for fp32 output (slot 0) only, without the fused epilogue
-gemm_status_t prepare_pair256rb(gemm_plan* plan, int slot);
-gemm_status_t launch_pair256rb(gemm_plan* plan, int slot, const Choice& ch, const Problem& pr, const void* C,
-                               void* D, int64_t ldc, float alpha, float beta, cudaStream_t s);
 // 8-bit and tf32 operands (no 256 x 224 tiles), without and with the fused epilogue
 #define TCDT_DECLARE_KIND_IN(name, suffix)                                                               \
     gemm_status_t launch_##name##_##suffix(gemm_plan* plan, int slot, const Choice& ch, const Problem& pr, \
@@ -414,34 +403,6 @@ gemm_status_t launch_tc(gemm_plan* plan, const Choice& ch, const Problem& pr, co
     p.fi_skip_load = plan->fi_skip_load;
 #endif
 
-    typename Cfg::XMaps xm;
-    std::memset(&xm, 0, sizeof(xm));
-    if constexpr (Cfg::RB) {
-        // the row-residue epilogue's maps: for r = 0..3 the rows i = r (mod 4)
-        // of C and of D, from the 16-byte boundary at or before row r's start
-        // (s elements back), so element (x, y) is row 4 y + r, column x - s
-        if (Cfg::CG != 2 || pr.swap || pr.M < 4) return GEMM_ERR_UNSUPPORTED;
-        for (int r = 0; r < 4; ++r) {
-            const uint64_t rows = static_cast<uint64_t>((pr.M - r + 3) / 4);
-            if (beta != 0.0f) {
-                const uintptr_t a = reinterpret_cast<uintptr_t>(C) + static_cast<uintptr_t>(r * ldc) * 4u;
-                const uint64_t s = (a & 15u) >> 2;
-                st = encode_map(plan, &xm.c[r], reinterpret_cast<const void*>(a - 4u * s), pr.N + s, rows, 4 * ldc,
-                                Cfg::RB_CW, 32, GEMM_F32, CU_TENSOR_MAP_SWIZZLE_NONE);
-                if (st != GEMM_OK) return st;
-            }
-            const uintptr_t a = reinterpret_cast<uintptr_t>(D) + static_cast<uintptr_t>(r * ldc) * 4u;
-            const uint64_t s = (a & 15u) >> 2;
-            // rows end at their last whole 16-byte unit (TMA stores write whole units);
-            // the kernel stores the elements after it one by one
-            const uint64_t inner = (pr.N + s) / 4 * 4;
-            st = encode_map(plan, &xm.d[r], reinterpret_cast<const void*>(a - 4u * s), inner < 4 ? 4 : inner, rows,
-                            4 * ldc, s ? 28 : 32, 32, GEMM_F32,
-                            s ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B);
-            if (st != GEMM_OK) return st;
-        }
-    }
-
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[1];
     fill_launch_config<Cfg>(cfg, attr, stream);
@@ -458,7 +419,7 @@ gemm_status_t launch_tc(gemm_plan* plan, const Choice& ch, const Problem& pr, co
         cfg.numAttrs = 1;
         cfg.gridDim = dim3(2 * p.num_tiles, 1, 1);
     }
-    if (cudaLaunchKernelEx(&cfg, tcdt::gemm_sm103_kernel<Cfg, EP>, tmA, tmB, tmBh, tmD, tmW, p, xm) != cudaSuccess) {
+    if (cudaLaunchKernelEx(&cfg, tcdt::gemm_sm103_kernel<Cfg, EP>, tmA, tmB, tmBh, tmD, tmW, p) != cudaSuccess) {
         cudaGetLastError();
         return GEMM_ERR_CUDA;
     }

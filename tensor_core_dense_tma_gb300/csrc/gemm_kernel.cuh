@@ -48,7 +48,6 @@
 #include <cuda_fp16.h>
 
 #include <cstdint>
-#include <type_traits>
 
 #include "ptx_sm103.cuh"
 
@@ -65,7 +64,6 @@ enum WaitSite : int {
     kSiteEpilogueAccFull = 4,
     kSitePartialReady = 5,
     kSiteMmaAccInit = 6,
-    kSiteEpilogueC = 7,
 };
 
 struct KernelParams {
@@ -116,15 +114,7 @@ struct KernelParams {
 // rows of the accumulator in its own tensor memory.  IN_ is the operand
 // kind (kInF16, kInF8, kInTF32): a K block is always one 128-byte swizzle
 // row of each operand row (64, 128 or 32 elements) and an MMA 32 bytes of it.
-// RB_: the row-residue epilogue for fp32 output (see rb_* below).
-struct RbMaps {
-    CUtensorMap c[4];   // C rows i = r (mod 4), from 16 bytes at or before each row's start
-    CUtensorMap d[4];   // D, the same
-};
-struct NoMaps {
-    int unused;
-};
-template <int BN_, int STAGES_, int CG_, bool ACC_F16_, int OUT_, int IN_ = kInF16, bool RB_ = false>
+template <int BN_, int STAGES_, int CG_, bool ACC_F16_, int OUT_, int IN_ = kInF16>
 struct TileConfig {
     static constexpr int CG = CG_;                 // CTAs per MMA (1 or 2)
     static constexpr int BM = 128;                 // accumulator rows per CTA (TMEM lanes)
@@ -156,28 +146,11 @@ struct TileConfig {
                                    : 2 * ACC_COLS <= 128 ? 128 : 2 * ACC_COLS <= 256 ? 256 : 512;
     static constexpr int NUM_EPI_WARPS = 4;
     static constexpr int NUM_THREADS = 32 * (2 + NUM_EPI_WARPS);
-    // row-residue epilogue (RB, see rb_* below): C and D of the CTA's 128 rows
-    // move as TMA boxes of the 32 rows with the same index mod 4.  C: RB_NC
-    // buffers of four 32 x 36 boxes (a 32-column chunk plus the row's 16-byte
-    // phase); D: RB_ND buffers of four 32 x 32 boxes (128-byte swizzled; 28
-    // columns used, unswizzled, for rows not 16-byte aligned).  The region
-    // also holds the staging buffers below (its first 32 KB).
-    static constexpr bool RB = RB_;
-    static constexpr int RB_CW = 36;
-    static constexpr int RB_CBOX = 32 * RB_CW * 4;
-    static constexpr int RB_CBUF = 4 * RB_CBOX;
-    static constexpr int RB_NC = 3;
-    static constexpr int RB_DBOX = 32 * 32 * 4;
-    static constexpr int RB_DBUF = 4 * RB_DBOX;
-    static constexpr int RB_ND = 2;
-    static constexpr int RB_BYTES = RB_NC * RB_CBUF + RB_ND * RB_DBUF;
-    static constexpr int NUM_BARRIERS = 2 * STAGES + 2 + 2 + 1 + 1 + NUM_EPI_WARPS + (RB ? RB_NC : 0);
+    static constexpr int NUM_BARRIERS = 2 * STAGES + 2 + 2 + 1 + 1 + NUM_EPI_WARPS;
     // epilogue staging for TMA stores: per epilogue warp two 32-row buffers
     // of up to 128 bytes a row (32 fp32 columns)
     static constexpr int STAGING_BUF = 32 * 128;
-    static constexpr int STAGING_WARP = 2 * STAGING_BUF;
-    static constexpr int STAGING_BYTES =
-        RB && RB_BYTES > NUM_EPI_WARPS * STAGING_WARP ? RB_BYTES : NUM_EPI_WARPS * STAGING_WARP;
+    static constexpr int STAGING_BYTES = NUM_EPI_WARPS * 2 * STAGING_BUF;
     // after the barriers: TMEM address, abort flag, 2 wait flags, 2 split flags
     static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + STAGING_BYTES + NUM_BARRIERS * 8 + 32;
     static_assert(CG == 1 || CG == 2, "CTA group");
@@ -186,10 +159,6 @@ struct TileConfig {
     static_assert(BN_CTA % 8 == 0, "K-major B tile rows come in 8-row swizzle atoms");
     static_assert(2 * ACC_COLS <= 512, "two accumulators must fit tensor memory");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
-    static_assert(!RB || (OUT == kOutF32 && W == 32 && CG == 2 && RB_BYTES % 1024 == 0 &&
-                          (RB_NC * RB_CBUF) % 1024 == 0), "row-residue epilogue");
-    // the row-residue epilogue's tensor maps (a kernel parameter of the RB kernels only)
-    using XMaps = typename std::conditional<RB, RbMaps, NoMaps>::type;
 };
 
 // Grouped raster: tiles run down a band of `group_m` m-blocks before moving
@@ -1060,114 +1029,13 @@ __device__ __forceinline__ void stage_and_store_f32(const void* tmap, const uint
 }
 
 // ---------------------------------------------------------------------------
-// row-residue epilogue (TileConfig RB, fp32 output, CTA pairs): tiles that
-// read an fp32 C, or whose D rows are not 16-byte aligned
-// ---------------------------------------------------------------------------
-// A tensor map needs 16-byte aligned rows, which an fp32 matrix whose ldc is
-// not a multiple of 4 does not have.  But the rows i = r (mod 4) of such a
-// matrix, for each r, are 16 ldc bytes apart: a matrix with 16-byte aligned
-// rows once its base is moved back to the 16-byte boundary at or before row
-// r's start, s_r elements back (s_r: row r's 16-byte phase in elements).
-// The host encodes one tensor map per residue r for C and for D; in map r,
-// element (x, y) is row 4 y + r, column x - s_r of the matrix.  A CTA's 128
-// rows (its first row a multiple of 4) are 32 rows of each residue, so a
-// 32-column chunk of C moves as four 32 x 36 boxes at x = the chunk's first
-// column (36 columns cover its 32 at any phase), and of D as four boxes of
-// the 16-byte-aligned part of each row's chunk: all 32 columns when s_r = 0,
-// else the 28 from column 4 - s_r, the 4 - s_r + s_r elements outside them
-// stored one by one.  Four requests per chunk move what element-wise
-// accesses across unaligned rows move in 64 instructions a lane.  Boxes
-// whose rows all lie past M are skipped; C columns past N read as zero.  A
-// TMA store writes whole 16-byte units, also where the tensor's row ends
-// inside one (measured: the units' other bytes, the next row's first
-// elements, were overwritten), so the D maps end at the last whole unit of
-// each row and the up to 3 elements after it are stored one by one.
-
-// Issue chunk C loads of the CTA's rows [4 y0, 4 y0 + 128) into buffer
-// `cbuf`, completing on `bar` (one thread).
-__device__ __forceinline__ void rb_load_c(const RbMaps& xm, uint32_t cbuf, uint32_t bar, int col0, int y0, int M,
-                                          int cbox_bytes) {
-    uint32_t bytes = 0;
-#pragma unroll
-    for (int r = 0; r < 4; ++r)
-        if (4 * y0 + r < M) bytes += static_cast<uint32_t>(cbox_bytes);
-    mbar_arrive_expect_tx(bar, bytes);
-#pragma unroll
-    for (int r = 0; r < 4; ++r)
-        if (4 * y0 + r < M) tma_load_2d(cbuf + static_cast<uint32_t>(r * cbox_bytes), &xm.c[r], bar, col0, y0);
-}
-
-// Issue the D stores of a chunk from buffer `dbuf` and commit them as one
-// bulk group (one thread).  sd_r: D row r's 16-byte phase in elements.
-__device__ __forceinline__ void rb_store_d(const RbMaps& xm, uint32_t dbuf, int col0, int y0, int M, int N,
-                                           uintptr_t d_addr, int64_t ldc, int dbox_bytes) {
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {
-        const int sd = static_cast<int>(((d_addr + static_cast<uintptr_t>(4 * y0 + r) * static_cast<uintptr_t>(ldc) * 4u) &
-                                         15u) >> 2);
-        const int first = col0 + (sd ? 4 - sd : 0);   // the box's first column
-        const int lim = (N + sd) & ~3;                 // the map's row length: whole 16-byte units
-        if (4 * y0 + r < M && first + sd < lim)
-            tma_store_2d(&xm.d[r], dbuf + static_cast<uint32_t>(r * dbox_bytes), first + sd, y0);
-    }
-    bulk_commit_group();
-}
-
-// This lane's part of a chunk: its row's 32 accumulator values, alpha * acc
-// (+ beta * C from the C box) into the D box, or straight to D for the
-// elements outside the box.  q: the lane's row within its residue's boxes.
-__device__ __forceinline__ void rb_chunk(const KernelParams& p, const uint32_t (&r)[32], int row, bool row_ok, int col0,
-                                         bool has_c, uint32_t cbox, uint32_t dbox, int q) {
-    const uintptr_t rowoff = static_cast<uintptr_t>(row) * static_cast<uintptr_t>(p.ldc) * 4u;
-    float v[32];
-    if (has_c) {
-        const int sc = static_cast<int>(((reinterpret_cast<uintptr_t>(p.C) + rowoff) & 15u) >> 2);
-        const uint32_t c0 = cbox + static_cast<uint32_t>(q * 144 + 4 * sc);
-        float c[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) c[i] = ld_shared_f32(c0 + 4u * i);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] = fmaf(p.alpha, __uint_as_float(r[i]), p.beta * c[i]);
-    } else {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] = p.alpha * __uint_as_float(r[i]);
-    }
-    const uintptr_t gd = reinterpret_cast<uintptr_t>(p.D) + rowoff + static_cast<uintptr_t>(col0) * 4u;
-    const int sd = static_cast<int>((gd & 15u) >> 2);
-    float* dst = reinterpret_cast<float*>(gd);
-    const int nvalid = p.N - col0;
-    const int nbox = ((p.N + sd) & ~3) - sd - col0;   // elements before the map's row end
-    if (sd == 0) {
-        // the whole chunk in the box, 128-byte swizzled: 16-byte unit u of box row q at u ^ (q % 8)
-        const uint32_t rowp = dbox + static_cast<uint32_t>(q * 128);
-#pragma unroll
-        for (int u = 0; u < 8; ++u)
-            st_shared_v4(rowp + ((static_cast<uint32_t>(u) ^ (static_cast<uint32_t>(q) & 7u)) << 4), __float_as_uint(v[4 * u]),
-                         __float_as_uint(v[4 * u + 1]), __float_as_uint(v[4 * u + 2]), __float_as_uint(v[4 * u + 3]));
-#pragma unroll
-        for (int i = 0; i < 32; ++i)
-            if (row_ok && i >= nbox && i < nvalid) dst[i] = v[i];
-    } else {
-        // columns [h, h + 28) in the box (rows of 112 bytes), the rest straight to D
-        const int h = 4 - sd;
-        const uint32_t base = dbox + static_cast<uint32_t>(q * 112 - 4 * h);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            if (i >= h && i < h + 28 && i < nbox) st_shared_f32(base + 4u * i, v[i]);
-            else if (row_ok && i < nvalid) dst[i] = v[i];
-        }
-    }
-}
-
-// ---------------------------------------------------------------------------
 // the kernel
 // ---------------------------------------------------------------------------
 template <class Cfg, bool EP = false>
 __global__ void __launch_bounds__(Cfg::NUM_THREADS, 1)
 gemm_sm103_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                   const __grid_constant__ CUtensorMap tmBh, const __grid_constant__ CUtensorMap tmD,
-                  const __grid_constant__ CUtensorMap tmW, const KernelParams p,
-                  const __grid_constant__ typename Cfg::XMaps xm) {
+                  const __grid_constant__ CUtensorMap tmW, const KernelParams p) {
     constexpr int CG = Cfg::CG;
     constexpr int W = Cfg::W;
     extern __shared__ uint8_t smem_raw[];
@@ -1184,8 +1052,6 @@ gemm_sm103_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     const uint32_t drain_bar = bar_base + 8u * (2 * Cfg::STAGES + 4);
     const uint32_t accinit_bar = bar_base + 8u * (2 * Cfg::STAGES + 5);   // owner accumulator seeded
     auto seed_bar = [&](int w) { return bar_base + 8u * (2 * Cfg::STAGES + 6 + w); };   // per epilogue warp
-    // row-residue epilogue: C chunk loads into buffer b
-    auto rb_bar = [&](int b) { return bar_base + 8u * (2 * Cfg::STAGES + 6 + Cfg::NUM_EPI_WARPS + b); };
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base_ptr + Cfg::STAGES * Cfg::STAGE_BYTES +
                                                       Cfg::STAGING_BYTES + 8 * Cfg::NUM_BARRIERS);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -1227,9 +1093,6 @@ gemm_sm103_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         mbar_init(drain_bar, 1);
         mbar_init(accinit_bar, Cfg::NUM_EPI_WARPS * CG);
         for (int w = 0; w < Cfg::NUM_EPI_WARPS; ++w) mbar_init(seed_bar(w), 1);
-        if constexpr (Cfg::RB) {
-            for (int b = 0; b < Cfg::RB_NC; ++b) mbar_init(rb_bar(b), 1);
-        }
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -1241,12 +1104,6 @@ gemm_sm103_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         if (p.n_halves && !b_mn) tma_prefetch_desc(&tmBh);
         if (p.d_tma) tma_prefetch_desc(&tmD);
         if (p.splits > 1) tma_prefetch_desc(&tmW);
-        if constexpr (Cfg::RB) {
-            for (int r = 0; r < 4; ++r) {
-                if (p.beta != 0.0f) tma_prefetch_desc(&xm.c[r]);
-                tma_prefetch_desc(&xm.d[r]);
-            }
-        }
     }
     if (warp == 1) {
         tmem_alloc<CG>(smem_addr(tmem_slot), Cfg::TMEM_COLS);
@@ -1457,19 +1314,12 @@ gemm_sm103_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         // ------------------------------------------------------------------
         const int quad = warp % 4;
         const int row_local = 32 * quad + lane;
-        const uint32_t stg = staging_base + static_cast<uint32_t>(warp - 2) * Cfg::STAGING_WARP;
+        const uint32_t stg = staging_base + static_cast<uint32_t>(warp - 2) * 2u * Cfg::STAGING_BUF;
         int sbuf = 0;                     // staging buffer for the next TMA store of this warp
         uint32_t seed_phase = 0;          // phase of this warp's seed barrier
         uint64_t t_prev_acc = globaltimer_ns();   // when the previous accumulator became ready
         int buf = 0;
         uint32_t acc_phase = 0;
-        // row-residue epilogue (Cfg::RB), the same in every epilogue thread:
-        // the C and D buffers of the next chunk, the phase of each C buffer's
-        // barrier, the C buffers with loads not yet waited for, and whether
-        // the previous item used this epilogue
-        int rb_cb = 0, rb_db = 0;
-        uint32_t rb_phase = 0, rb_pending = 0;
-        bool rb_prev = false;
         int iter = 0;
         for (; iter < num_items; ++iter) {
             const WorkItem x = item_at(iter);
@@ -1479,25 +1329,6 @@ gemm_sm103_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             const bool half = Cfg::HALVES_OK && x.half >= 0;
             const int n0 = nb * Cfg::BN + (half ? x.half * (Cfg::BN / 2) : 0);
             const int nchunks = (half ? Cfg::BN / 2 : Cfg::BN) / W;
-            bool rb_item = false;
-            int rb_np = 0;   // chunks of this item (0: none; the same in all four warps)
-            if constexpr (Cfg::RB && !EP) {
-                rb_item = (x.nsplit == 1 || x.role == kRoleOwner) && !p.trans_out && (p.beta != 0.0f || !p.d_tma);
-                const int cols = min(nchunks * W, p.N - n0);
-                // (C loads still pending here mean a wait gave up: the launch is aborting)
-                if (rb_item && cols > 0 && m0 < p.M && rb_pending == 0) rb_np = (cols + W - 1) / W;
-                // warm L2 with this thread's C row of the next item too
-                if (p.beta != 0.0f && !p.trans_out && iter + 1 < num_items) {
-                    const WorkItem y = item_at(iter + 1);
-                    int mby, nby;
-                    tile_coords(p, y.tile, mby, nby);
-                    const int m0y = mby * Cfg::UMMA_M + Cfg::BM * static_cast<int>(rank);
-                    const bool halfy = Cfg::HALVES_OK && y.half >= 0;
-                    const int n0y = nby * Cfg::BN + (halfy ? y.half * (Cfg::BN / 2) : 0);
-                    if (m0y + row_local < p.M)
-                        prefetch_c_row<Cfg>(p, m0y + row_local, n0y, halfy ? Cfg::BN / 2 : Cfg::BN);
-                }
-            }
             // warm L2 with this thread's C row while the main loop runs
             if (p.beta != 0.0f && !p.trans_out && m0 + row_local < p.M)
                 prefetch_c_row<Cfg>(p, m0 + row_local, n0, nchunks * W);
@@ -1606,25 +1437,6 @@ gemm_sm103_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 }
                 if (seed_failed) break;
             }
-            if constexpr (Cfg::RB && !EP) {
-                // C of the first three chunks needs no accumulator: load it while the
-                // main loop runs.  The C buffers overlap the staging buffers: TMA
-                // stores an earlier item issued from those finish reading first.
-                if (rb_np > 0 && p.beta != 0.0f) {
-                    if (!rb_prev) {
-                        if (lane == 0) bulk_wait_group_read<0>();
-                        named_bar_sync(1, 32 * Cfg::NUM_EPI_WARPS);
-                    }
-#pragma unroll 1
-                    for (int q = 0; q < 3 && q < rb_np; ++q) {
-                        const int b = (rb_cb + q) % Cfg::RB_NC;
-                        if (threadIdx.x == 64)
-                            rb_load_c(xm, staging_base + static_cast<uint32_t>(b * Cfg::RB_CBUF), rb_bar(b), n0 + W * q,
-                                      m0 / 4, p.M, Cfg::RB_CBOX);
-                        rb_pending |= 1u << b;
-                    }
-                }
-            }
             if (threadIdx.x == 64)
                 epi_ok_flag[iter & 1] = wait_phase(accf_bar(buf), acc_phase, wctx, kSiteEpilogueAccFull) ? 1 : 0;
             named_bar_sync(1, 32 * Cfg::NUM_EPI_WARPS);
@@ -1709,51 +1521,8 @@ gemm_sm103_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 }
             } else if (x.nsplit == 1 || x.role == kRoleOwner) {
                 bool staged = false;
-                if constexpr (Cfg::RB && !EP) {
-                    if (rb_item) {
-                        staged = true;
-                        const bool has_c = p.beta != 0.0f;
-                        const int rres = lane & 3;                       // this row's residue (m0 % 4 == 0)
-                        const int qrow = 8 * quad + (lane >> 2);         // its row in the residue's boxes
-                        const uint32_t dbase = staging_base + static_cast<uint32_t>(Cfg::RB_NC * Cfg::RB_CBUF);
-#pragma unroll 1
-                        for (int g = 0; g < rb_np; ++g) {
-                            const int col0 = n0 + W * g;
-                            const int cb = (rb_cb + g) % Cfg::RB_NC;
-                            const int db = (rb_db + g) & 1;
-                            bool ok = true;
-                            if (has_c) {
-                                ok = warp_wait_phase(rb_bar(cb), (rb_phase >> cb) & 1u, wctx, kSiteEpilogueC);
-                                rb_phase ^= 1u << cb;
-                                rb_pending &= ~(1u << cb);
-                            }
-                            if (ok) {
-                                __syncwarp();
-                                uint32_t r[W];
-                                tmem_ld_row<W>(t_row + W * g, r);
-                                tmem_ld_wait();
-                                rb_chunk(p, r, row, row_ok, col0, has_c,
-                                         staging_base + static_cast<uint32_t>(cb * Cfg::RB_CBUF + rres * Cfg::RB_CBOX),
-                                         dbase + static_cast<uint32_t>(db * Cfg::RB_DBUF + rres * Cfg::RB_DBOX), qrow);
-                            }
-                            fence_proxy_async_smem();   // the D box writes before the tensor unit reads them
-                            // the previous chunk's D stores have read their buffer (the next chunk's)
-                            if (threadIdx.x == 64) bulk_wait_group_read<0>();
-                            // all warps are done with this chunk's C and D buffers (and all succeeded)
-                            if (!named_bar_and(1, 32 * Cfg::NUM_EPI_WARPS, ok)) break;
-                            if (threadIdx.x == 64) {
-                                rb_store_d(xm, dbase + static_cast<uint32_t>(db * Cfg::RB_DBUF), col0, m0 / 4, p.M, p.N,
-                                           reinterpret_cast<uintptr_t>(p.D), p.ldc, Cfg::RB_DBOX);
-                                if (has_c && g + 3 < rb_np)
-                                    rb_load_c(xm, staging_base + static_cast<uint32_t>(cb * Cfg::RB_CBUF), rb_bar(cb),
-                                              col0 + 3 * W, m0 / 4, p.M, Cfg::RB_CBOX);
-                            }
-                            if (has_c && g + 3 < rb_np) rb_pending |= 1u << cb;
-                        }
-                    }
-                }
                 if constexpr (W == 32) {
-                    if (!staged && p.d_tma && (p.beta == 0.0f || Cfg::OUT != kOutF32)) {
+                    if (p.d_tma && (p.beta == 0.0f || Cfg::OUT != kOutF32)) {
                         // staged through shared memory, one TMA store per 32 x 32 segment.
                         // When another tile follows, the segments are spread over about half
                         // the time the last tile took, so that their shared-memory and store
@@ -1969,11 +1738,6 @@ gemm_sm103_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                     }
                 }
             }
-            if constexpr (Cfg::RB && !EP) {
-                rb_cb = (rb_cb + rb_np) % Cfg::RB_NC;
-                rb_db = (rb_db + rb_np) & 1;
-                rb_prev = rb_np > 0;
-            }
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0) {
@@ -1983,14 +1747,6 @@ gemm_sm103_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             if (++buf == 2) {
                 buf = 0;
                 acc_phase ^= 1u;
-            }
-        }
-        if constexpr (Cfg::RB && !EP) {
-            // after an abort: C loads still in flight land before the CTA leaves
-            if (threadIdx.x == 64) {
-#pragma unroll 1
-                for (int b = 0; b < Cfg::RB_NC; ++b)
-                    if ((rb_pending >> b) & 1u) wait_phase_drain(rb_bar(b), (rb_phase >> b) & 1u, 100000000ull);
             }
         }
         // TMA stores still reading the staging buffers (or writing D) finish first

@@ -160,23 +160,6 @@ __device__ __forceinline__ void prefetch_l2_bulk(const void* addr, uint32_t byte
                  : "memory");
 }
 
-// Contiguous (non-tensor) bulk copy global -> this CTA's shared memory of
-// `bytes` bytes, completing on the mbarrier `bar` (complete_tx).  Both
-// addresses 16-byte aligned, `bytes` a nonzero multiple of 16.
-__device__ __forceinline__ void bulk_load_1d(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-                 "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
-                 : "memory");
-}
-
-// Contiguous bulk copy shared -> global, tracked with bulk async-groups (same
-// alignment rules as bulk_load_1d).
-__device__ __forceinline__ void bulk_store_1d(void* dst, uint32_t src, uint32_t bytes) {
-    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(reinterpret_cast<uint64_t>(dst)),
-                 "r"(src), "r"(bytes)
-                 : "memory");
-}
-
 // TMA store: shared-memory box -> global tensor (out-of-range elements are
 // not written).  Completion is tracked with bulk async-groups.
 __device__ __forceinline__ void tma_store_2d(const void* tmap, uint32_t src, int32_t x, int32_t y) {
@@ -450,21 +433,6 @@ __device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
 // Named barrier over `count` threads (id 0 is __syncthreads).
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
-}
-
-// named_bar_sync that also ANDs a predicate over the participating threads:
-// true in every thread iff `pred` was true in all of them.
-__device__ __forceinline__ bool named_bar_and(uint32_t id, uint32_t count, bool pred) {
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\t"
-        "setp.ne.u32 p, %1, 0;\n\t"
-        "barrier.cta.red.and.pred q, %2, %3, p;\n\t"
-        "selp.u32 %0, 1, 0, q;\n\t}"
-        : "=r"(r)
-        : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(count)
-        : "memory");
-    return r != 0;
 }
 
 __device__ __forceinline__ void tmem_ld_wait() {
