@@ -155,6 +155,11 @@ struct FixedCosts {
 // L2-flushed benchmark measures at 80.5 us against 82.1 us for half-width
 // items.)
 constexpr FixedCosts kFixed = {16.0, 6.7, 2.0, 9.0, 22.7, 5.9};
+// Once per launch of a CTA-pair (cluster) kernel: measured with the L2 flushed
+// before every step, 256^3 runs in 14.3 us on CTA pairs against 12.5-12.7 us
+// on single CTAs with the same number of SMs and the same division (about 6.7
+// steps of 0.27 us); the fit above, over larger shapes, could not see it.
+constexpr double kPairLaunch = 6.7;
 // The transposed product (M <= 64, HBM-bound) keeps the constants of an
 // earlier fit over its own shapes: 5 per item, 3.4 per half item, and a
 // reduction of 8 + 30 * BN / 256 + 2 * s.
@@ -210,6 +215,7 @@ Choice choose(const gemm_plan* plan, int64_t M, int64_t N, int64_t K, gemm_dtype
     bool any = false;
     auto consider = [&](double cost, int kind, int splits, int64_t dp, bool halves, int64_t tiles, int64_t units,
                         bool early = false, bool stream_k = false, bool pair = false) {
+        if (!swap && kCfgCtas[kind] == 2) cost += kPairLaunch;
         // a pinned division (gemm_plan_force_division) admits only its own kind of candidate
         const int division = pair       ? GEMM_DIVISION_PAIR_SPLIT
                              : halves   ? GEMM_DIVISION_HALVES

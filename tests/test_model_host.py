@@ -37,6 +37,17 @@ def test_benchmark_workloads():
         "tc2cta_256x256_acc32_outbf16_esplitk2 ")
 
 
+def test_small_problems_take_single_cta_tiles():
+    # a CTA-pair launch costs about 1.8 us more than a one-CTA launch (measured
+    # with the L2 flushed: 256^3 14.3-14.9 against 12.5-13.6 us on the same
+    # number of SMs), so problems of a few tiles run on single CTAs
+    for shape in ((256, 256, 256), (512, 512, 512), (1024, 1024, 256)):
+        assert model("f16", *shape).startswith("tc1cta_128x256_acc32_out32_nhalves "), shape
+    # with more tiles, or deep K, the pairs' cheaper K steps win
+    assert model("bf16", 2048, 2048, 2048, "row", "row", "f32", "bf16").startswith("tc2cta_256x256_")
+    assert model("f16", 8192, 8192, 8192).startswith("tc2cta_256x256_acc32_out32_esplitk2 ")
+
+
 def test_rules():
     # fp16 accumulation is never split
     for shape in ((1024, 1024, 16384), (4096, 4096, 4096), (300, 300, 8192)):
