@@ -338,6 +338,28 @@ def pin_k_zero(lib):
     assert np.array_equal(D.astype(np.float64), 2 * C)
 
 
+def pin_k_zero_signed_zero(lib):
+    """K = 0 with beta = 0: the empty sum is +0 and D = alpha * r[i] * c[j] * (+0),
+    whose sign is the product of the signs (IEEE 754 multiplication); adding
+    beta * C = +0 gives +0 (IEEE 754: -0 + +0 = +0 in round to nearest)."""
+    empty = np.zeros(0, np.uint16)
+    f32 = lambda D: D.view(np.uint32)
+    neg0, pos0 = np.uint32(0x80000000), np.uint32(0)
+    D = oracle.gemm("f16", empty, empty, None, 2, 3, 0, 1, 3, 3, "row", "row", "f32", -1.0, 0.0, lib=lib)
+    assert np.all(f32(D) == neg0)
+    D = oracle.gemm("f16", empty, empty, None, 2, 3, 0, 1, 3, 3, "row", "row", "f32", 2.0, 0.0, lib=lib)
+    assert np.all(f32(D) == pos0)
+    rs = np.array([1.0, -1.0], np.float32)
+    D = oracle.gemm("f16", empty, empty, None, 2, 3, 0, 1, 3, 3, "row", "row", "f32", -1.0, 0.0, lib=lib,
+                    row_scale=rs)
+    assert np.all(f32(D[0]) == neg0) and np.all(f32(D[1]) == pos0)
+    C = np.zeros((2, 3), np.float32)
+    D = oracle.gemm("f16", empty, empty, C, 2, 3, 0, 1, 3, 3, "row", "row", "f32", -1.0, 0.5, lib=lib)
+    assert np.all(f32(D) == pos0)
+    Dh = oracle.gemm("f16", empty, empty, None, 2, 3, 0, 1, 3, 3, "row", "row", "bf16", -1.0, 0.0, lib=lib)
+    assert np.all(Dh == np.uint16(0x8000))
+
+
 def pin_bf16_inputs(lib):
     rng = np.random.default_rng(16)
     A = _int_matrix(rng, 16, 32)

@@ -24,6 +24,9 @@ MUTANTS = {
     "C_ld_ignored": ("i * g->ldc + j", "i * g->N + j"),
     "beta_dropped": ("v += g->beta * c;", "v += 0.0 * c;"),
     "alpha_dropped": ("double v = g->alpha * acc;", "double v = acc;"),
+    # K = 0 taken as D = beta * C alone (alpha not applied to the empty sum):
+    # loses the sign of alpha * (+0)
+    "empty_sum_unscaled": ("double v = g->alpha * acc;", "double v = g->K ? g->alpha * acc : 0.0;"),
     "sign_flipped": ("acc += p;", "acc -= p;"),
     "k_off_by_one": ("k < g->K; ++k", "k < g->K - 1; ++k"),
     "k_starts_at_one": ("int64_t k = 0; k < g->K", "int64_t k = 1; k < g->K"),
