@@ -359,6 +359,31 @@ gemm_status_t gemm_describe_model(int sm_count, gemm_dtype_t in_dtype, int64_t M
                                   gemm_dtype_t accum_dtype, gemm_dtype_t out_dtype,
                                   char *buf, int64_t len);
 
+/* The work the model's choice gives one unit of the persistent tile
+ * scheduler, without touching any device (for tests and for planning): the
+ * problem and the device are as for gemm_describe_model, `division` /
+ * `division_splits` pin a division as gemm_plan_force_division does
+ * (GEMM_DIVISION_AUTO and 0: the model's).  A unit is a persistent CTA, a CTA
+ * pair, or (GEMM_DIVISION_PAIR_SPLIT) the cluster of two CTAs of one tile,
+ * whose two items are the CTAs' K halves.  Writes *n_units (the units the
+ * launch runs) and *n_items (the unit's items, in the order it runs them),
+ * and the first min(*n_items, max_items) items to `items` (host memory owned
+ * by the caller), 9 ints each: tile, tile row, tile column (of the product
+ * the kernel computes: transposed when M <= 64), first and end 64-deep K
+ * block (128-byte K blocks for the 8-bit and tf32 operand kinds), column half
+ * (-1 whole width, 0 or 1), role (0 whole, 1 split with a last-arriver
+ * reduction, 2 early partial, 3 owner of early partials, 4 half of a CTA-pair
+ * split), split index, split count.  M, N or K = 0 give no units.
+ * GEMM_ERR_INVALID_ARG for the arguments gemm_describe_model rejects, a
+ * division outside the enum, splits outside 0..16, a unit outside
+ * 0..*n_units-1 or a null output; GEMM_ERR_UNSUPPORTED when the pinned
+ * division does not fit the problem. */
+gemm_status_t gemm_schedule_model(int sm_count, gemm_dtype_t in_dtype, int64_t M, int64_t N, int64_t K,
+                                  gemm_layout_t layoutA, gemm_layout_t layoutB,
+                                  gemm_dtype_t accum_dtype, gemm_dtype_t out_dtype,
+                                  gemm_division_t division, int division_splits, int unit,
+                                  int32_t *items, int max_items, int *n_items, int *n_units);
+
 /* gemm_run for callers that cannot allocate device memory.  The paper has no
  * counterpart to this entry point: its kernels need no workspace at all.
  *

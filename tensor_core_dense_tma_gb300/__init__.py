@@ -33,7 +33,7 @@ __all__ = [
     "gemm_plan_sm_count", "gemm_plan_describe", "gemm_plan_destroy", "gemm_status_string",
     "gemm_plan_force_config", "CONFIG", "gemm_run_static_scratch", "gemm_plan_autotune",
     "gemm_plan_clear_tuning", "gemm_plan_tuned_count", "gemm_plan_force_division", "DIVISION",
-    "gemm_run_prior_art", "PRIOR_ART", "gemm_mma_fragment_map", "run_prior_art", "gemm_describe_model",
+    "gemm_run_prior_art", "PRIOR_ART", "gemm_mma_fragment_map", "run_prior_art", "gemm_describe_model", "gemm_schedule_model",
     "gemm_plan_device_status_async", "gemm_plan_tensor_map_stats", "gemm_static_scratch_device_status",
     "gemm_plan_host_trace", "gemm_plan_host_trace_read",
 ]
@@ -109,6 +109,10 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.gemm_plan_autotune.restype = i32
     lib.gemm_describe_model.argtypes = [i32, i32, i64, i64, i64, i32, i32, i32, i32, ctypes.c_char_p, i64]
     lib.gemm_describe_model.restype = i32
+    lib.gemm_schedule_model.argtypes = [i32, i32, i64, i64, i64, i32, i32, i32, i32, i32, i32, i32,
+                                        ctypes.POINTER(ctypes.c_int32), i32, ctypes.POINTER(ctypes.c_int),
+                                        ctypes.POINTER(ctypes.c_int)]
+    lib.gemm_schedule_model.restype = i32
     lib.gemm_run_host.argtypes = [p, p, p, p, p, i64, i64, i64, i64, i64, i64, i32, i32, i32, i32, f32, f32,
                                   ctypes.POINTER(Epilogue), p]
     lib.gemm_run_host.restype = i32
@@ -337,6 +341,30 @@ def gemm_describe_model(sm_count: int, in_dtype: str, M, N, K, layoutA="row", la
     if st != 0:
         raise GemmError(st, "gemm_describe_model")
     return buf.value.decode()
+
+
+SCHEDULE_FIELDS = ("tile", "tile_row", "tile_col", "kb0", "kb1", "half", "role", "split", "nsplit")
+
+
+def gemm_schedule_model(sm_count: int, in_dtype: str, M, N, K, layoutA="row", layoutB="row",
+                        accum_dtype="f32", out_dtype="f32", division: str | int = "auto", splits: int = 0,
+                        unit: int = 0):
+    """(number of units, the items unit `unit` runs) for the cost model's choice
+    on a device with `sm_count` SMs (no GPU needed); each item a dict of
+    SCHEDULE_FIELDS."""
+    lib = load()
+    n_items, n_units = ctypes.c_int(0), ctypes.c_int(0)
+    args = (sm_count, DTYPE[in_dtype], M, N, K, LAYOUT[layoutA], LAYOUT[layoutB], DTYPE[accum_dtype],
+            DTYPE[out_dtype], DIVISION[division] if isinstance(division, str) else division, splits, unit)
+    st = lib.gemm_schedule_model(*args, None, 0, ctypes.byref(n_items), ctypes.byref(n_units))
+    if st != 0:
+        raise GemmError(st, "gemm_schedule_model")
+    buf = (ctypes.c_int32 * (9 * max(1, n_items.value)))()
+    st = lib.gemm_schedule_model(*args, buf, n_items.value, ctypes.byref(n_items), ctypes.byref(n_units))
+    if st != 0:
+        raise GemmError(st, "gemm_schedule_model")
+    items = [dict(zip(SCHEDULE_FIELDS, buf[9 * i:9 * i + 9])) for i in range(n_items.value)]
+    return n_units.value, items
 
 
 def gemm_plan_destroy(plan) -> int:

@@ -878,6 +878,62 @@ gemm_status_t gemm_describe_model(int sm_count, gemm_dtype_t in_dtype, int64_t M
     return describe_impl(&model, M, N, K, layoutA, layoutB, accum_dtype, out_dtype, buf, len);
 }
 
+gemm_status_t gemm_schedule_model(int sm_count, gemm_dtype_t in_dtype, int64_t M, int64_t N, int64_t K,
+                                  gemm_layout_t layoutA, gemm_layout_t layoutB, gemm_dtype_t accum_dtype,
+                                  gemm_dtype_t out_dtype, gemm_division_t division, int division_splits, int unit,
+                                  int32_t* items, int max_items, int* n_items, int* n_units) {
+    if (sm_count < 2 || sm_count > 4096 || !valid_dtype(in_dtype) || in_dtype == GEMM_F32 || !n_items || !n_units ||
+        max_items < 0 || (max_items > 0 && !items) || static_cast<int>(division) < GEMM_DIVISION_AUTO ||
+        static_cast<int>(division) > GEMM_DIVISION_PAIR_SPLIT || division_splits < 0 || division_splits > kMaxSplits)
+        return GEMM_ERR_INVALID_ARG;
+    *n_items = 0;
+    *n_units = 0;
+    const int64_t lda = layoutA == GEMM_ROW_MAJOR ? K : M, ldb = layoutB == GEMM_ROW_MAJOR ? N : K;
+    const int64_t pad = 16 / dtype_bytes(in_dtype);
+    gemm_status_t st = validate(in_dtype, nullptr, nullptr, nullptr, nullptr, M, N, K,
+                                lda < pad ? pad : (lda + pad - 1) / pad * pad,
+                                ldb < pad ? pad : (ldb + pad - 1) / pad * pad, N, layoutA, layoutB, accum_dtype,
+                                out_dtype, 0.0f, false);
+    if (st != GEMM_OK) return st;
+    if (M == 0 || N == 0 || K == 0) return GEMM_OK;   // no tile kernel runs
+    gemm_plan model;   // never touches a device, as in gemm_describe_model
+    model.sm_count = sm_count;
+    model.in_dtype = in_dtype;
+    model.ws_bytes = kWorkspaceBytes;
+    model.flags_ready = true;
+    model.forced_division = static_cast<int>(division);
+    model.forced_division_splits = division_splits;
+    bool valid = true;
+    const Choice ch = select_choice(&model, M, N, K, layoutA, layoutB, accum_dtype, out_dtype, &valid, nullptr);
+    if (!valid) return GEMM_ERR_UNSUPPORTED;
+    const int tn = kCfgTileN[ch.kind];
+    const ScheduleShape sh{kCfgTileM[ch.kind], tn, static_cast<int>(k_block(in_dtype)), kCfgHalves[ch.kind], tn >= 32,
+                           kCfgCtas[ch.kind] == 1 && tn <= 64};
+    tcdt::KernelParams p{};
+    bool pair = false;
+    const int units = fill_schedule(p, ch, ch.swap ? N : M, ch.swap ? M : N, K, sh, true, &pair);
+    *n_units = units;
+    if (unit < 0 || unit >= units) return GEMM_ERR_INVALID_ARG;
+    const int count = pair ? 2 * tcdt::pair_items(p, unit) : tcdt::unit_items(p, unit, units);
+    *n_items = count;
+    for (int i = 0; i < count && i < max_items; ++i) {
+        const tcdt::WorkItem x = pair ? tcdt::pair_item(p, unit, i) : tcdt::unit_item(p, unit, units, i);
+        int mb = 0, nb = 0;
+        tcdt::tile_coords(p, x.tile, mb, nb);
+        int32_t* o = items + 9 * static_cast<int64_t>(i);
+        o[0] = x.tile;
+        o[1] = mb;
+        o[2] = nb;
+        o[3] = x.kb0;
+        o[4] = x.kb1;
+        o[5] = x.half;
+        o[6] = x.role;
+        o[7] = x.split;
+        o[8] = x.nsplit;
+    }
+    return GEMM_OK;
+}
+
 }  // extern "C"
 
 namespace {

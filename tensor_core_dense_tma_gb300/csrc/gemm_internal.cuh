@@ -302,6 +302,47 @@ gemm_status_t prepare(gemm_plan* plan, int kind, int slot) {
     return GEMM_OK;
 }
 
+// The tile scheduler's fields of the kernel parameters for a chosen
+// configuration and division (the product the kernel computes is M x N x K),
+// and the number of units -- persistent CTAs, CTA pairs, or with `pair` one
+// cluster of two CTAs per tile -- the launch runs.  The launch and
+// gemm_schedule_model both build them here, so the schedule that call lists
+// is the one a launch runs.
+struct ScheduleShape {
+    int tile_m, tile_n, bk;
+    bool halves_ok;   // tiles can run as two half-width items
+    bool w32;         // whole 32-column epilogue chunks (early partials need them)
+    bool pair_ok;     // a transposed one-CTA tile that can split its K across a CTA pair
+};
+
+inline int fill_schedule(KernelParams& p, const Choice& ch, int64_t M, int64_t N, int64_t K, const ScheduleShape& sh,
+                         bool flags_ready, bool* pair_out) {
+    const bool n_halves = ch.n_halves && sh.halves_ok && ch.splits == 1;
+    const bool pair = ch.pair_split && sh.pair_ok;
+    p.num_m_blocks = static_cast<int32_t>((M + sh.tile_m - 1) / sh.tile_m);
+    p.num_n_blocks = static_cast<int32_t>((N + sh.tile_n - 1) / sh.tile_n);
+    p.num_k_blocks = static_cast<int32_t>((K + sh.bk - 1) / sh.bk);
+    p.num_tiles = p.num_m_blocks * p.num_n_blocks;
+    p.splits = ch.splits;
+    p.n_halves = n_halves ? 1 : 0;
+    p.dp_tiles = static_cast<int32_t>((ch.splits > 1 || n_halves) ? ch.dp_tiles : p.num_tiles);
+    // raster bands of 16 tile-rows (4096 rows with 256-row tiles): measured
+    // against 4, 8, 24 and 32, 4096^3 is ~1 % faster than with 8 and the
+    // 8192^3 and larger shapes within their power-capped noise
+    p.group_m = 16;
+    p.early = (ch.early && ch.splits > 1 && flags_ready && sh.w32) ? 1 : 0;
+    p.stream_k = (p.early && ch.stream_k) ? 1 : 0;
+    p.pair_split = pair ? 1 : 0;
+    if (pair) {
+        p.splits = 2;
+        p.dp_tiles = 0;
+    }
+    *pair_out = pair;
+    if (pair) return p.num_tiles;
+    const int64_t work = p.dp_tiles + static_cast<int64_t>(p.num_tiles - p.dp_tiles) * (n_halves ? 2 : p.splits);
+    return work < ch.units ? static_cast<int>(work) : ch.units;
+}
+
 template <class Cfg, bool EP = false>
 gemm_status_t launch_tc(gemm_plan* plan, const Choice& ch, const Problem& pr, const void* C, void* D,
                         int64_t ldc, float alpha, float beta, gemm_dtype_t out_dtype, cudaStream_t stream) {
@@ -353,17 +394,10 @@ gemm_status_t launch_tc(gemm_plan* plan, const Choice& ch, const Problem& pr, co
     p.M = static_cast<int32_t>(pr.M);
     p.N = static_cast<int32_t>(pr.N);
     p.K = static_cast<int32_t>(pr.K);
-    p.num_m_blocks = static_cast<int32_t>((pr.M + Cfg::UMMA_M - 1) / Cfg::UMMA_M);
-    p.num_n_blocks = static_cast<int32_t>((pr.N + Cfg::BN - 1) / Cfg::BN);
-    p.num_k_blocks = static_cast<int32_t>((pr.K + Cfg::BK - 1) / Cfg::BK);
-    p.num_tiles = p.num_m_blocks * p.num_n_blocks;
-    p.splits = ch.splits;
-    p.n_halves = n_halves ? 1 : 0;
-    p.dp_tiles = static_cast<int32_t>((ch.splits > 1 || n_halves) ? ch.dp_tiles : p.num_tiles);
-    // raster bands of 16 tile-rows (4096 rows with 256-row tiles): measured
-    // against 4, 8, 24 and 32, 4096^3 is ~1 % faster than with 8 and the
-    // 8192^3 and larger shapes within their power-capped noise
-    p.group_m = 16;
+    bool pair_launch = false;
+    const int units = fill_schedule(p, ch, pr.M, pr.N, pr.K,
+                                    {Cfg::UMMA_M, Cfg::BN, Cfg::BK, Cfg::HALVES_OK, Cfg::W == 32, Cfg::CG == 1 && Cfg::BN <= 64},
+                                    plan->d_flags != nullptr, &pair_launch);
     p.ldc = ldc;
     p.C = C;
     p.D = D;
@@ -385,13 +419,6 @@ gemm_status_t launch_tc(gemm_plan* plan, const Choice& ch, const Problem& pr, co
     p.ep = (pr.act || pr.rs_row || pr.cs_col || pr.bias_row || pr.bias_col) ? 1u : 0u;
     p.ws = plan->d_ws;
     p.counters = plan->d_counters;
-    p.early = (ch.early && ch.splits > 1 && plan->d_flags && Cfg::W == 32) ? 1 : 0;
-    p.stream_k = (p.early && ch.stream_k) ? 1 : 0;
-    p.pair_split = pair ? 1 : 0;
-    if (pair) {
-        p.splits = 2;
-        p.dp_tiles = 0;
-    }
     {
         const uint32_t e = static_cast<uint32_t>(plan->launches + 1);
         p.epoch = e == 0u ? 1u : e;
@@ -406,10 +433,8 @@ gemm_status_t launch_tc(gemm_plan* plan, const Choice& ch, const Problem& pr, co
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[1];
     fill_launch_config<Cfg>(cfg, attr, stream);
-    const int64_t work = p.dp_tiles + static_cast<int64_t>(p.num_tiles - p.dp_tiles) * (n_halves ? 2 : p.splits);
-    const int units = work < ch.units ? static_cast<int>(work) : ch.units;
     cfg.gridDim = dim3(Cfg::CG * units, 1, 1);
-    if (pair) {
+    if (pair_launch) {
         // one cluster of two CTAs per tile (the plan offers this only when the
         // tiles fit one wave of pairs)
         attr[0].id = cudaLaunchAttributeClusterDimension;

@@ -163,7 +163,7 @@ struct TileConfig {
 
 // Grouped raster: tiles run down a band of `group_m` m-blocks before moving
 // to the next n-block, so concurrently running CTAs share B panels in L2.
-__device__ __forceinline__ void tile_coords(const KernelParams& p, int tile, int& mb, int& nb) {
+__host__ __device__ __forceinline__ void tile_coords(const KernelParams& p, int tile, int& mb, int& nb) {
     const int per_group = p.group_m * p.num_n_blocks;
     const int g = tile / per_group;
     const int first_m = g * p.group_m;
@@ -204,11 +204,11 @@ struct WorkItem {
     int role;
 };
 
-__device__ __forceinline__ int num_work_items(const KernelParams& p) {
+__host__ __device__ __forceinline__ int num_work_items(const KernelParams& p) {
     return p.dp_tiles + (p.num_tiles - p.dp_tiles) * (p.n_halves ? 2 : p.splits);
 }
 
-__device__ __forceinline__ WorkItem work_item(const KernelParams& p, int w) {
+__host__ __device__ __forceinline__ WorkItem work_item(const KernelParams& p, int w) {
     WorkItem x;
     x.half = -1;
     x.role = kRoleWhole;
@@ -263,12 +263,12 @@ struct StreamRange {
     int64_t s, e;   // K blocks of the unit's range, counted from tile dp_tiles
 };
 
-__device__ __forceinline__ StreamRange stream_range(const KernelParams& p, int unit, int units) {
+__host__ __device__ __forceinline__ StreamRange stream_range(const KernelParams& p, int unit, int units) {
     const int64_t w = static_cast<int64_t>(p.num_tiles - p.dp_tiles) * p.num_k_blocks;
     return {w * unit / units, w * (unit + 1) / units};
 }
 
-__device__ __forceinline__ int unit_items(const KernelParams& p, int unit, int units) {
+__host__ __device__ __forceinline__ int unit_items(const KernelParams& p, int unit, int units) {
     if (p.stream_k) {
         const StreamRange r = stream_range(p, unit, units);
         const int kb = p.num_k_blocks;
@@ -283,7 +283,7 @@ __device__ __forceinline__ int unit_items(const KernelParams& p, int unit, int u
     return whole + (unit < (p.num_tiles - p.dp_tiles) * p.splits ? 1 : 0);
 }
 
-__device__ __forceinline__ WorkItem unit_item(const KernelParams& p, int unit, int units, int i) {
+__host__ __device__ __forceinline__ WorkItem unit_item(const KernelParams& p, int unit, int units, int i) {
     if (p.stream_k) {
         const int whole = p.dp_tiles / units;
         if (i < whole) return work_item(p, unit + i * units);
@@ -333,9 +333,9 @@ __device__ __forceinline__ WorkItem unit_item(const KernelParams& p, int unit, i
 // pair_split: cluster u (a pair of CTAs) computes tile u; CTA `prank` of the
 // pair takes K blocks [prank * kb / 2, (prank + 1) * kb / 2).  There are at
 // most as many tiles as pairs, so a pair has one item (or none).
-__device__ __forceinline__ int pair_items(const KernelParams& p, int unit) { return unit < p.num_tiles ? 1 : 0; }
+__host__ __device__ __forceinline__ int pair_items(const KernelParams& p, int unit) { return unit < p.num_tiles ? 1 : 0; }
 
-__device__ __forceinline__ WorkItem pair_item(const KernelParams& p, int unit, int prank) {
+__host__ __device__ __forceinline__ WorkItem pair_item(const KernelParams& p, int unit, int prank) {
     WorkItem x;
     x.tile = unit;
     x.stile = -1;
